@@ -1,0 +1,350 @@
+"""Pins that tie the scalar oracle to facts fixed outside the oracle itself.
+
+Each ``pin_*`` function takes an oracle library handle (``None`` = the real
+oracle) and raises AssertionError when the oracle disagrees with:
+  * a hand-derived worked example (tests/golden/w12_worked_example.txt);
+  * a closed form (brute force over all 65536 BF16 patterns, constructed rows);
+  * the definition of losslessness (bit-exact round trip);
+  * a library routine (numpy float64 matmul) or exact integer arithmetic;
+  * the figures the pages print (escape fraction, bits per weight).
+The same functions run against deliberately broken copies of the oracle in
+test_oracle_mutants.py, which is how we know the pins can fail.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle as O
+import workloads as WL
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden_example():
+    rows = {}
+    with open(os.path.join(GOLDEN, "w12_worked_example.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            rows.setdefault(key, []).append(vals)
+    return rows
+
+
+def _blob_arrays(blob: bytes, N: int, K: int):
+    b = np.frombuffer(blob, dtype=np.uint8)
+    n_esc = int(b[24:32].view(np.uint64)[0])
+    T = int(b[32:40].view(np.uint64)[0])
+    brow = 4 * ((K + 7) // 8)
+    off = 40
+    ebase = b[off:off + N]
+    off += N
+    ae = b[off:off + N * K].reshape(N, K)
+    off += N * K
+    bpl = b[off:off + N * brow].reshape(N, brow)
+    off += N * brow
+    tptr = b[off:off + 4 * (T + 1)].view("<u4")
+    off += 4 * (T + 1)
+    esc = b[off:off + 4 * n_esc].view("<u4")
+    return ebase, ae, bpl, tptr, esc
+
+
+# ---- hand-derived worked example -------------------------------------------
+
+def pin_worked_example(lib=None):
+    g = _golden_example()
+    N, K = int(g["N"][0][0]), int(g["K"][0][0])
+    W = np.array([[int(v, 16) for v in r] for r in g["W"]], dtype=np.uint16)
+    blob = O.encode(W, lib=lib)
+    assert len(blob) == int(g["BLOBLEN"][0][0]), "blob length"
+    assert blob[:4] == b"W12\x00"
+    ebase, ae, bpl, tptr, esc = _blob_arrays(blob, N, K)
+    assert list(ebase) == [int(v) for v in g["EBASE"][0]], "ebase"
+    want_ae = np.array([[int(v, 16) for v in r] for r in g["AE"]], dtype=np.uint8)
+    assert np.array_equal(ae, want_ae), "AE plane"
+    words = bpl.view("<u4").reshape(N, -1)
+    want_w = [int(r[0], 16) for r in g["BWORD"]]
+    assert [int(words[n, 0]) for n in range(N)] == want_w, "B plane"
+    assert [int(v) for v in tptr] == [int(v) for v in g["TILEPTR"][0]], "tile_ptr"
+    assert [int(v) for v in esc] == [int(v, 16) for v in g["ESC"][0]], "escapes"
+    dec = O.decode(blob, lib=lib)
+    assert np.array_equal(dec, W), "lossless decode"
+    q8 = O.decode_q8(blob, lib=lib)
+    want_q8 = np.array([[int(v, 16) for v in r] for r in g["Q8"]], dtype=np.uint16)
+    assert np.array_equal(q8, want_q8), "Q8 view"
+
+
+# ---- closed forms ------------------------------------------------------------
+
+def pin_all_patterns(lib=None, seed=7):
+    """One channel holding every BF16 pattern once: ebase 239, 4096 in window."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    row = rng.permutation(np.arange(65536, dtype=np.uint32)).astype(np.uint16)[None, :]
+    blob = O.encode(row, lib=lib)
+    N, K, n_esc, T = O.blob_header(blob, lib=lib)
+    assert (N, K) == (1, 65536)
+    assert T == 256
+    ebase, ae, bpl, tptr, esc = _blob_arrays(blob, 1, 65536)
+    assert int(ebase[0]) == 239, int(ebase[0])
+    # 16 binades x 2 signs x 128 mantissas in the window
+    assert n_esc == 65536 - 4096, n_esc
+    assert np.array_equal(O.decode(blob, lib=lib), row)
+    # every escape entry carries the exact original pattern at its position
+    k_of = np.empty(65536, dtype=np.int64)
+    k_of[row[0].astype(np.int64)] = np.arange(65536)
+    for t in range(T):
+        for i in range(int(tptr[t]), int(tptr[t + 1])):
+            e = int(esc[i])
+            k = t * 256 + ((e >> 16) & 0xFF)
+            assert (e >> 24) == 0
+            assert int(row[0, k]) == (e & 0xFFFF)
+
+
+def pin_constructed_rows(lib=None):
+    # (a) every pattern with exponent 0..16: emax 16 -> ebase 1; only the 256
+    #     e = 0 patterns (+-0 and subnormals) escape
+    pats = np.array([(s << 15) | (e << 7) | m for s in (0, 1) for e in range(17)
+                     for m in range(128)], dtype=np.uint16)[None, :]
+    blob = O.encode(pats, lib=lib)
+    _, _, n_esc, _ = O.blob_header(blob, lib=lib)
+    ebase = _blob_arrays(blob, 1, pats.shape[1])[0]
+    assert int(ebase[0]) == 1 and n_esc == 256, (int(ebase[0]), n_esc)
+    assert np.array_equal(O.decode(blob, lib=lib), pats)
+    # (b) a row of zeros: no finite normal -> ebase 1, all escape
+    z = np.zeros((3, 40), dtype=np.uint16)
+    z[1] = 0x8000
+    blob = O.encode(z, lib=lib)
+    _, _, n_esc, _ = O.blob_header(blob, lib=lib)
+    assert n_esc == 120 and list(_blob_arrays(blob, 3, 40)[0]) == [1, 1, 1]
+    assert np.array_equal(O.decode(blob, lib=lib), z)
+    # (c) +-Inf and NaN never set the window; they escape with payload kept
+    r = np.full((1, 16), 0x3F80, dtype=np.uint16)  # 1.0, e = 127
+    r[0, 3] = 0x7F80
+    r[0, 5] = 0xFF80
+    r[0, 9] = 0x7FC3
+    blob = O.encode(r, lib=lib)
+    _, _, n_esc, _ = O.blob_header(blob, lib=lib)
+    assert int(_blob_arrays(blob, 1, 16)[0][0]) == 112 and n_esc == 3
+    assert np.array_equal(O.decode(blob, lib=lib), r)
+    # (d) window edges: emax 20 -> ebase 5; e = 5 is in, e = 4 escapes
+    r = np.array([[(20 << 7), (5 << 7) | 0x7F, (4 << 7) | 0x7F, 0x8000 | (19 << 7)]],
+                 dtype=np.uint16)
+    blob = O.encode(r, lib=lib)
+    ebase, ae, _, _, esc = _blob_arrays(blob, 1, 4)
+    assert int(ebase[0]) == 5
+    assert [int(v) for v in esc] == [(2 << 16) | int(r[0, 2])]
+    assert int(ae[0, 1]) == ((0x7F >> 4) << 4) | 0  # A = top mantissa bits, E = 0
+    assert int(ae[0, 3]) == ((8 | 0) << 4) | 14     # negative, E = 19 - 5
+    # (e) the largest finite exponent 254 sets ebase 239 exactly
+    r = np.array([[0x7F7F, 0x3F80, (239 << 7), (238 << 7)]], dtype=np.uint16)
+    blob = O.encode(r, lib=lib)
+    ebase, _, _, _, esc = _blob_arrays(blob, 1, 4)
+    assert int(ebase[0]) == 239 and len(esc) == 2
+
+
+def pin_roundtrip(lib=None):
+    """Lossless: decode(encode(W)) == W bit for bit, shapes with ragged tiles."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    cases = [
+        WL.tiny_weights(1)[0],
+        WL.projection_weights(300, 777, seed=3, outlier_frac=3e-3),
+        WL.heavy_weights(129, 520, seed=4),
+        rng.integers(0, 65536, size=(130, 259), dtype=np.uint16),  # any pattern
+        np.zeros((0, 16), dtype=np.uint16),
+        np.zeros((5, 0), dtype=np.uint16),
+        WL.normal_rows(1, 1, seed=5),
+    ]
+    for W in cases:
+        blob = O.encode(W, lib=lib)
+        N, K, _, T = O.blob_header(blob, lib=lib)
+        assert (N, K) == W.shape
+        assert T == (-(-N // 128)) * (-(-K // 256))
+        assert np.array_equal(O.decode(blob, lib=lib), W), W.shape
+        if N >= 2:
+            part = O.decode_rows(blob, 1, N - 1, lib=lib)
+            assert np.array_equal(part, W[1:N - 1])
+
+
+def pin_escape_list_structure(lib=None):
+    """Escape entries: sorted and unique per tile, positions hold placeholders."""
+    W = WL.heavy_weights(300, 700, seed=9)
+    blob = O.encode(W, lib=lib)
+    N, K, n_esc, T = O.blob_header(blob, lib=lib)
+    ebase, ae, bpl, tptr, esc = _blob_arrays(blob, N, K)
+    assert tptr[0] == 0 and tptr[-1] == n_esc
+    tiles_c = -(-K // 256)
+    seen = np.zeros((N, K), dtype=bool)
+    for t in range(T):
+        seg = esc[int(tptr[t]):int(tptr[t + 1])]
+        assert np.all(np.diff(seg.astype(np.int64)) > 0)
+        for e in seg:
+            e = int(e)
+            n = (t // tiles_c) * 128 + (e >> 24)
+            k = (t % tiles_c) * 256 + ((e >> 16) & 0xFF)
+            assert n < N and k < K
+            seen[n, k] = True
+            s = (int(W[n, k]) >> 15) & 1
+            assert int(ae[n, k]) == (s << 7), "placeholder A = s<<3, E = 0"
+    # every weight that is not an escape is in its row's window
+    e = (W.astype(np.int32) >> 7) & 0xFF
+    inwin = (e >= 1) & (e <= 254) & (e >= ebase[:, None]) & (e <= ebase[:, None].astype(np.int32) + 15)
+    assert np.array_equal(~inwin, seen)
+
+
+# ---- the 8-bit view ------------------------------------------------------------
+
+def pin_q8_nesting(lib=None):
+    """Q8 = the weight with its low four mantissa bits cleared (in window);
+    escaped slots read +-2^(ebase-127); the AE byte is the record's top byte."""
+    W = WL.projection_weights(256, 512, seed=21, outlier_frac=2e-3)
+    blob = O.encode(W, lib=lib)
+    N, K, _, _ = O.blob_header(blob, lib=lib)
+    ebase, ae, bpl, _, _ = _blob_arrays(blob, N, K)
+    q8 = O.decode_q8(blob, lib=lib)
+    e = (W.astype(np.int32) >> 7) & 0xFF
+    inwin = (e >= 1) & (e <= 254) & (e >= ebase[:, None]) & (e <= ebase[:, None].astype(np.int32) + 15)
+    assert np.array_equal(q8[inwin], W[inwin] & 0xFFF0)
+    s = W.astype(np.int32) >> 15
+    ph = (s << 15) | (ebase[:, None].astype(np.int32) << 7)
+    assert np.array_equal(q8[~inwin].astype(np.int32), ph[~inwin])
+    # the value the Q pass sees is A+E only: the full decode differs from it
+    # exactly in the low four mantissa bits of in-window weights
+    full = O.decode(blob, lib=lib)
+    assert np.array_equal(full[inwin] & 0xFFF0, q8[inwin])
+    assert np.array_equal((full[inwin] & 0xF), (W[inwin] & 0xF))
+
+
+# ---- GEMM ----------------------------------------------------------------------
+
+def pin_gemm_numpy(lib=None):
+    """fp64 reference against numpy's float64 matmul of the decoded matrix."""
+    W = WL.projection_weights(200, 300, seed=5, outlier_frac=1e-3)
+    x = WL.activations(5, 300, seed=6)
+    y = O.gemm(x, W, lib=lib)
+    xf = WL.bf16_bits_to_f32(x).astype(np.float64)
+    wf = WL.bf16_bits_to_f32(W).astype(np.float64)
+    ref = xf @ wf.T
+    scale = np.abs(xf) @ np.abs(wf).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * scale + 1e-300)
+    s = O.abs_gemm(x, W, lib=lib)
+    assert np.allclose(s, scale, rtol=1e-12, atol=0)
+    # rows computed block-wise agree with the full call
+    blk = O.gemm_rows(x, W[17:40], lib=lib)
+    assert np.array_equal(blk, y[:, 17:40])
+
+
+def pin_gemm_one_hot(lib=None):
+    """x = unit rows e_k: y[m][n] is exactly W[n][k] (any finite W)."""
+    W = WL.heavy_weights(64, 96, seed=13)
+    W[0, :] = np.arange(96, dtype=np.uint16) | 0x0001  # subnormals
+    K = W.shape[1]
+    for k0 in (0, 37, 95):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k0] = 0x3F80  # 1.0
+        y = O.gemm(x, W, lib=lib)
+        assert np.array_equal(y[0], WL.bf16_bits_to_f32(W[:, k0]).astype(np.float64))
+
+
+def pin_gemm_exact_integers(lib=None):
+    """All-ones x and W of powers of two: sums are exact integers."""
+    rng = np.random.Generator(np.random.PCG64(17))
+    N, K = 40, 200
+    ex = rng.integers(-4, 6, size=(N, K))
+    sg = rng.integers(0, 2, size=(N, K))
+    W = ((sg << 15) | ((127 + ex) << 7)).astype(np.uint16)
+    x = np.full((2, K), 0x3F80, dtype=np.uint16)
+    x[1, ::2] = 0xBF80  # -1 on even k
+    y = O.gemm(x, W, lib=lib)
+    for n in range(N):
+        v = [Fraction(-1 if sg[n, k] else 1) * Fraction(2) ** int(ex[n, k]) for k in range(K)]
+        assert y[0, n] == float(sum(v))
+        assert y[1, n] == float(sum(-v[k] if k % 2 == 0 else v[k] for k in range(K)))
+
+
+# ---- the printed figures -------------------------------------------------------
+
+def printed_figures():
+    out = {}
+    with open(os.path.join(GOLDEN, "printed_figures.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                out[k] = float(v)
+    return out
+
+
+def expected_escape_fraction(K: int, sigma0: float = 0.02, n_scale: int = 400) -> float:
+    """Analytic escape probability of one weight for rows W ~ N(0, (sigma0 c)^2),
+    c ~ U(0.5, 2), with the window anchored at the row maximum's binade.
+
+    A weight escapes iff |w| < 2^(j-15) where 2^j <= max|row| < 2^(j+1); since
+    such a weight cannot be the maximum, P = sum_j F(2^(j-15)) *
+    [F(2^(j+1))^(K-1) - F(2^j)^(K-1)] with F(t) = erf(t / (sigma sqrt 2)).
+    """
+    from scipy.special import erf
+
+    j = np.arange(-40, 8, dtype=np.float64)
+    acc = 0.0
+    cs = 0.5 + 1.5 * (np.arange(n_scale) + 0.5) / n_scale
+    for c in cs:
+        sig = sigma0 * c
+
+        def F(t):
+            return erf(t / (sig * np.sqrt(2.0)))
+
+        p = F(2.0 ** (j - 15)) * (F(2.0 ** (j + 1)) ** (K - 1) - F(2.0 ** j) ** (K - 1))
+        acc += p.sum()
+    return acc / len(cs)
+
+
+def pin_escape_fraction(lib=None, N=2048, K=5120, seed=31):
+    """Normal weights: the oracle's escape fraction matches the analytic value
+    for the max-anchored window and lands near the pages' 7.3e-5."""
+    W = WL.normal_rows(N, K, seed=seed)
+    blob = O.encode(W, lib=lib)
+    _, _, n_esc, _ = O.blob_header(blob, lib=lib)
+    frac = n_esc / (N * K)
+    # per-row escape counts -> a standard error that includes the row-level
+    # correlation through the shared maximum
+    ebase = _blob_arrays(blob, N, K)[0].astype(np.int32)
+    e = (W.astype(np.int32) >> 7) & 0xFF
+    per_row = ((e < ebase[:, None]) | (e == 0)).sum(axis=1) / K
+    se = per_row.std(ddof=1) / np.sqrt(N)
+    ana = expected_escape_fraction(K)
+    assert abs(frac - ana) <= 5 * se + 0.03 * ana, (frac, ana, se)
+    fig = printed_figures()["escape_fraction"]
+    assert abs(frac - fig) <= 0.15 * fig, (frac, fig)
+    return frac, ana
+
+
+def pin_bits_per_weight(lib=None):
+    """Storage: 12 bits + escapes + metadata, within the pages' 12.01-12.02."""
+    N, K = 1024, 5120
+    W = WL.normal_rows(N, K, seed=41)
+    blob = O.encode(W, lib=lib)
+    _, _, n_esc, T = O.blob_header(blob, lib=lib)
+    bpw = 8 * len(blob) / (N * K)
+    fig = printed_figures()
+    assert 12.0 < bpw <= fig["bits_per_weight_max"], bpw
+    # the size is fixed by the layout: 12 bits + 8/K (ebase) + tile pointers + escapes
+    want = 40 + N + N * K + N * 4 * ((K + 7) // 8) + 4 * (T + 1) + 4 * n_esc
+    assert len(blob) == want
+    return bpw
+
+
+FAST_PINS = (
+    pin_worked_example,
+    pin_all_patterns,
+    pin_constructed_rows,
+    pin_roundtrip,
+    pin_escape_list_structure,
+    pin_q8_nesting,
+    pin_gemm_numpy,
+    pin_gemm_one_hot,
+    pin_gemm_exact_integers,
+)
