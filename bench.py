@@ -1,0 +1,495 @@
+"""W12 skinny-GEMM benchmark: weight-GB/s and fraction of the HBM roofline.
+
+Workload (default): the M = 1 single-row decode projections of one dense layer
+with hidden 5120 / intermediate 17408 / 8 KV heads of 128 -- q 5120x5120,
+k 1024x5120, v 1024x5120, o 5120x5120, gate 17408x5120, up 17408x5120,
+down 5120x17408 -- with W ~ N(0, 0.02^2) x per-row U(0.5, 2) and 1e-4
+Student-t(2) x 0.5 outliers, x ~ N(0, 1).  One step = the 7 W12 GEMMs of one
+layer; steps rotate over several independently drawn layers, each ~0.5 GB of
+W12 data, so every step streams its weights from HBM (inputs > L2).
+
+Prints one JSON line (rank 0).  `--impl reference` times the scalar CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "W12 GEMM weight-GB/s and % of GB300 HBM roofline at M=1/32/64; µs per layer"
+WORKLOAD = ("single-row decode projections, M=1: q/o 5120x5120, k/v 1024x5120, gate/up "
+            "17408x5120, down 5120x17408 (one dense layer; N(0,0.02^2) x U(0.5,2) rows, "
+            "1e-4 Student-t(2)x0.5 outliers)")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_fma.cu", "kernels.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "lossless_bit_weight_skinny_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", f"{name}.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_sha") != _kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:7], float(parts[7])))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[3] > 0] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(loaded), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def _make_layers(w12, torch, n_layers, seed0=1000):
+    """Draw, encode and upload `n_layers` layers; returns [[(name, Dev, stats)]]."""
+    layers = []
+    for li in range(n_layers):
+        projs = []
+        for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
+            wb = WL.projection_weights_torch(N, K, seed=seed0 + 16 * li + pi)
+            host = wb.cpu().numpy().view(np.uint16)
+            del wb
+            h = w12.w12_encode(host)
+            st = h.stats()
+            d = w12.w12_upload(h)
+            torch.cuda.synchronize()
+            projs.append((name, d, st))
+        layers.append(projs)
+    return layers
+
+
+def _step_bytes(layer, M):
+    """Algorithmic bytes of one step: W12 arrays (incl. metadata) + x + y."""
+    tot = 0
+    for name, d, st in layer:
+        tot += st["bytes_total"] - 40 + 2 * M * d.K + 4 * M * d.N
+    return tot
+
+
+def run_w12(args):
+    import torch
+
+    from lossless_bit_weight_skinny_gb300 import build as b
+
+    b.build()
+    import lossless_bit_weight_skinny_gb300 as w12
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+
+    layers = _make_layers(w12, torch, args.layers)
+    M = 1
+    xs = {}
+    ys = {}
+    for name, N, K in WL.LAYER_PROJECTIONS:
+        xs[name] = torch.from_numpy(WL.activations(M, K, seed=7).view(np.int16)).cuda().view(torch.bfloat16)
+        ys[name] = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    n_proj = len(WL.LAYER_PROJECTIONS)
+
+    def step(i, ev=None):
+        layer = layers[i % len(layers)]
+        for j, (name, d, st) in enumerate(layer):
+            if ev is not None:
+                ev[j][0].record(stream)
+            w12.w12_gemm(xs[name], d, ys[name], stream)
+            if ev is not None:
+                ev[j][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    for layer in layers:
+        for _, d, _ in layer:
+            assert w12.w12_dev_status(d) == 0
+
+    # one CUDA graph holds G steps (rotating over the layers) with an event
+    # pair around every GEMM launch; the timed region replays it
+    G = args.graph_steps
+    try:
+        evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                for _ in range(n_proj)] for _ in range(G)]
+    except TypeError:
+        evs = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            step(i, evs[i] if evs else None)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // G)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.25)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    clocks = sampler.stop()
+    args.steps = reps * G
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    for layer in layers:
+        for _, d, _ in layer:
+            assert w12.w12_dev_status(d) == 0, "device status after timing"
+
+    step_bytes = _step_bytes(layers[0], M)
+    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    # per-launch durations of the dominant kernel (the M = 1 CUDA-core GEMM),
+    # from the event pairs of the last replay inside the timed region
+    kern_ms = 0.0
+    kern_bytes = 0
+    per_proj = {}
+    for i in range(G):
+        layer = layers[i % len(layers)]
+        for j, (name, d, st) in enumerate(layer):
+            bts = st["bytes_total"] - 40 + 2 * M * d.K + 4 * M * d.N
+            dt = evs[i][j][0].elapsed_time(evs[i][j][1]) if evs else None
+            if dt is None:
+                continue
+            kern_ms += dt
+            kern_bytes += bts
+            p = per_proj.setdefault(name, [0.0, 0, bts])
+            p[0] += dt
+            p[1] += 1
+    if not evs:  # no timing events in graphs: bound the kernel time by the step time
+        kern_ms, kern_bytes = ms, step_bytes * args.steps
+    peak, peak_kind = _peaks()
+    achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
+    n_launch = args.steps * n_proj
+    traffic = _traffic("gemm_fma_m1")
+
+    # the same layer at M = 32 and M = 64 (tensor-core path), shorter runs
+    by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
+    for Mx in (32, 64):
+        xm = {n: torch.from_numpy(WL.activations(Mx, K, seed=9).view(np.int16)).cuda().view(torch.bfloat16)
+              for n, N, K in WL.LAYER_PROJECTIONS}
+        ym = {n: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
+
+        def stepm(i):
+            for name, d, st in layers[i % len(layers)]:
+                w12.w12_gemm(xm[name], d, ym[name], stream)
+
+        for i in range(max(3, args.warmup // 4)):
+            stepm(i)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nsteps = max(10, args.steps // 4)
+        s0.record(stream)
+        for i in range(nsteps):
+            stepm(i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        msm = s0.elapsed_time(s1)
+        for layer in layers:
+            for _, d, _ in layer:
+                assert w12.w12_dev_status(d) == 0
+        bm = _step_bytes(layers[0], Mx)
+        by_m[str(Mx)] = {"weight_GBps": round(bm * nsteps / (msm * 1e-3) / 1e9, 1),
+                         "us_per_layer": round(1e3 * msm / nsteps, 2)}
+
+    # end to end through the host-buffer entry point: pinned x in, y out, per step
+    xh = {n: torch.from_numpy(WL.activations(M, K, seed=7).view(np.int16)).pin_memory()
+          for n, N, K in WL.LAYER_PROJECTIONS}
+    yh = {n: torch.empty((M, N), dtype=torch.float32).pin_memory() for n, N, K in WL.LAYER_PROJECTIONS}
+    xd = {n: torch.empty((M, K), dtype=torch.int16, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
+
+    def step_e2e(i):
+        for name, d, st in layers[i % len(layers)]:
+            w12.w12_gemm_host(xh[name], xd[name], d, ys[name], yh[name], stream)
+
+    for i in range(args.warmup):
+        step_e2e(i)
+    torch.cuda.synchronize()
+    e_steps = max(10, args.steps // 2)
+    tw = time.perf_counter()
+    for i in range(e_steps):
+        step_e2e(i)
+    torch.cuda.synchronize()
+    e_s = time.perf_counter() - tw
+    h2d = sum(2 * M * K for _, N, K in WL.LAYER_PROJECTIONS)
+    d2h = sum(4 * M * N for _, N, K in WL.LAYER_PROJECTIONS)
+    e2e = {"value": round(world * step_bytes * e_steps / e_s / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "us_per_layer": round(1e6 * e_s / e_steps, 2)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        st_all = [st for _, _, st in layers[0]]
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 5),
+            "us_per_layer": round(1e3 * ms / args.steps, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16 weights (W12) x bf16 activations, fp32 accumulate",
+            "data": "synthetic",
+            "config": {
+                "workload": WORKLOAD,
+                "M": M,
+                "layers_rotated": args.layers,
+                "step": "7 GEMMs (q,k,v,o,gate,up,down) of one layer",
+                "bytes_per_step": step_bytes,
+                "l2": "inputs larger than L2: each step streams ~0.5 GB of W12 weights",
+                "escape_fraction": round(sum(s["n_escapes"] for s in st_all)
+                                         / sum(s["N"] * s["K"] for s in st_all), 7),
+                "bits_per_weight": round(8 * sum(s["bytes_total"] for s in st_all)
+                                         / sum(s["N"] * s["K"] for s in st_all), 4),
+                "parallelism": f"replicas x{world}",
+            },
+            "by_M": by_m,
+            "per_projection_us": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "gemm_fma_kernel<1,false> (M=1)",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "frac_of_8TBps": round(achieved / 8000.0, 4),
+            },
+            "e2e": e2e,
+            "gpu_launches": n_launch,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------------
+# the scalar CPU oracle (reference arm and CPU baseline)
+# ---------------------------------------------------------------------------------------
+
+def _oracle_sample(rows_frac: int, seed0=1000):
+    """Per projection: the first N/rows_frac rows, encoded by the oracle."""
+    import oracle as O
+
+    out = []
+    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
+        R = max(1, N // rows_frac)
+        W = WL.projection_weights(R, K, seed=seed0 + pi)
+        blob = O.encode(W)
+        x = WL.activations(1, K, seed=7)
+        out.append((name, R, K, blob, x, len(blob) - 40 + 2 * K + 4 * R))
+    return out
+
+
+def _oracle_pass(sample, threads):
+    """Decode + float64 GEMM of every sampled projection, rows split over threads."""
+    import concurrent.futures as cf
+
+    import oracle as O
+
+    def job(item):
+        name, R, K, blob, x, _ = item
+        W = O.decode(blob)
+        return O.gemm(x, W)
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(job, sample))
+
+
+def cpu_baseline(seconds_budget: float):
+    """The oracle as it stands, timed on this host's cores on a bounded sample."""
+    import oracle as O
+
+    O.build()
+    cores = len(os.sched_getaffinity(0))
+    threads = min(cores, len(WL.LAYER_PROJECTIONS))
+    frac = 16
+    sample = _oracle_sample(frac)
+    t = time.perf_counter()
+    _oracle_pass(sample, threads)
+    dt = time.perf_counter() - t
+    reps = max(1, int(seconds_budget / max(dt, 1e-3)))
+    reps = min(reps, 20)
+    t = time.perf_counter()
+    for _ in range(reps):
+        _oracle_pass(sample, threads)
+    dt = (time.perf_counter() - t) / reps
+    nbytes = sum(s[5] for s in sample)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"first 1/{frac} of the rows of each of the 7 projections of one layer, "
+                      f"M=1: oracle decode + float64 GEMM, projections in parallel threads, "
+                      f"{reps} reps; host has {cores} cores"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as O
+
+    O.build()
+    cores = len(os.sched_getaffinity(0))
+    threads = min(cores, len(WL.LAYER_PROJECTIONS))
+    frac = 64
+    sample = _oracle_sample(frac)
+    for _ in range(args.warmup):
+        _oracle_pass(sample, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_pass(sample, threads)
+    dt = time.perf_counter() - t
+    nbytes = sum(s[5] for s in sample) * args.steps
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 weights (W12) x bf16 activations, fp64 accumulate",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1,
+                   "sample": f"first 1/{frac} of the rows of each projection per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first 1/{frac} of the rows of each of the 7 projections, "
+                                   "oracle decode + float64 GEMM per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
+    ap.add_argument("--layers", type=int, default=3)
+    ap.add_argument("--graph-steps", type=int, default=12)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_w12(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * w12.h -- C ABI of the W12 library: lossless 12-bit storage of BF16 weights
+ * and the skinny-M GEMM (1..64 activation rows) that decodes it on the fly on
+ * one GB300 GPU (sm_103a).
+ *
+ * Sources (pages about "SpecPilot: Autonomous Algorithm Discovery and Systems
+ * Optimization for Speculative Decoding"):
+ *   [F5a] thelatestinai.com page, Figure 5(a) caption -- the format: per BF16
+ *         weight three 4-bit planes A (sign + top three mantissa bits), E
+ *         (exponent offset in a 16-binade window per output channel) and B
+ *         (low mantissa bits); weights outside the window go to an exact
+ *         escape list; A and E form the 8-bit view read by the Q pass.
+ *   [F5b] same page, Figure 5(b) caption -- the GEMM decodes W12 records on
+ *         the fly and feeds the tensor cores.
+ *   [F7]  same page, Figure 7 caption -- the Q pass reads the 8-bit view
+ *         nested in each W12 record.
+ *   [MF]  ai.info "AI summary" page, Main Findings -- "W12 compression"
+ *         (lossless, 12.01-12.02 bits/weight, 7.3e-5 escapes) and "W12 works
+ *         beyond speculation" (the W12 GEMM against cuBLAS at 1 and 32 rows).
+ *   [KC3] ai.info page, Key Contributions 3 -- the zero-copy Q pass.
+ *
+ * Conventions shared by every call:
+ *   - W is [N][K] row-major BF16 (raw 16-bit patterns): row n = output
+ *     channel n.  x is [M][K] row-major BF16, y is [M][N] row-major FP32,
+ *     y = x . W^T.
+ *   - Layout of an encoded matrix: AE byte = A<<4|E per weight, B packed 8 weights per little-endian 32-bit word (evens in
+ *     nibble slots 0..3, odds in 4..7), window = 16 binades ending at the
+ *     row's largest finite normal exponent, escapes grouped by 128 x 256 tile
+ *     as (row%128)<<24 | (k%256)<<16 | bits, sorted inside each tile.
+ *   - Errors are returned as w12_status; no call aborts or throws.  Device
+ *     calls are asynchronous on the given stream and never synchronise,
+ *     except w12_dev_status.
+ *   - Streams are CUDA runtime streams (cudaStream_t); NULL = legacy default.
+ *   - Host-side objects are opaque and owned by the library; free them with
+ *     the matching *_free call.  Caller-provided buffers stay caller-owned.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *w12_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    W12_OK = 0,
+    W12_ERR_INVALID_ARG = 1, /* NULL pointer or negative size               */
+    W12_ERR_SHAPE = 2,       /* N/K disagree with the encoded matrix         */
+    W12_ERR_ALIGNMENT = 3,   /* a device buffer is not 16-byte aligned       */
+    W12_ERR_UNSUPPORTED = 4, /* M outside 1..64, K % 32 != 0 for the GEMM    */
+    W12_ERR_OOM = 5,         /* host or device allocation failed             */
+    W12_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed            */
+    W12_ERR_CORRUPT = 7,     /* an encoded matrix breaks a format invariant  */
+    W12_ERR_TIMEOUT = 8,     /* a kernel gave up waiting (device status)     */
+    W12_ERR_IO = 9           /* file could not be read or written            */
+} w12_status;
+
+typedef struct w12_host w12_host; /* encoded matrix in host memory   */
+typedef struct w12_dev w12_dev;   /* encoded matrix in device memory */
+
+typedef struct {
+    int64_t N, K;
+    int64_t n_escapes;
+    int64_t n_tiles;              /* 128 x 256 escape tiles               */
+    int64_t max_escapes_per_tile;
+    double bits_per_weight;       /* 8 * blob bytes / (N K), incl. header */
+    double escape_fraction;       /* n_escapes / (N K)                    */
+    size_t bytes_total;           /* blob bytes (header + all arrays)     */
+    size_t bytes_ae, bytes_b;     /* the two plane arrays                 */
+} w12_stats;
+
+/* Human-readable name of a status code (static string). */
+const char *w12_status_string(w12_status s);
+
+/* ---- host side ------------------------------------------------------------ */
+
+/*
+ * Encode W[N][K] (host, row-major BF16 bit patterns) into W12 [F5a], losslessly
+ * [MF].  N, K >= 0 (empty matrices are valid).  n_threads: worker threads, 0 =
+ * all hardware threads.  Synchronous, host-only; *out receives a new handle.
+ * Errors: INVALID_ARG (NULL, negative size), OOM.
+ */
+w12_status w12_encode(const uint16_t *w_bf16, int64_t N, int64_t K, int n_threads,
+                      w12_host **out);
+
+void w12_host_free(w12_host *h);
+
+/* Storage statistics of an encoded matrix [MF "W12 compression"]. */
+w12_status w12_host_stats(const w12_host *h, w12_stats *out);
+
+/*
+ * Borrow the arrays of an encoded matrix (valid until w12_host_free):
+ * ebase[N] (window base per row), ae[N*K] (A<<4|E bytes), b[N*brow] with
+ * brow = 4*ceil(K/8), tile_ptr[T+1], esc[n_escapes].  Any output may be NULL.
+ */
+w12_status w12_host_view(const w12_host *h, const uint8_t **ebase, const uint8_t **ae,
+                         const uint8_t **b, const uint32_t **tile_ptr, const uint32_t **esc);
+
+/* Check every invariant of the format; W12_ERR_CORRUPT on the first breach. */
+w12_status w12_validate(const w12_host *h);
+
+/*
+ * Serialise into the portable blob ("W12\0", version 1, N, K, n_esc, T, then
+ * ebase, AE, B, tile_ptr, escapes; little-endian).  buf == NULL queries the
+ * size into *len.  Errors: INVALID_ARG (cap too small).
+ */
+w12_status w12_serialize(const w12_host *h, uint8_t *buf, size_t cap, size_t *len);
+
+/* Parse and validate a blob into a new host handle (CORRUPT if malformed). */
+w12_status w12_deserialize(const uint8_t *buf, size_t len, w12_host **out);
+
+/* Blob + CRC-32 trailer to/from a file (IO, CORRUPT on a bad checksum). */
+w12_status w12_save(const w12_host *h, const char *path);
+w12_status w12_load(const char *path, w12_host **out);
+
+/* ---- device side ------------------------------------------------------------ */
+
+/*
+ * Copy an encoded matrix to the current CUDA device: one device allocation
+ * holding every array (256-byte aligned), filled by asynchronous copies on
+ * `stream` (the host handle must stay alive until the stream has passed
+ * them).  Errors: INVALID_ARG, OOM, CUDA.
+ */
+w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out);
+
+/* Free a device handle (synchronises with the device first). */
+void w12_dev_free(w12_dev *d);
+
+/* Shape and device-byte count of a device handle. */
+w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device_bytes);
+
+/*
+ * y[M][N] = x[M][K] . W^T with W decoded to exact BF16 on the fly [F5a, F5b]
+ * and FP32 accumulation.  x: device BF16 [M][K], 16-byte aligned; y: device
+ * FP32 [M][N], 16-byte aligned; both caller-owned.  1 <= M <= 64 (M = 0 is a
+ * no-op), N and K must equal the handle's; K % 32 == 0 (else UNSUPPORTED).
+ * Kernel choice is a function of M only: M <= 8 CUDA-core FMA with warp
+ * reductions, 9..64 tcgen05 tensor cores with TMEM accumulators.  Uses a
+ * library-owned workspace cached per (device, stream); the first call on a
+ * stream allocates it (stream-ordered), so make that first call outside any
+ * stream capture.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM,
+ * CUDA.  Device-side failures are reported by w12_dev_status.
+ */
+w12_status w12_gemm(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                     w12_stream_t stream);
+
+/*
+ * The Q pass [F7, KC3]: the same product over the nested 8-bit view only --
+ * each weight rebuilt from its A+E byte with B = 0 and escapes left as their
+ * placeholders.  Reads 1 byte per weight and nothing else of the matrix.
+ * Same arguments, limits and errors as w12_gemm.
+ */
+w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                           w12_stream_t stream);
+
+/*
+ * End-to-end form of w12_gemm for host-resident activations: copies
+ * x_host -> x_dev, runs w12_gemm into y_dev, copies y_dev -> y_host, all on
+ * `stream` (use pinned host memory for asynchronous copies).  Every buffer is
+ * caller-owned; nothing is allocated beyond w12_gemm's workspace.
+ */
+w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, float *y_dev,
+                         float *y_host, int M, int N, int K, w12_stream_t stream);
+
+/*
+ * Lossless decode on the device: out[N][K] BF16 bit patterns (device, caller
+ * owned, 16-byte aligned), bit-identical to the matrix that was encoded [MF].
+ */
+w12_status w12_decode(const w12_dev *w, uint16_t *w_bf16_out, w12_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the handle's device status word:
+ * W12_OK, W12_ERR_TIMEOUT (a kernel's bounded wait ran out; its output is
+ * invalid) or W12_ERR_CORRUPT (a kernel met metadata it could not use).
+ */
+w12_status w12_dev_status(const w12_dev *w, w12_stream_t stream);
+
+/* Release every cached GEMM workspace of the current device (synchronises). */
+w12_status w12_release_workspaces(void);
+
+/*
+ * Test hooks for the failure path.  w12_set_spin_limit: the wall-time limit in
+ * nanoseconds of every bounded device-side wait of later GEMM launches (0 =
+ * the default, 200 ms); a kernel whose wait runs out records W12_ERR_TIMEOUT
+ * in the handle's status word, stops waiting, lets its in-flight copies land
+ * and returns.  w12_debug_inject_stall(1): later GEMM launches also wait on a
+ * barrier that nothing ever signals, so they take that path on purpose.
+ */
+void w12_set_spin_limit(uint32_t limit_ns);
+void w12_debug_inject_stall(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

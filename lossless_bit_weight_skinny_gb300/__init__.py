@@ -1,0 +1,314 @@
+"""Python binding of the W12 library (lossless 12-bit BF16 weights + skinny GEMM).
+
+Argument marshalling only: every step of the encode, upload, decode and GEMM
+runs in ``_lib/libw12.so`` (host C++ and sm_103a CUDA kernels).  PyTorch is
+used for device memory and streams.  There is no fallback: if the library is
+missing or fails to load, importing this package raises ImportError.
+
+Function names mirror the C ABI in ``include/w12.h``:
+
+    h = w12_encode(w_bits)                 # host handle (CPU)
+    d = w12_upload(h)                      # device handle, current device/stream
+    y = w12_gemm(x, d)                     # x: cuda bf16 [M][K] -> y: cuda f32 [M][N]
+    y = w12_gemm_q8view(x, d)              # Q pass over the nested 8-bit view
+    w = w12_decode(d)                      # cuda int16 [N][K], bit-exact BF16 patterns
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libw12.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"W12 library not built: {LIB_PATH} is missing "
+        "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+try:
+    _lib = ctypes.CDLL(LIB_PATH)
+except OSError as e:  # pragma: no cover - load failure is fatal
+    raise ImportError(f"W12 library failed to load: {e}") from e
+
+W12_OK = 0
+STATUS_NAMES = {
+    0: "OK", 1: "INVALID_ARG", 2: "SHAPE", 3: "ALIGNMENT", 4: "UNSUPPORTED", 5: "OOM",
+    6: "CUDA", 7: "CORRUPT", 8: "TIMEOUT", 9: "IO",
+}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_ST = ctypes.c_int
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("n_escapes", ctypes.c_int64),
+        ("n_tiles", ctypes.c_int64), ("max_escapes_per_tile", ctypes.c_int64),
+        ("bits_per_weight", ctypes.c_double), ("escape_fraction", ctypes.c_double),
+        ("bytes_total", ctypes.c_size_t), ("bytes_ae", ctypes.c_size_t),
+        ("bytes_b", ctypes.c_size_t),
+    ]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+def _sig(name, args, res=_ST):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_sig("w12_status_string", [_ST], ctypes.c_char_p)
+_sig("w12_encode", [_P, _I64, _I64, _I, ctypes.POINTER(_P)])
+_sig("w12_host_free", [_P], None)
+_sig("w12_host_stats", [_P, ctypes.POINTER(Stats)])
+_sig("w12_host_view", [_P] + [ctypes.POINTER(_P)] * 5)
+_sig("w12_validate", [_P])
+_sig("w12_serialize", [_P, _P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)])
+_sig("w12_deserialize", [_P, ctypes.c_size_t, ctypes.POINTER(_P)])
+_sig("w12_save", [_P, ctypes.c_char_p])
+_sig("w12_load", [ctypes.c_char_p, ctypes.POINTER(_P)])
+_sig("w12_upload", [_P, _P, ctypes.POINTER(_P)])
+_sig("w12_dev_free", [_P], None)
+_sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
+_sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
+_sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
+_sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
+_sig("w12_decode", [_P, _P, _P])
+_sig("w12_dev_status", [_P, _P])
+_sig("w12_release_workspaces", [])
+_sig("w12_set_spin_limit", [ctypes.c_uint32], None)
+_sig("w12_debug_inject_stall", [_I], None)
+
+EXPORTED = (
+    "w12_status_string", "w12_encode", "w12_host_free", "w12_host_stats", "w12_host_view",
+    "w12_validate", "w12_serialize", "w12_deserialize", "w12_save", "w12_load", "w12_upload",
+    "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
+    "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
+    "w12_debug_inject_stall",
+)
+
+
+class W12Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.w12_status_string(status).decode()
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def _check(st: int, where: str):
+    if st != W12_OK:
+        raise W12Error(st, where)
+
+
+def _u16_host(w) -> np.ndarray:
+    """Host BF16 bit patterns as a contiguous uint16 numpy array."""
+    try:
+        import torch
+        if isinstance(w, torch.Tensor):
+            if w.is_cuda:
+                raise ValueError("w12_encode takes a host tensor")
+            if w.dtype == torch.bfloat16:
+                w = w.view(torch.int16)
+            w = w.contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(w)
+    if a.dtype in (np.int16,):
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16 or a.ndim != 2:
+        raise TypeError("expected a 2-D array of BF16 bit patterns (uint16/int16/bfloat16)")
+    return a
+
+
+class Host:
+    """An encoded matrix in host memory (owns a ``w12_host*``)."""
+
+    def __init__(self, ptr: int, N: int, K: int):
+        self._ptr = ptr
+        self.N, self.K = N, K
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def __del__(self):
+        if getattr(self, "_ptr", None):
+            _lib.w12_host_free(self._ptr)
+            self._ptr = None
+
+    def stats(self) -> dict:
+        s = Stats()
+        _check(_lib.w12_host_stats(self._ptr, ctypes.byref(s)), "w12_host_stats")
+        return s.as_dict()
+
+    def validate(self) -> int:
+        return _lib.w12_validate(self._ptr)
+
+    def view(self):
+        """(ebase, ae, b, tile_ptr, esc) as numpy arrays (copies)."""
+        ptrs = [_P() for _ in range(5)]
+        _check(_lib.w12_host_view(self._ptr, *[ctypes.byref(p) for p in ptrs]), "w12_host_view")
+        st = self.stats()
+        N, K = self.N, self.K
+        brow = 4 * ((K + 7) // 8)
+        sizes = [(N, np.uint8), (N * K, np.uint8), (N * brow, np.uint8),
+                 (st["n_tiles"] + 1, np.uint32), (st["n_escapes"], np.uint32)]
+        out = []
+        for p, (n, dt) in zip(ptrs, sizes):
+            if n == 0 or not p.value:
+                out.append(np.zeros(n, dtype=dt))
+            else:
+                buf = (ctypes.c_char * (n * np.dtype(dt).itemsize)).from_address(p.value)
+                out.append(np.frombuffer(buf, dtype=dt).copy())
+        ebase, ae, b, tptr, esc = out
+        return ebase, ae.reshape(N, K), b.reshape(N, brow), tptr, esc
+
+    def serialize(self) -> bytes:
+        n = ctypes.c_size_t()
+        _check(_lib.w12_serialize(self._ptr, None, 0, ctypes.byref(n)), "w12_serialize")
+        buf = ctypes.create_string_buffer(max(n.value, 1))
+        _check(_lib.w12_serialize(self._ptr, buf, n.value, ctypes.byref(n)), "w12_serialize")
+        return buf.raw[:n.value]
+
+    def save(self, path: str):
+        _check(_lib.w12_save(self._ptr, path.encode()), "w12_save")
+
+    def upload(self, stream=None) -> "Dev":
+        return w12_upload(self, stream)
+
+
+class Dev:
+    """An encoded matrix in device memory (owns a ``w12_dev*``)."""
+
+    def __init__(self, ptr: int, N: int, K: int, host: Host | None = None):
+        self._ptr = ptr
+        self.N, self.K = N, K
+        self._host = host  # keeps the source alive until the uploads have run
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def free(self):
+        if getattr(self, "_ptr", None):
+            _lib.w12_dev_free(self._ptr)
+            self._ptr = None
+
+    def __del__(self):
+        self.free()
+
+    def device_bytes(self) -> int:
+        n, k, b = _I64(), _I64(), ctypes.c_size_t()
+        _check(_lib.w12_dev_info(self._ptr, ctypes.byref(n), ctypes.byref(k), ctypes.byref(b)), "w12_dev_info")
+        return b.value
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---- the C ABI, one Python function per entry point -------------------------
+
+def w12_encode(w_bits, n_threads: int = 0) -> Host:
+    a = _u16_host(w_bits)
+    N, K = a.shape
+    out = _P()
+    _check(_lib.w12_encode(a.ctypes.data_as(_P), N, K, n_threads, ctypes.byref(out)), "w12_encode")
+    return Host(out.value, N, K)
+
+
+def w12_deserialize(blob: bytes) -> Host:
+    out = _P()
+    buf = ctypes.create_string_buffer(blob, len(blob))
+    _check(_lib.w12_deserialize(buf, len(blob), ctypes.byref(out)), "w12_deserialize")
+    h = Host(out.value, 0, 0)
+    st = h.stats()
+    h.N, h.K = st["N"], st["K"]
+    return h
+
+
+def w12_load(path: str) -> Host:
+    out = _P()
+    _check(_lib.w12_load(path.encode(), ctypes.byref(out)), "w12_load")
+    h = Host(out.value, 0, 0)
+    st = h.stats()
+    h.N, h.K = st["N"], st["K"]
+    return h
+
+
+def w12_upload(h: Host, stream=None) -> Dev:
+    out = _P()
+    _check(_lib.w12_upload(h.ptr, _stream_ptr(stream), ctypes.byref(out)), "w12_upload")
+    return Dev(out.value, h.N, h.K, host=h)
+
+
+def _gemm(fn, name, x, d: Dev, y=None, stream=None):
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, d.N), dtype=torch.float32, device=x.device)
+    _check(fn(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
+              _stream_ptr(stream)), name)
+    return y
+
+
+def w12_gemm(x, d: Dev, y=None, stream=None):
+    """y[M][N] = x[M][K] . W^T on the device (W decoded exactly on the fly)."""
+    return _gemm(_lib.w12_gemm, "w12_gemm", x, d, y, stream)
+
+
+def w12_gemm_q8view(x, d: Dev, y=None, stream=None):
+    """The Q pass: the same product over the 8-bit A+E view only."""
+    return _gemm(_lib.w12_gemm_q8view, "w12_gemm_q8view", x, d, y, stream)
+
+
+def w12_gemm_host(x_host, x_dev, d: Dev, y_dev, y_host, stream=None):
+    """H2D copy of x, GEMM, D2H copy of y, all on one stream (pinned buffers)."""
+    M, K = x_host.shape
+    _check(_lib.w12_gemm_host(ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(x_dev.data_ptr()),
+                              d.ptr, ctypes.c_void_p(y_dev.data_ptr()), ctypes.c_void_p(y_host.data_ptr()),
+                              M, d.N, K, _stream_ptr(stream)), "w12_gemm_host")
+    return y_host
+
+
+def w12_decode(d: Dev, out=None, stream=None):
+    """Bit-exact BF16 patterns [N][K] (int16 CUDA tensor)."""
+    import torch
+    if out is None:
+        out = torch.empty((d.N, d.K), dtype=torch.int16, device="cuda")
+    _check(_lib.w12_decode(d.ptr, ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)), "w12_decode")
+    return out
+
+
+def w12_dev_status(d: Dev, stream=None) -> int:
+    """Synchronise and return (then clear) the handle's device status code."""
+    return _lib.w12_dev_status(d.ptr, _stream_ptr(stream))
+
+
+def w12_release_workspaces():
+    _check(_lib.w12_release_workspaces(), "w12_release_workspaces")
+
+
+def w12_set_spin_limit(limit_ns: int):
+    _lib.w12_set_spin_limit(int(limit_ns))
+
+
+def w12_debug_inject_stall(on: bool):
+    _lib.w12_debug_inject_stall(1 if on else 0)
+
+
+def lib():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib

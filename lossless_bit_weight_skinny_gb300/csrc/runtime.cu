@@ -1,0 +1,389 @@
+// runtime.cu -- device side of the C ABI: upload of encoded matrices, TMA
+// descriptors, the per-stream GEMM workspace cache and kernel dispatch.
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <utility>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+#include "w12_internal.h"
+
+using namespace w12;
+
+namespace {
+
+std::atomic<uint64_t> g_limit_ns{200ull * 1000 * 1000}; // bounded waits: 200 ms
+std::atomic<int> g_inject_stall{0};
+
+// ---- TMA descriptor encoding through the driver entry point -----------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a row-major [rows][cols] array of `esize`-byte elements.
+bool make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols,
+               uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMap *tmap_of(w12_tmap &t) { return reinterpret_cast<CUtensorMap *>(&t); }
+const CUtensorMap *tmap_of(const w12_tmap &t) { return reinterpret_cast<const CUtensorMap *>(&t); }
+static_assert(sizeof(w12_tmap) == sizeof(CUtensorMap), "tensor map size");
+
+int sm_count(int dev)
+{
+    static int cache[64] = {0};
+    if (dev < 0 || dev >= 64)
+        return 148;
+    if (!cache[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = v > 0 ? v : 148;
+    }
+    return cache[dev];
+}
+
+// ---- workspace cache: one growable buffer per (device, stream) --------------
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+    uint32_t epoch = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+constexpr size_t kCounterBytes = 1 << 16; // room for 8192 row blocks
+
+// Returns partial-sum and counter pointers for a call that needs `part_bytes`
+// of partial sums, and this call's epoch.
+w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **partials,
+                         unsigned long long **counters, uint32_t *epoch)
+{
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace &w = g_ws[{dev, st}];
+    const size_t need = kCounterBytes + ((part_bytes + 255) & ~static_cast<size_t>(255));
+    if (w.bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return W12_ERR_UNSUPPORTED; // grow outside capture: make one call first
+        // first use: room for the largest call (M = 64, one CTA per SM), so a
+        // workspace never moves under a captured CUDA graph
+        const size_t most = kCounterBytes + sizeof(float) * 2 * static_cast<size_t>(sm_count(dev)) * 64 * 128;
+        const size_t grow = need < most ? most : need;
+        if (w.ptr)
+            cudaFreeAsync(w.ptr, st);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, grow, st) != cudaSuccess)
+            return W12_ERR_OOM;
+        if (cudaMemsetAsync(p, 0, kCounterBytes, st) != cudaSuccess)
+            return W12_ERR_CUDA;
+        w.ptr = p;
+        w.bytes = grow;
+    }
+    *counters = static_cast<unsigned long long *>(w.ptr);
+    *partials = reinterpret_cast<float *>(static_cast<char *>(w.ptr) + kCounterBytes);
+    if (++w.epoch == 0)
+        w.epoch = 1;
+    *epoch = w.epoch;
+    return W12_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, int K,
+                     cudaStream_t st, bool q8)
+{
+    if (!w || M < 0)
+        return W12_ERR_INVALID_ARG;
+    if (N != w->N || K != w->K)
+        return W12_ERR_SHAPE;
+    if (M > 64)
+        return W12_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return W12_OK;
+    if (!x || !y)
+        return W12_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y))
+        return W12_ERR_ALIGNMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (cur != w->device)
+        return W12_ERR_INVALID_ARG;
+    if (K == 0)
+        return cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st) == cudaSuccess
+                   ? W12_OK
+                   : W12_ERR_CUDA;
+    if (!w->gemm_ok)
+        return W12_ERR_UNSUPPORTED;
+
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    const bool tc = mt >= 16;
+    const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
+    const int kstep = tc ? kTcKStep : kFmaKStep;
+    GemmArgs a{};
+    a.ebase = w->ebase;
+    a.tile_ptr = w->tile_ptr;
+    a.esc = w->esc;
+    a.y = y;
+    a.status = w->status;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.tiles_c = static_cast<int>(w->tiles_c);
+    a.n_rowblk = static_cast<int>(ceil_div(N, rows_blk));
+    a.n_kstep = static_cast<int>(ceil_div(K, kstep));
+    const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
+    if (iters > (1ll << 30) || a.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
+        return W12_ERR_UNSUPPORTED;
+    a.total_iters = static_cast<int>(iters);
+    a.limit_ns = g_limit_ns.load();
+    a.inject_stall = g_inject_stall.load();
+    const int grid = static_cast<int>(std::min<int64_t>(sm_count(cur), iters));
+
+    const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
+    w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters, &a.epoch);
+    if (ws != W12_OK)
+        return ws;
+
+    CUtensorMap tmx;
+    const bool okx = tc ? make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, mt,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)
+                        : make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 256, mt,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!okx)
+        return W12_ERR_CUDA;
+    cudaError_t e;
+    if (tc)
+        e = launch_gemm_tc(mt, q8, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
+    else if (rows_blk == 128)
+        e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma128), tmap_of(w->tm_b_fma128), &tmx, grid, st);
+    else
+        e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma64), tmap_of(w->tm_b_fma64), &tmx, grid, st);
+    return e == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+} // namespace
+
+extern "C" {
+
+w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
+{
+    if (!h || !out)
+        return W12_ERR_INVALID_ARG;
+    *out = nullptr;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    w12_dev *d = new (std::nothrow) w12_dev;
+    if (!d)
+        return W12_ERR_OOM;
+    if (cudaGetDevice(&d->device) != cudaSuccess) {
+        delete d;
+        return W12_ERR_CUDA;
+    }
+    d->N = h->N;
+    d->K = h->K;
+    d->T = num_tiles(h->N, h->K);
+    d->n_esc = static_cast<int64_t>(h->esc.size());
+    d->brow = b_row_bytes(h->K);
+    d->tiles_c = ceil_div(h->K, kTileCols);
+    auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    const size_t s_status = 256, s_ebase = up(h->ebase.size()), s_ae = up(h->ae.size()),
+                 s_b = up(h->b.size()), s_ptr = up(4 * h->tile_ptr.size()), s_esc = up(4 * h->esc.size());
+    d->bytes = s_status + s_ebase + s_ae + s_b + s_ptr + s_esc;
+    if (cudaMalloc(&d->base, d->bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete d;
+        return W12_ERR_OOM;
+    }
+    char *p = static_cast<char *>(d->base);
+    d->status = reinterpret_cast<int *>(p);
+    p += s_status;
+    d->ebase = reinterpret_cast<uint8_t *>(p);
+    p += s_ebase;
+    d->ae = reinterpret_cast<uint8_t *>(p);
+    p += s_ae;
+    d->b = reinterpret_cast<uint8_t *>(p);
+    p += s_b;
+    d->tile_ptr = reinterpret_cast<uint32_t *>(p);
+    p += s_ptr;
+    d->esc = reinterpret_cast<uint32_t *>(p);
+    bool ok = cudaMemsetAsync(d->status, 0, 256, st) == cudaSuccess;
+    auto cp = [&](void *dst, const void *src, size_t n) {
+        if (n)
+            ok = ok && cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    cp(d->ebase, h->ebase.data(), h->ebase.size());
+    cp(d->ae, h->ae.data(), h->ae.size());
+    cp(d->b, h->b.data(), h->b.size());
+    cp(d->tile_ptr, h->tile_ptr.data(), 4 * h->tile_ptr.size());
+    cp(d->esc, h->esc.data(), 4 * h->esc.size());
+    if (!ok) {
+        cudaFree(d->base);
+        delete d;
+        return W12_ERR_CUDA;
+    }
+    // GEMM descriptors: rows of both planes must start on 16-byte boundaries
+    if (h->N > 0 && h->K >= 32 && h->K % 32 == 0) {
+        const uint64_t N = h->N, K = h->K;
+        const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        bool t = make_tmap(tmap_of(d->tm_ae_fma128), U8, 1, d->ae, K, N, 256, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_ae_fma64), U8, 1, d->ae, K, N, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_b_fma128), U8, 1, d->b, K / 2, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_b_fma64), U8, 1, d->b, K / 2, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_ae_tc), U8, 1, d->ae, K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        t = t && make_tmap(tmap_of(d->tm_b_tc), U8, 1, d->b, K / 2, N, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+        d->gemm_ok = t;
+    }
+    *out = d;
+    return W12_OK;
+}
+
+void w12_dev_free(w12_dev *d)
+{
+    if (!d)
+        return;
+    cudaDeviceSynchronize();
+    cudaFree(d->base);
+    delete d;
+}
+
+w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device_bytes)
+{
+    if (!d)
+        return W12_ERR_INVALID_ARG;
+    if (N)
+        *N = d->N;
+    if (K)
+        *K = d->K;
+    if (device_bytes)
+        *device_bytes = d->bytes;
+    return W12_OK;
+}
+
+w12_status w12_gemm(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                     w12_stream_t stream)
+{
+    return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                           w12_stream_t stream)
+{
+    return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, float *y_dev,
+                         float *y_host, int M, int N, int K, w12_stream_t stream)
+{
+    if (!w || M < 0 || N < 0 || K < 0)
+        return W12_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return W12_OK;
+    if (!x_host || !x_dev || !y_dev || !y_host)
+        return W12_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, sizeof(uint16_t) * static_cast<size_t>(M) * K,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return W12_ERR_CUDA;
+    const w12_status s = gemm_impl(x_dev, w, y_dev, M, N, K, st, false);
+    if (s != W12_OK)
+        return s;
+    if (cudaMemcpyAsync(y_host, y_dev, sizeof(float) * static_cast<size_t>(M) * N,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return W12_OK;
+}
+
+w12_status w12_decode(const w12_dev *w, uint16_t *out, w12_stream_t stream)
+{
+    if (!w || (!out && w->N * w->K > 0))
+        return W12_ERR_INVALID_ARG;
+    if (w->N * w->K == 0)
+        return W12_OK;
+    if (w->K % 8 == 0 && !aligned16(out))
+        return W12_ERR_ALIGNMENT;
+    return launch_decode(w->ebase, w->ae, w->b, w->tile_ptr, w->esc, out, w->N, w->K,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+w12_status w12_dev_status(const w12_dev *w, w12_stream_t stream)
+{
+    if (!w)
+        return W12_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (cudaMemcpy(&v, w->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (v != 0 && cudaMemset(w->status, 0, sizeof v) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return static_cast<w12_status>(v);
+}
+
+w12_status w12_release_workspaces(void)
+{
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return W12_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto it = g_ws.begin(); it != g_ws.end();) {
+        if (it->first.first == cur) {
+            if (it->second.ptr)
+                cudaFree(it->second.ptr);
+            it = g_ws.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    return W12_OK;
+}
+
+void w12_set_spin_limit(uint32_t limit_ns)
+{
+    g_limit_ns.store(limit_ns ? limit_ns : 200ull * 1000 * 1000);
+}
+
+void w12_debug_inject_stall(int on) { g_inject_stall.store(on ? 1 : 0); }
+
+} // extern "C"

@@ -1,0 +1,182 @@
+"""The library's host side against the oracle (CPU only, no GPU needed).
+
+The library encoder is separate code from the oracle's; its blob must be byte
+for byte the oracle's on every input.  Also: the C ABI exports every symbol
+include/w12.h declares, the validator rejects corrupted handles, and the file
+format round-trips.
+"""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def w12():
+    from lossless_bit_weight_skinny_gb300 import build as b
+
+    b.build()
+    import lossless_bit_weight_skinny_gb300 as m
+
+    return m
+
+
+def _cases():
+    rng = np.random.Generator(np.random.PCG64(5))
+    allpat = rng.permutation(np.arange(65536, dtype=np.uint32)).astype(np.uint16).reshape(2, 32768)
+    return {
+        "tiny": WL.tiny_weights(1)[0],
+        "ragged": WL.projection_weights(300, 777, seed=3, outlier_frac=3e-3),
+        "heavy": WL.heavy_weights(257, 1000, seed=4),
+        "random_bits": rng.integers(0, 65536, size=(131, 263), dtype=np.uint16),
+        "all_patterns": allpat,
+        "empty_rows": np.zeros((0, 64), dtype=np.uint16),
+        "empty_cols": np.zeros((7, 0), dtype=np.uint16),
+        "single": np.array([[0x3F80]], dtype=np.uint16),
+        "zeros": np.zeros((130, 300), dtype=np.uint16),
+        "k5120": WL.projection_weights(1024, 5120, seed=2),
+    }
+
+
+@pytest.mark.parametrize("name", list(_cases().keys()))
+def test_encoder_matches_oracle_bytes(w12, name):
+    W = _cases()[name]
+    blob = O.encode(W)
+    for threads in (1, 0):
+        h = w12.w12_encode(W, n_threads=threads)
+        assert h.validate() == 0
+        assert h.serialize() == blob
+    st = h.stats()
+    N, K, n_esc, T = O.blob_header(blob)
+    assert (st["N"], st["K"], st["n_escapes"], st["n_tiles"]) == (N, K, n_esc, T)
+    assert st["bytes_total"] == len(blob)
+
+
+def test_encoder_full_projection_shape(w12):
+    W = WL.projection_weights(5120, 5120, seed=2)
+    h = w12.w12_encode(W)
+    assert h.serialize() == O.encode(W)
+    st = h.stats()
+    assert 12.0 < st["bits_per_weight"] < 12.05
+
+
+def test_deserialize_roundtrip_and_view(w12):
+    W = WL.projection_weights(200, 512, seed=8, outlier_frac=2e-3)
+    blob = O.encode(W)
+    h = w12.w12_deserialize(blob)
+    assert h.serialize() == blob
+    ebase, ae, b, tptr, esc = h.view()
+    assert ae.shape == (200, 512) and b.shape == (200, 256)
+    assert tptr[-1] == esc.size
+
+
+def test_save_load(w12, tmp_path):
+    W = WL.heavy_weights(64, 96, seed=12)
+    h = w12.w12_encode(W)
+    p = str(tmp_path / "m.w12")
+    h.save(p)
+    h2 = w12.w12_load(p)
+    assert h2.serialize() == h.serialize()
+    raw = bytearray(open(p, "rb").read())
+    raw[100] ^= 0x40
+    open(p, "wb").write(bytes(raw))
+    with pytest.raises(w12.W12Error) as e:
+        w12.w12_load(p)
+    assert e.value.status == 7  # CORRUPT (checksum)
+
+
+def _corrupt(blob: bytes, N: int, K: int, what: str) -> bytes:
+    b = bytearray(blob)
+    n_esc = int.from_bytes(b[24:32], "little")
+    T = int.from_bytes(b[32:40], "little")
+    brow = 4 * ((K + 7) // 8)
+    off_eb = 40
+    off_ae = off_eb + N
+    off_b = off_ae + N * K
+    off_ptr = off_b + N * brow
+    off_esc = off_ptr + 4 * (T + 1)
+    if what == "ebase_zero":
+        b[off_eb] = 0
+    elif what == "ebase_high":
+        b[off_eb + 1] = 240
+    elif what == "unsorted":
+        e0 = b[off_esc:off_esc + 4]
+        b[off_esc:off_esc + 4] = b[off_esc + 4:off_esc + 8]
+        b[off_esc + 4:off_esc + 8] = e0
+    elif what == "ptr":
+        v = int.from_bytes(b[off_ptr + 4:off_ptr + 8], "little") + 1
+        b[off_ptr + 4:off_ptr + 8] = v.to_bytes(4, "little")
+    elif what == "placeholder":
+        e = int.from_bytes(b[off_esc:off_esc + 4], "little")
+        n, k = e >> 24, (e >> 16) & 0xFF
+        b[off_ae + n * K + k] ^= 0x01
+    elif what == "in_window_escape":
+        # rewrite the first escape's bits to a value inside its row's window
+        e = int.from_bytes(b[off_esc:off_esc + 4], "little")
+        n = e >> 24
+        eb = b[off_eb + n]
+        e = (e & 0xFFFF0000) | ((eb + 3) << 7)
+        b[off_esc:off_esc + 4] = e.to_bytes(4, "little")
+    elif what == "truncated":
+        return bytes(b[:-4])
+    return bytes(b)
+
+
+@pytest.mark.parametrize("what", ["ebase_zero", "ebase_high", "unsorted", "ptr", "placeholder",
+                                  "in_window_escape", "truncated"])
+def test_validator_rejects_corruption(w12, what):
+    W = WL.projection_weights(64, 256, seed=21, outlier_frac=5e-3)
+    W[0, :3] = 0  # a few escapes in row 0
+    blob = O.encode(W)
+    bad = _corrupt(blob, 64, 256, what)
+    with pytest.raises(w12.W12Error) as e:
+        w12.w12_deserialize(bad)
+    assert e.value.status == 7
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "w12.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(w12_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(w12):
+    declared = _declared_functions()
+    assert len(declared) >= 18
+    out = subprocess.run(["nm", "-D", "--defined-only", w12.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(w12_\w+)", out))
+    missing = [n for n in declared if n not in exported]
+    assert not missing, missing
+    for n in declared:
+        assert hasattr(w12.lib(), n)
+    assert set(w12.EXPORTED) == set(declared)
+
+
+def test_invalid_arguments(w12):
+    import ctypes
+
+    lib = w12.lib()
+    out = ctypes.c_void_p()
+    assert lib.w12_encode(None, 4, 4, 0, ctypes.byref(out)) == 1
+    assert lib.w12_encode(None, -1, 4, 0, ctypes.byref(out)) == 1
+    assert lib.w12_validate(None) == 1
+    assert lib.w12_status_string(8) == b"device wait timed out"
+
+
+def test_no_oracle_on_product_path():
+    """The package and its C++/CUDA sources never reference the oracle."""
+    pkg = os.path.join(ROOT, "lossless_bit_weight_skinny_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
