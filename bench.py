@@ -151,9 +151,9 @@ def _step_bytes(layer, M):
 def run_w12(args):
     import torch
 
-    from lossless_bit_weight_skinny_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__._load_builder().build()
     import lossless_bit_weight_skinny_gb300 as w12
 
     rank = int(os.environ.get("RANK", "0"))

@@ -24,9 +24,9 @@ def w12():
 
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from lossless_bit_weight_skinny_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__._load_builder().build()
     import lossless_bit_weight_skinny_gb300 as m
 
     return m

@@ -20,9 +20,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="session")
 def w12():
-    from lossless_bit_weight_skinny_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__._load_builder().build()
     import lossless_bit_weight_skinny_gb300 as m
 
     return m
