@@ -167,6 +167,24 @@ w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, 
                          float *y_host, int M, int N, int K, w12_stream_t stream);
 
 /*
+ * w12_gemm without any device allocation, for callers that may not allocate:
+ * code whose host process hands all device memory to its own pool, plug-ins
+ * whose framework must own every allocation, loops that may not take the
+ * allocator's locks.  (The pages have no counterpart; this is a library
+ * convenience.)  Same arguments, result and errors as w12_gemm, but the
+ * split-K scratch comes from one fixed 16 MiB array in device memory that
+ * every GPU loading this library holds until exit; a call needing more
+ * (over 8192 row blocks, or a GPU too large for 2 * SMs * M * 128 partial
+ * sums) fails with W12_ERR_UNSUPPORTED.  All calls on a device share the
+ * array, so calls whose kernels overlap on the GPU (other streams, other
+ * threads) race: serialise them.  The first call on each device looks up the
+ * array, clears its counters and synchronises the device; make it before any
+ * stream capture.
+ */
+w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                            w12_stream_t stream);
+
+/*
  * Lossless decode on the device: out[N][K] BF16 bit patterns (device, caller
  * owned, 16-byte aligned), bit-identical to the matrix that was encoded [MF].
  */

@@ -80,6 +80,7 @@ _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POI
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
+_sig("w12_gemm_noalloc", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_decode", [_P, _P, _P])
 _sig("w12_dev_status", [_P, _P])
 _sig("w12_release_workspaces", [])
@@ -91,7 +92,7 @@ EXPORTED = (
     "w12_validate", "w12_serialize", "w12_deserialize", "w12_save", "w12_load", "w12_upload",
     "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
-    "w12_debug_inject_stall",
+    "w12_debug_inject_stall", "w12_gemm_noalloc",
 )
 
 
@@ -272,6 +273,12 @@ def w12_gemm(x, d: Dev, y=None, stream=None):
 def w12_gemm_q8view(x, d: Dev, y=None, stream=None):
     """The Q pass: the same product over the 8-bit A+E view only."""
     return _gemm(_lib.w12_gemm_q8view, "w12_gemm_q8view", x, d, y, stream)
+
+
+def w12_gemm_noalloc(x, d: Dev, y, stream=None):
+    """w12_gemm with its scratch in the library's fixed device array: no
+    device allocation at all (y must be given).  Overlapping calls race."""
+    return _gemm(_lib.w12_gemm_noalloc, "w12_gemm_noalloc", x, d, y, stream)
 
 
 def w12_gemm_host(x_host, x_dev, d: Dev, y_dev, y_host, stream=None):
