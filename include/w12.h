@@ -209,6 +209,10 @@ w12_status w12_release_workspaces(void);
  * barrier that nothing ever signals, so they take that path on purpose.
  */
 void w12_set_spin_limit(uint32_t limit_ns);
+
+/* Name of the last CUDA error behind a W12_ERR_CUDA from a GEMM launch on this
+ * host thread (static string; "no error" if none). */
+const char *w12_last_cuda_error(void);
 void w12_debug_inject_stall(int on);
 
 #ifdef __cplusplus

@@ -81,6 +81,7 @@ _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_noalloc", [_P, _P, _P, _I, _I, _I, _P])
+_sig("w12_last_cuda_error", [], ctypes.c_char_p)
 _sig("w12_decode", [_P, _P, _P])
 _sig("w12_dev_status", [_P, _P])
 _sig("w12_release_workspaces", [])
@@ -92,7 +93,7 @@ EXPORTED = (
     "w12_validate", "w12_serialize", "w12_deserialize", "w12_save", "w12_load", "w12_upload",
     "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
-    "w12_debug_inject_stall", "w12_gemm_noalloc",
+    "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error",
 )
 
 
@@ -100,6 +101,8 @@ class W12Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         msg = _lib.w12_status_string(status).decode()
+        if status == 6:
+            msg += ": " + _lib.w12_last_cuda_error().decode()
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({msg})")
 
 

@@ -9,23 +9,45 @@
 // one persistent CTA per SM (stream-K), and row blocks shared by several CTAs
 // are combined by the last contributor in a fixed order.
 //
-// CTA = 8 consumer warps + 1 producer warp.  The producer streams each
+// CTA = CW consumer warps + 1 producer warp.  The producer streams each
 // block's AE bytes, B words and x slice with TMA into a ring of shared-memory
-// stages, and copies the block's escape entries next to them with cp.async.
-// Consumer warp w owns RW rows of the block; lane l owns columns 8l..8l+7 of
-// the 256-column step and keeps the products of all its rows in registers
-// until the row block ends, then the warp reduces across lanes.
+// stages, and copies the tile's escape entries and row-group index next to
+// them with cp.async.  Consumer warp w owns RW rows of the block; lane l owns
+// columns 8l..8l+7 of the 256-column step and keeps the products of its rows
+// in registers until the row block ends, then the warp reduces across lanes.
+//
+// Escapes: the main loop multiplies every slot as decoded -- an escaped slot
+// holds the placeholder +-2^(ebase-127) -- and has no branches.  After each
+// step the warp walks its own escapes (a contiguous run of the tile's sorted
+// list) and accumulates, per output, the two exact-order correction sums
+// sum(-x * placeholder) and sum(x * exact value), added to the output in that
+// order at the end.  With a single non-zero product (one-hot x) this gives the
+// exact escaped value back, Inf/NaN escapes propagate, and otherwise the
+// result is the same sum in another order.
 #include "kernels.cuh"
 
 namespace w12 {
 namespace {
 
+#ifndef W12_FMA_CW
+#define W12_FMA_CW 8 // consumer warps of the M <= 4 kernels (8 or 16)
+#endif
+#ifndef W12_FMA_MIXED
+#define W12_FMA_MIXED 1 // M <= 2: BF16 x BF16 -> FP32 FMAs instead of packed FP32 FMAs
+#endif
+
 template <int MT>
 struct FmaShape {
-    static constexpr int RBLK = (MT <= 4) ? 128 : 64; // rows per block
-    static constexpr int CW = 8;                      // consumer warps
-    static constexpr int RW = RBLK / CW;              // rows per consumer warp
+    static constexpr int RBLK = (MT <= 4) ? 128 : 64;         // rows per block
+    static constexpr int CW = (MT <= 4) ? W12_FMA_CW : 8;     // consumer warps
+    static constexpr int RW = RBLK / CW;                      // rows per consumer warp
     static constexpr int THREADS = (CW + 1) * 32;
+    // registers per thread for one resident CTA: each of the 4 SM sub-partitions
+    // has 16K registers and holds ceil(warps / 4) of the CTA's warps
+    static constexpr int PER_SMSP = (CW + 1 + 3) / 4;
+    static constexpr int MAXREG_RAW = (16384 / (32 * PER_SMSP)) & ~7;
+    static constexpr int MAXREG = MAXREG_RAW > 255 ? 255 : MAXREG_RAW;
+    static_assert(RW % 8 == 0 && RBLK % CW == 0, "warps own whole 8-row escape groups");
 };
 
 constexpr int r128(int v) { return (v + 127) & ~127; }
@@ -38,7 +60,10 @@ struct FmaSmem {
     static constexpr int B = Q8 ? 0 : S::RBLK * 128;
     static constexpr int X = MT * 256 * 2;
     static constexpr int ESC_CAP = 512;
-    static constexpr int ESC = Q8 ? 0 : 16 + ESC_CAP * 4;
+    // escape area: [lo, hi, -, -] u32 | row-group index u16[16] | entries
+    static constexpr int ESC_GP = 16;
+    static constexpr int ESC_LIST = 48;
+    static constexpr int ESC = Q8 ? 0 : ESC_LIST + ESC_CAP * 4;
     static constexpr int OFF_AE = 0;
     static constexpr int OFF_B = r128(AE);
     static constexpr int OFF_X = OFF_B + r128(B);
@@ -47,7 +72,7 @@ struct FmaSmem {
     static constexpr int STAGES_RAW = (212 * 1024) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int TX_BYTES = AE + B + X;
-    static constexpr int BARS = STAGES * STAGE;           // barrier area offset
+    static constexpr int BARS = STAGES * STAGE; // barrier area offset
     static constexpr int TOTAL = BARS + 8 * (2 * STAGES + 1) + 16 + 1024; // + slack to align the base
 };
 
@@ -75,23 +100,67 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
+// One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
+// holding those two bytes and its B word:
+//   PRMT spreads the two AE bytes into two 16-bit lanes, replicating each byte's
+//   sign into the lane's high byte; then per lane
+//   sign (bit 15) | (ebase + E) << 7 | (A & 7) << 4 | B.
+// Written as explicit PTX so that it stays PRMT + LOP3/IMAD/LOP3 + SHF/LOP3.
+template <int I, bool Q8>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, uint32_t eb2)
+{
+    uint32_t p, t, r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(p) : "r"(ae_word), "n"((I & 1) ? 0xB3A2 : 0x9180));
+    asm("and.b32 %0, %1, 0x000F000F;" : "=r"(t) : "r"(p));
+    asm("mad.lo.u32 %0, %1, 128, %2;" : "=r"(t) : "r"(t), "r"(eb2));
+    asm("lop3.b32 %0, %1, 0x80708070, %2, 0xEA;" : "=r"(r) : "r"(p), "r"(t)); // (p & m) | t
+    if (!Q8) {
+        uint32_t b = bw;
+        if (I)
+            asm("shr.b32 %0, %1, %2;" : "=r"(b) : "r"(bw), "n"(4 * I));
+        asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(b), "r"(r)); // (b & m) | r
+    }
+    return r;
+}
+
 // Decode 8 weights (AE bytes k..k+7, their B word) to FP32 values.
-// Per pair: PRMT spreads two AE bytes into two 16-bit lanes with the sign
-// replicated into the high byte; then sign | (ebase + E) << 7 | A&7 << 4 | B.
 template <bool Q8>
 __device__ __forceinline__ void decode8(uint2 ae, uint32_t bw, uint32_t eb2, float (&wf)[8])
 {
+    const uint32_t r0 = decode_pair<0, Q8>(ae.x, bw, eb2);
+    const uint32_t r1 = decode_pair<1, Q8>(ae.x, bw, eb2);
+    const uint32_t r2 = decode_pair<2, Q8>(ae.y, bw, eb2);
+    const uint32_t r3 = decode_pair<3, Q8>(ae.y, bw, eb2);
+    const uint32_t r[4] = {r0, r1, r2, r3};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t src = (i < 2) ? ae.x : ae.y;
-        uint32_t p;
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(src), "r"(0u), "r"((i & 1) ? 0xB3A2u : 0x9180u));
-        uint32_t r = (p & 0x80708070u) | ((p & 0x000F000Fu) * 128u + eb2);
-        if (!Q8)
-            r |= (bw >> (4 * i)) & 0x000F000Fu;
-        wf[2 * i] = __uint_as_float(r << 16);
-        wf[2 * i + 1] = __uint_as_float(r & 0xFFFF0000u);
+        wf[2 * i] = __uint_as_float(r[i] << 16);
+        wf[2 * i + 1] = __uint_as_float(r[i] & 0xFFFF0000u);
     }
+}
+
+// The same 8 weights left as four BF16x2 words.
+template <bool Q8>
+__device__ __forceinline__ void decode8_bf16x2(uint2 ae, uint32_t bw, uint32_t eb2, uint32_t (&r)[4])
+{
+    r[0] = decode_pair<0, Q8>(ae.x, bw, eb2);
+    r[1] = decode_pair<1, Q8>(ae.x, bw, eb2);
+    r[2] = decode_pair<2, Q8>(ae.y, bw, eb2);
+    r[3] = decode_pair<3, Q8>(ae.y, bw, eb2);
+}
+
+// acc.x += lo(w) * lo(x), acc.y += hi(w) * hi(x) on BF16 halves with FP32
+// accumulation and one rounding each (the BF16 product is exact in FP32, so
+// this equals an FP32 FMA of the widened values).
+__device__ __forceinline__ void fma_bf16x2_f32(float2 &acc, uint32_t w, uint32_t x)
+{
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "r"(w), "r"(x));
 }
 
 // Reduce V per-lane values across the warp.  Afterwards, for V >= 32, lane l
@@ -121,7 +190,7 @@ struct XReduce {
 };
 
 template <int MT, bool Q8>
-__global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
+__global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     gemm_fma_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_x)
@@ -131,10 +200,9 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
     constexpr int RBLK = S::RBLK, CW = S::CW, RW = S::RW, STAGES = L::STAGES;
     constexpr int V = RW * MT;           // per-lane partial sums
     constexpr int VPL = V >= 32 ? V / 32 : 1;
-    constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : 2;
+    constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : 3;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // swizzled TMA tiles need 1024-byte aligned shared addresses
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * STAGES + 1);
@@ -171,13 +239,12 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
         int win = -1;
         uint32_t my_lo = 0, my_hi = 0;
         int issued = 0;
+        int rb = it0 / nk, ks = it0 % nk, s = 0;
+        uint32_t ph = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
             const bool ok = __all_sync(0xffffffffu, wait_or_abort(empty0 + 8 * s, ph ^ 1, a, abort_flag));
             if (!ok)
                 break;
-            const int gi = it0 + it, rb = gi / nk, ks = gi % nk;
             const int row0 = rb * RBLK, k0 = ks * 256;
             uint8_t *st = smem + s * L::STAGE;
             const uint32_t fb = full0 + 8 * s;
@@ -190,9 +257,12 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
             }
             if (!Q8) {
                 const int t = (row0 / 128) * a.tiles_c + ks;
-                uint32_t *hdr = reinterpret_cast<uint32_t *>(st + L::OFF_ESC);
+                uint8_t *esc_area = st + L::OFF_ESC;
                 if (lane < 2)
-                    cp_async_4(smem_u32(hdr + lane), a.tile_ptr + t + lane);
+                    cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
+                else if (lane < 4)
+                    cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
+                                a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
                 if (win < 0 || it - win >= 32) {
                     win = it;
                     const int gj = it0 + it + lane;
@@ -204,12 +274,25 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
                 }
                 const uint32_t lo = __shfl_sync(0xffffffffu, my_lo, it - win);
                 const uint32_t hi = __shfl_sync(0xffffffffu, my_hi, it - win);
+#ifdef W12_EXP_NOESCCOPY
+                const uint32_t cnt = 0u * (hi - lo);
+#else
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
+#endif
+                uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
-                    cp_async_4(smem_u32(hdr + 4 + idx), a.esc + lo + idx);
+                    cp_async_4(smem_u32(list + idx), a.esc + lo + idx);
                 cp_async_arrive_noinc(fb);
             }
             issued = it + 1;
+            if (++ks == nk) {
+                ks = 0;
+                ++rb;
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1;
+            }
         }
         // drain: every copy this warp started must land before the CTA exits
         for (int it = issued - 1; it >= 0 && it >= issued - STAGES; --it) {
@@ -222,10 +305,29 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
         float acc[MT <= 2 ? 1 : RW][MT <= 2 ? 1 : MT];
         float2 acc2[MT <= 2 ? RW : 1][MT <= 2 ? MT : 1];
         uint32_t eb2[RW];
+        // the (row, m) outputs whose escape corrections this lane keeps:
+        // index i = r * MT + m, i = lane (V <= 32) or 2 lane + q (V = 64)
+        float cneg[VPL], cpos[VPL];
+        uint32_t cph[VPL]; // placeholder magnitude bits of the pair's row (eb << 23)
+        int cr[VPL], cm[VPL];
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int i = (V >= 32) ? lane * VPL + q : lane;
+            cr[q] = (i < V) ? i / MT : -1; // -1: this lane keeps no output
+            cm[q] = (i < V) ? i % MT : 0;
+        }
         int cur_rb = -1;
+        int rb = it0 / nk, ks = it0 % nk; // (row block, k step) of iteration it
+        int s = 0;
+        uint32_t ph = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
+            // window bases of a new row block: start the load before waiting
+            uint32_t e_pre = 1u;
+            if (rb != cur_rb) {
+                const int n = rb * RBLK + wrow + lane;
+                if (lane < RW && n < a.N)
+                    e_pre = __ldg(a.ebase + n);
+            }
             bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
             if (a.inject_stall)
                 ok = wait_or_abort(stall_bar, 0, a, abort_flag) && ok;
@@ -233,7 +335,6 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
             // every named barrier) but works on stale data and reads nothing
             // through addresses taken from shared memory.
             ok = __all_sync(0xffffffffu, ok);
-            const int gi = it0 + it, rb = gi / nk, ks = gi % nk;
             const int row0 = rb * RBLK;
             const uint8_t *st = smem + s * L::STAGE;
 
@@ -248,75 +349,148 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
                         else
                             acc[r][m] = 0.f;
                     }
-                const int n = row0 + wrow + lane;
-                const uint32_t e = (lane < RW && n < a.N) ? __ldg(a.ebase + n) : 1u;
+                const uint32_t e = e_pre;
 #pragma unroll
                 for (int r = 0; r < RW; ++r) {
                     const uint32_t er = __shfl_sync(0xffffffffu, e, r);
                     eb2[r] = (er << 7) | (er << 23);
                 }
+#pragma unroll
+                for (int q = 0; q < VPL; ++q) {
+                    cneg[q] = 0.f;
+                    cpos[q] = 0.f;
+                    cph[q] = __shfl_sync(0xffffffffu, e, cr[q] & 31) << 23;
+                }
             }
 
-            // this lane's x[m][8l .. 8l+7] as FP32 pairs
+#ifdef W12_EXP_SKIP
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8 * s);
+            // next iteration: (row block, k step) and ring slot
+            if (++ks == nk) {
+                ks = 0;
+                ++rb;
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1;
+            }
+            continue;
+#endif
+            // this lane's x[m][8l .. 8l+7]: raw BF16x2 words and FP32 pairs
+            constexpr bool kMixed = W12_FMA_MIXED && MT <= 2;
+            uint32_t xw[MT][4];
             float2 x2[MT][4];
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const uint4 v = *reinterpret_cast<const uint4 *>(st + L::OFF_X + m * 512 + lane * 16);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                xw[m][0] = v.x;
+                xw[m][1] = v.y;
+                xw[m][2] = v.z;
+                xw[m][3] = v.w;
+                if constexpr (!kMixed) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    x2[m][i] = make_float2(__uint_as_float(w4[i] << 16),
-                                           __uint_as_float(w4[i] & 0xFFFF0000u));
-            }
-
-            // escapes of this warp's rows: [p, ub) in the tile's sorted list
-            uint32_t mask = 0;
-            uint32_t p = 0, ub = 0;
-            const uint32_t *list = nullptr;
-            const int base_row = (row0 & 127) + wrow;
-            if (!Q8) {
-                const uint32_t *hdr = reinterpret_cast<const uint32_t *>(st + L::OFF_ESC);
-                const uint32_t lo = hdr[0], hi = hdr[1];
-                const uint32_t cnt = ok ? hi - lo : 0u;
-                list = (cnt <= static_cast<uint32_t>(L::ESC_CAP)) ? hdr + 4 : a.esc + lo;
-                uint32_t n_in = 0;
-                for (uint32_t j = 0; j < cnt; j += 32) {
-                    const uint32_t idx = j + lane;
-                    const uint32_t e = idx < cnt ? list[idx] : 0xFFFFFFFFu;
-                    const int r7 = static_cast<int>(e >> 24);
-                    const bool inr = idx < cnt && r7 >= base_row && r7 < base_row + RW;
-                    p += __popc(__ballot_sync(0xffffffffu, idx < cnt && r7 < base_row));
-                    n_in += __popc(__ballot_sync(0xffffffffu, inr));
-                    mask |= __reduce_or_sync(0xffffffffu, inr ? (1u << (r7 - base_row)) : 0u);
+                    for (int i = 0; i < 4; ++i)
+                        x2[m][i] = make_float2(__uint_as_float(xw[m][i] << 16),
+                                               __uint_as_float(xw[m][i] & 0xFFFF0000u));
                 }
-                ub = p + n_in;
             }
 
-            const uint8_t *ae_p = st + L::OFF_AE + wrow * 256 + lane * 8;
-            const uint8_t *b_p = st + L::OFF_B + wrow * 128 + lane * 4;
+            if (!Q8) {
+                // this warp's escapes: its RW rows are whole 8-row groups of the tile
+                const uint8_t *esc_area = st + L::OFF_ESC;
+                const uint32_t lo = *reinterpret_cast<const uint32_t *>(esc_area);
+                const uint32_t hi = *reinterpret_cast<const uint32_t *>(esc_area + 4);
+                const uint32_t cnt = ok ? hi - lo : 0u;
+                if (cnt) {
+                    const uint16_t *gp = reinterpret_cast<const uint16_t *>(esc_area + L::ESC_GP);
+                    const int g = ((row0 & 127) + wrow) >> 3; // first 8-row group of this warp
+                    const uint32_t lb = gp[g];
+                    const uint32_t ub = (g + RW / 8 >= 16) ? cnt : gp[g + RW / 8];
+                    // entries are fetched 4 at a time (independent loads), then
+                    // applied strictly in list order
+                    const uint32_t pend = ub < cnt ? ub : cnt;
+                    const bool in_smem = cnt <= static_cast<uint32_t>(L::ESC_CAP);
+                    const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
+                    const uint32_t *list_g = a.esc + lo; // when more than fit in the stage
+                    const int rbase = (row0 & 127) + wrow;
+                    for (uint32_t p = lb; p < pend; p += 4) {
+                        uint32_t e[4];
+                        if (in_smem) {
 #pragma unroll
-            for (int r = 0; r < RW; ++r) {
-                const uint2 aw = *reinterpret_cast<const uint2 *>(ae_p + r * 256);
-                const uint32_t bw = Q8 ? 0u : *reinterpret_cast<const uint32_t *>(b_p + r * 128);
-                float wf[8];
-                decode8<Q8>(aw, bw, eb2[r], wf);
-                if (!Q8 && ((mask >> r) & 1u)) {
-                    const uint32_t rr = static_cast<uint32_t>(base_row + r);
-                    while (p < ub) {
-                        const uint32_t e = list[p];
-                        if ((e >> 24) != rr)
-                            break;
-                        const uint32_t k8 = (e >> 16) & 0xFFu;
-                        if ((k8 >> 3) == static_cast<uint32_t>(lane)) {
-                            const float f = __uint_as_float((e & 0xFFFFu) << 16);
+                            for (int u = 0; u < 4; ++u)
+                                e[u] = (p + u < pend) ? list_s[p + u] : 0xFFFFFFFFu;
+                        } else {
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (static_cast<uint32_t>(j) == (k8 & 7u))
-                                    wf[j] = f;
+                            for (int u = 0; u < 4; ++u)
+                                e[u] = (p + u < pend) ? __ldg(list_g + p + u) : 0xFFFFFFFFu;
                         }
-                        ++p;
+                        float xv[4][VPL];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+#pragma unroll
+                            for (int q = 0; q < VPL; ++q) {
+                                const uint32_t k8 = (e[u] >> 16) & 0xFFu;
+                                const uint32_t xb =
+                                    *reinterpret_cast<const uint16_t *>(st + L::OFF_X + cm[q] * 512 + k8 * 2);
+                                xv[u][q] = __uint_as_float(xb << 16);
+                            }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int r = static_cast<int>(e[u] >> 24) - rbase; // 255 - .. for padding
+                            const float wex = __uint_as_float((e[u] & 0xFFFFu) << 16);
+#pragma unroll
+                            for (int q = 0; q < VPL; ++q) {
+                                if (cr[q] == r) {
+                                    const float wph = __uint_as_float(((e[u] & 0x8000u) << 16) | cph[q]);
+                                    cneg[q] = fmaf(xv[u][q], -wph, cneg[q]);
+                                    cpos[q] = fmaf(xv[u][q], wex, cpos[q]);
+                                }
+                            }
+                        }
                     }
                 }
+            }
+            // For M = 1 the warp's raw planes fit in registers: load them all and
+            // hand the stage back to the producer before computing on them, so
+            // the refill overlaps the arithmetic.  Larger M reads them row by
+            // row and releases the stage afterwards.
+            constexpr bool kEarly = MT == 1;
+            const uint8_t *ae_p = st + L::OFF_AE + wrow * 256 + lane * 8;
+            const uint8_t *b_p = st + L::OFF_B + wrow * 128 + lane * 4;
+            uint2 aw[RW];
+            uint32_t bwr[RW];
+            if constexpr (kEarly) {
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    aw[r] = *reinterpret_cast<const uint2 *>(ae_p + r * 256);
+                    bwr[r] = Q8 ? 0u : *reinterpret_cast<const uint32_t *>(b_p + r * 128);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty0 + 8 * s);
+            }
+            // main loop: every row of this warp, no branches
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                if constexpr (!kEarly) {
+                    aw[r] = *reinterpret_cast<const uint2 *>(ae_p + r * 256);
+                    bwr[r] = Q8 ? 0u : *reinterpret_cast<const uint32_t *>(b_p + r * 128);
+                }
+                const uint32_t bw = bwr[r];
+                if constexpr (kMixed) {
+                    uint32_t wr[4];
+                    decode8_bf16x2<Q8>(aw[r], bw, eb2[r], wr);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            fma_bf16x2_f32(acc2[r][m], wr[i], xw[m][i]);
+                    continue;
+                }
+                float wf[8];
+                decode8<Q8>(aw[r], bw, eb2[r], wf);
                 const float2 w01 = make_float2(wf[0], wf[1]), w23 = make_float2(wf[2], wf[3]);
                 const float2 w45 = make_float2(wf[4], wf[5]), w67 = make_float2(wf[6], wf[7]);
 #pragma unroll
@@ -337,9 +511,12 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty0 + 8 * s);
+            if constexpr (!kEarly) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty0 + 8 * s);
+            }
+
 
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- the row block ends here for this CTA: reduce and store ----
@@ -362,28 +539,49 @@ __global__ void __launch_bounds__(FmaShape<MT>::THREADS, 1)
 #pragma unroll
                 for (int q = 0; q < VPL; ++q) {
                     const int idx = (V >= 32) ? lane * VPL + q : (lane >> (5 - LOGV));
+                    float cn = cneg[q], cp = cpos[q];
+                    if constexpr (V < 32) {
+                        cn = __shfl_sync(0xffffffffu, cneg[0], idx);
+                        cp = __shfl_sync(0xffffffffu, cpos[0], idx);
+                    }
+                    // the placeholder products out first, then the exact ones in
+                    const float total = (v[q] + cn) + cp;
                     const int r = idx / MT, m = idx % MT;
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
                         if (direct) {
                             if (n < a.N)
-                                a.y[static_cast<size_t>(m) * a.N + n] = v[q];
+                                a.y[static_cast<size_t>(m) * a.N + n] = total;
                         } else {
-                            a.partials[(static_cast<size_t>(slot) * a.M + m) * RBLK + wrow + r] = v[q];
+                            a.partials[(static_cast<size_t>(slot) * a.M + m) * RBLK + wrow + r] = total;
                         }
                     }
                 }
                 if (!direct) {
-                    __threadfence();
+                    // the CTA barrier orders every thread's partial stores before
+                    // thread 0's GPU-scope fence and arrival (cumulativity), and
+                    // thread 0's fence after the last arrival before everyone's reads
                     named_bar_sync(1, CW * 32);
-                    if (threadIdx.x == 0)
-                        *seg_last = sk_arrive(a.counters + rb, a.epoch, c_last - c_first + 1) ? 1 : 0;
-                    named_bar_sync(1, CW * 32);
-                    if (*seg_last) {
+                    if (threadIdx.x == 0) {
                         __threadfence();
-                        sk_reduce_block(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
+                        const bool last = sk_arrive(a.counters + rb, a.epoch, c_last - c_first + 1);
+                        if (last)
+                            __threadfence();
+                        *seg_last = last ? 1 : 0;
                     }
+                    named_bar_sync(1, CW * 32);
+                    if (*seg_last)
+                        sk_reduce_block(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
                 }
+            }
+            // next iteration: (row block, k step) and ring slot
+            if (++ks == nk) {
+                ks = 0;
+                ++rb;
+            }
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1;
             }
         }
     }

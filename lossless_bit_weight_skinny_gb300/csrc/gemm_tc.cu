@@ -390,15 +390,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!direct) {
-                    __threadfence();
                     named_bar_sync(1, kDecodeWarps * 32);
-                    if (threadIdx.x == 0)
-                        *seg_last = sk_arrive(a.counters + rb, a.epoch, c_last - c_first + 1) ? 1 : 0;
-                    named_bar_sync(1, kDecodeWarps * 32);
-                    if (*seg_last) {
+                    if (threadIdx.x == 0) {
                         __threadfence();
-                        sk_reduce_block(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);
+                        const bool last = sk_arrive(a.counters + rb, a.epoch, c_last - c_first + 1);
+                        if (last)
+                            __threadfence();
+                        *seg_last = last ? 1 : 0;
                     }
+                    named_bar_sync(1, kDecodeWarps * 32);
+                    if (*seg_last)
+                        sk_reduce_block(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);
                 }
             }
         }

@@ -18,16 +18,17 @@ struct GemmArgs {
     const uint8_t *ebase;          // [N] window base per row
     const uint32_t *tile_ptr;      // [T + 1]
     const uint32_t *esc;           // escape entries
+    const uint16_t *gptr;          // [T][16]: entries of tile t in rows < 8g
     float *y;                      // [M][N]
     float *partials;               // [2 * grid][M][rows_blk] split-K partial sums
-    unsigned long long *counters;  // [n_rowblk] epoch<<32 | arrivals
+    unsigned long long *counters;  // [n_rowblk] arrivals (zero between launches)
     int *status;                   // device status word of the handle
     int M, N, K;
     int tiles_c;                   // ceil(K / 256): escape tiles per row band
     int n_rowblk;                  // row blocks
     int n_kstep;                   // k steps per row block
     int total_iters;               // n_rowblk * n_kstep
-    uint32_t epoch;                // unique per call on this workspace
+    uint32_t epoch;                // call counter (diagnostic only)
     uint64_t limit_ns;             // bounded-wait limit
     int inject_stall;              // test hook: wait on a barrier nobody arrives on
 };
@@ -52,27 +53,19 @@ __device__ __forceinline__ int sk_slot(int c, int rb, int grid, int iters, int n
     return 2 * c + (rb == first_rb ? 0 : 1);
 }
 
-// Register one arrival for row block rb under this call's epoch; returns true
-// for the last of `n` contributors.  Stale counts left by an earlier call that
-// was aborted are discarded by the epoch compare.
-__device__ __forceinline__ bool sk_arrive(unsigned long long *ctr, uint32_t epoch, uint32_t n)
+// Register one arrival for row block rb; returns true for the last of `n`
+// contributors, which also resets the count to zero for the next launch (or a
+// replay of this one from a CUDA graph).  One atomicAdd per contributor: no
+// retry loop, so many CTAs sharing a row block do not serialise on the L2.
+// Every contributor arrives exactly once even after a timeout (the kernels
+// keep their loop shape), so the count always completes and resets.
+__device__ __forceinline__ bool sk_arrive(unsigned long long *ctr, uint32_t /*epoch*/, uint32_t n)
 {
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(ctr);
-    for (;;) {
-        const unsigned long long nxt = (static_cast<uint32_t>(cur >> 32) == epoch)
-                                           ? cur + 1
-                                           : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(ctr, cur, nxt);
-        if (prev == cur) {
-            if (static_cast<uint32_t>(nxt) != n)
-                return false;
-            // last one: zero the count (keeping the epoch) so that a replay of
-            // the same launch -- e.g. from a CUDA graph -- counts from zero
-            atomicExch(ctr, static_cast<unsigned long long>(epoch) << 32);
-            return true;
-        }
-        cur = prev;
-    }
+    const unsigned long long old = atomicAdd(ctr, 1ull);
+    if (old + 1 != n)
+        return false;
+    atomicExch(ctr, 0ull);
+    return true;
 }
 
 __device__ __forceinline__ void report(int *status, int code)
@@ -81,22 +74,49 @@ __device__ __forceinline__ void report(int *status, int code)
 }
 
 // The last contributor sums every partial of row block rb in contributor
-// order (fixed, so results are bitwise reproducible) and writes y.
-// Threads [0, nthreads) of the CTA take part.
+// order (fixed, so results are bitwise reproducible) and writes y.  Threads
+// [0, nthreads) of the CTA take part; each owns float4 groups of (m, 4 rows)
+// and fetches the contributors' values 4 at a time with independent 16-byte
+// loads (the sums still run in contributor order).
 __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int rows_blk, int grid,
                                                 int c_first, int c_last, int tid, int nthreads)
 {
     const int row0 = rb * rows_blk;
-    const int total = a.M * rows_blk;
-    for (int idx = tid; idx < total; idx += nthreads) {
-        const int m = idx / rows_blk, r = idx % rows_blk;
-        float s = 0.f;
-        for (int c = c_first; c <= c_last; ++c) {
-            const int slot = sk_slot(c, rb, grid, a.total_iters, a.n_kstep);
-            s += __ldcg(a.partials + (static_cast<size_t>(slot) * a.M + m) * rows_blk + r);
+    const int groups = a.M * rows_blk / 4; // float4 groups per partial
+    const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
+    const float4 *base = reinterpret_cast<const float4 *>(a.partials);
+    // the first contributor's slot index is 0 or 1; the others start in this
+    // row block, so their slot is 2c
+    const int slot_first = sk_slot(c_first, rb, grid, a.total_iters, a.n_kstep);
+    for (int g = tid; g < groups; g += nthreads) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u;
+                if (c <= c_last) {
+                    const int slot = (c == c_first) ? slot_first : 2 * c;
+                    v[u] = __ldcg(base + slot * slot4 + g);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (c0 + u <= c_last) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
         }
-        if (row0 + r < a.N)
-            a.y[static_cast<size_t>(m) * a.N + row0 + r] = s;
+        const int m = (4 * g) / rows_blk, r = (4 * g) % rows_blk;
+        float *yp = a.y + static_cast<size_t>(m) * a.N + row0 + r;
+        const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (row0 + r + q < a.N)
+                yp[q] = v4[q];
     }
 }
 

@@ -94,6 +94,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // The barrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar)

@@ -6,6 +6,7 @@
 #include <mutex>
 #include <new>
 #include <utility>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -18,6 +19,13 @@ using namespace w12;
 namespace {
 
 std::atomic<uint64_t> g_limit_ns{200ull * 1000 * 1000}; // bounded waits: 200 ms
+thread_local const char *g_last_error = "no error";
+
+w12_status cuda_fail(cudaError_t e)
+{
+    g_last_error = cudaGetErrorName(e);
+    return W12_ERR_CUDA;
+}
 std::atomic<int> g_inject_stall{0};
 
 // ---- TMA descriptor encoding through the driver entry point -----------------
@@ -161,6 +169,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     a.ebase = w->ebase;
     a.tile_ptr = w->tile_ptr;
     a.esc = w->esc;
+    a.gptr = w->gptr;
     a.y = y;
     a.status = w->status;
     a.M = M;
@@ -187,8 +196,10 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
                                     CU_TENSOR_MAP_SWIZZLE_128B)
                         : make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 256, mt,
                                     CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!okx)
+    if (!okx) {
+        g_last_error = "cuTensorMapEncodeTiled failed for x";
         return W12_ERR_CUDA;
+    }
     cudaError_t e;
     if (tc)
         e = launch_gemm_tc(mt, q8, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
@@ -196,7 +207,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
         e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma128), tmap_of(w->tm_b_fma128), &tmx, grid, st);
     else
         e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma64), tmap_of(w->tm_b_fma64), &tmx, grid, st);
-    return e == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+    return e == cudaSuccess ? W12_OK : cuda_fail(e);
 }
 
 } // namespace
@@ -224,8 +235,28 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
     d->tiles_c = ceil_div(h->K, kTileCols);
     auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
     const size_t s_status = 256, s_ebase = up(h->ebase.size()), s_ae = up(h->ae.size()),
-                 s_b = up(h->b.size()), s_ptr = up(4 * h->tile_ptr.size()), s_esc = up(4 * h->esc.size());
-    d->bytes = s_status + s_ebase + s_ae + s_b + s_ptr + s_esc;
+                 s_b = up(h->b.size()), s_ptr = up(4 * h->tile_ptr.size()), s_esc = up(4 * h->esc.size()),
+                 s_gp = up(32 * static_cast<size_t>(d->T));
+    d->bytes = s_status + s_ebase + s_ae + s_b + s_ptr + s_esc + s_gp;
+    // row-group index of every escape tile: gp[t][g] = entries of tile t whose
+    // row (within the tile) is below 8g, so the entries of rows [8g, 8g+8) are
+    // [gp[t][g], gp[t][g+1]) (gp[t][16] being the tile's count)
+    std::vector<uint16_t> gp;
+    try {
+        gp.assign(16 * static_cast<size_t>(d->T), 0);
+    } catch (...) {
+        delete d;
+        return W12_ERR_OOM;
+    }
+    for (int64_t t = 0; t < d->T; ++t) {
+        const uint32_t lo = h->tile_ptr[t], hi = h->tile_ptr[t + 1];
+        uint32_t i = lo;
+        for (int g = 0; g < 16; ++g) {
+            while (i < hi && (h->esc[i] >> 24) < static_cast<uint32_t>(8 * g))
+                ++i;
+            gp[16 * t + g] = static_cast<uint16_t>(i - lo);
+        }
+    }
     if (cudaMalloc(&d->base, d->bytes) != cudaSuccess) {
         cudaGetLastError();
         delete d;
@@ -243,6 +274,8 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
     d->tile_ptr = reinterpret_cast<uint32_t *>(p);
     p += s_ptr;
     d->esc = reinterpret_cast<uint32_t *>(p);
+    p += s_esc;
+    d->gptr = reinterpret_cast<uint16_t *>(p);
     bool ok = cudaMemsetAsync(d->status, 0, 256, st) == cudaSuccess;
     auto cp = [&](void *dst, const void *src, size_t n) {
         if (n)
@@ -253,6 +286,9 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
     cp(d->b, h->b.data(), h->b.size());
     cp(d->tile_ptr, h->tile_ptr.data(), 4 * h->tile_ptr.size());
     cp(d->esc, h->esc.data(), 4 * h->esc.size());
+    cp(d->gptr, gp.data(), 2 * gp.size());
+    if (ok && !gp.empty())
+        ok = cudaStreamSynchronize(st) == cudaSuccess; // gp is a local staging buffer
     if (!ok) {
         cudaFree(d->base);
         delete d;
@@ -385,5 +421,7 @@ void w12_set_spin_limit(uint32_t limit_ns)
 }
 
 void w12_debug_inject_stall(int on) { g_inject_stall.store(on ? 1 : 0); }
+
+const char *w12_last_cuda_error(void) { return g_last_error; }
 
 } // extern "C"

@@ -46,6 +46,7 @@ struct w12_dev {
     uint8_t *b = nullptr;
     uint32_t *tile_ptr = nullptr;
     uint32_t *esc = nullptr;
+    uint16_t *gptr = nullptr; // [T][16] row-group offsets inside each escape tile
     int *status = nullptr; // device status word
     bool gemm_ok = false;  // K % 32 == 0 and tensor maps built
     // tensor maps over the planes: plain boxes for the FMA kernels, swizzled
