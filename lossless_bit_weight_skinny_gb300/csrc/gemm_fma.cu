@@ -274,11 +274,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 }
                 const uint32_t lo = __shfl_sync(0xffffffffu, my_lo, it - win);
                 const uint32_t hi = __shfl_sync(0xffffffffu, my_hi, it - win);
-#ifdef W12_EXP_NOESCCOPY
-                const uint32_t cnt = 0u * (hi - lo);
-#else
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
-#endif
                 uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
                     cp_async_4(smem_u32(list + idx), a.esc + lo + idx);
@@ -363,21 +359,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 }
             }
 
-#ifdef W12_EXP_SKIP
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty0 + 8 * s);
-            // next iteration: (row block, k step) and ring slot
-            if (++ks == nk) {
-                ks = 0;
-                ++rb;
-            }
-            if (++s == STAGES) {
-                s = 0;
-                ph ^= 1;
-            }
-            continue;
-#endif
             // this lane's x[m][8l .. 8l+7]: raw BF16x2 words and FP32 pairs
             constexpr bool kMixed = W12_FMA_MIXED && MT <= 2;
             uint32_t xw[MT][4];
