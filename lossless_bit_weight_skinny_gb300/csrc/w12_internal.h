@@ -3,7 +3,7 @@
 #include <cstdint>
 #include <vector>
 
-#include "../../include/w12.h"
+#include "w12.h"
 
 namespace w12 {
 
