@@ -54,8 +54,11 @@ def _kernel_hash():
     return h.hexdigest()[:16]
 
 
-def _traffic(name):
-    """DRAM bytes per launch from a committed ncu summary, if still current."""
+def _traffic(name, alg_bytes_per_launch):
+    """DRAM bytes per launch, from a committed ncu capture of one large launch
+    of the same kernel: its DRAM/algorithmic byte ratio times this run's
+    algorithmic bytes per launch (traffic grows in proportion to the weights
+    streamed).  None if the kernel source changed since the capture."""
     p = os.path.join(ROOT, "profiles", f"{name}.json")
     try:
         with open(p) as f:
@@ -64,7 +67,7 @@ def _traffic(name):
         return None
     if d.get("kernel_sha") != _kernel_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    return int(d["traffic_over_algorithmic"] * alg_bytes_per_launch)
 
 
 class ClockSampler:
@@ -257,7 +260,8 @@ def run_w12(args):
     peak, peak_kind = _peaks()
     achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
     n_launch = args.steps * n_proj
-    traffic = _traffic("gemm_fma_m1")
+    n_meas = sum(v[1] for v in per_proj.values()) if per_proj else args.steps * n_proj
+    traffic = _traffic("gemm_fma_m1", kern_bytes / max(1, n_meas))
 
     # the same layer at M = 32 and M = 64 (tensor-core path), shorter runs
     by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
@@ -472,6 +476,29 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(case):
+    """A small profiling case: one 17408x5120 W12 matrix (134 MB, larger than
+    L2) and three launches of one kernel (for ncu captures)."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__._load_builder().build()
+    import lossless_bit_weight_skinny_gb300 as w12
+
+    N, K = 17408, 5120
+    wb = WL.projection_weights_torch(N, K, seed=5)
+    d = w12.w12_upload(w12.w12_encode(wb.cpu().numpy().view(np.uint16)))
+    M = {"fma": 1, "fma2": 2, "fma4": 4, "tc16": 16, "tc32": 32, "tc": 64, "q8": 64, "q8m1": 1}[case]
+    x = torch.from_numpy(WL.activations(M, K, seed=1).view(np.int16)).cuda().view(torch.bfloat16)
+    fn = w12.w12_gemm_q8view if case.startswith("q8") else w12.w12_gemm
+    for _ in range(3):
+        y = fn(x, d)
+    torch.cuda.synchronize()
+    assert w12.w12_dev_status(d) == 0
+    print(case, "ok", float(y.abs().sum()))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,10 +509,13 @@ def main():
     ap.add_argument("--graph-steps", type=int, default=12)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="profiling case: fma, fma2, fma4, tc16, tc32, tc, q8, q8m1")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args.case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_w12(args)
