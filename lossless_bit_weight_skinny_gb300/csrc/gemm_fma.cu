@@ -1,4 +1,4 @@
-// gemm_fma.cu -- W12 skinny GEMM for M <= 8 activation rows on the CUDA cores.
+// gemm_fma.cu -- W12 skinny GEMM for M <= 4 activation rows on the CUDA cores.
 //
 // y[m][n] = sum_k x[m][k] * W[n][k], W decoded from its W12 planes to exact
 // BF16 values (SpecPilot, Figure 5(a) caption) in registers and accumulated in
@@ -596,7 +596,7 @@ int fma_smem_bytes(int mt, bool q8)
     case 1: return q8 ? FmaSmem<1, true>::TOTAL : FmaSmem<1, false>::TOTAL;
     case 2: return q8 ? FmaSmem<2, true>::TOTAL : FmaSmem<2, false>::TOTAL;
     case 4: return q8 ? FmaSmem<4, true>::TOTAL : FmaSmem<4, false>::TOTAL;
-    default: return q8 ? FmaSmem<8, true>::TOTAL : FmaSmem<8, false>::TOTAL;
+    default: return q8 ? FmaSmem<4, true>::TOTAL : FmaSmem<4, false>::TOTAL;
     }
 }
 
@@ -611,8 +611,6 @@ cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMa
                       : launch_one<2, false>(a, tm_ae, tm_b, tm_x, grid, st);
     case 4: return q8 ? launch_one<4, true>(a, tm_ae, tm_b, tm_x, grid, st)
                       : launch_one<4, false>(a, tm_ae, tm_b, tm_x, grid, st);
-    case 8: return q8 ? launch_one<8, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                      : launch_one<8, false>(a, tm_ae, tm_b, tm_x, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -1,4 +1,4 @@
-// gemm_tc.cu -- W12 skinny GEMM for 9..64 activation rows on the tcgen05
+// gemm_tc.cu -- W12 skinny GEMM for 5..64 activation rows on the tcgen05
 // tensor cores.
 //
 // The product is computed transposed: D[n][m] = sum_k W[n][k] x[m][k], with the
@@ -11,45 +11,69 @@
 // tcgen05.st and the MMA reads A from there, so decoded weights never touch
 // shared memory.
 //
-// CTA = 8 decode warps + 1 TMA producer warp + 1 MMA warp.  Work split and
-// split-K fix-up are the stream-K scheme of the CUDA-core kernel, over blocks of
-// 128 rows x 128 columns (half an escape tile).
+// CTA = 16 decode warps + a weight-TMA warp + an activation-TMA warp + an MMA
+// warp, over three independent rings:
+//   * weights (AE, B, escapes) in shared memory: a decode warp copies its share
+//     of a stage into registers and releases the slot at once, so the weight
+//     stream never waits for the tensor cores;
+//   * activations (the B operand) in shared memory, released by the MMA;
+//   * decoded weights (the A operand) in tensor memory, released by the MMA.
+// Work split and split-K fix-up are the stream-K scheme of the CUDA-core
+// kernel, over blocks of 128 rows x 128 columns (half an escape tile).
 #include "kernels.cuh"
 
 namespace w12 {
 namespace {
 
-constexpr int kDecodeWarps = 8;
-constexpr int kThreads = (kDecodeWarps + 2) * 32;
-constexpr int kScrPitch = 144; // escape scratch row pitch (bytes): 64 BF16 + pad
+#ifndef W12_TC_DECODE_WARPS
+#define W12_TC_DECODE_WARPS 16
+#endif
+constexpr int kDecodeWarps = W12_TC_DECODE_WARPS; // 8 or 16
+constexpr int kKQ = kDecodeWarps / 4;  // decode warps per 32-row quadrant
+constexpr int kKW = 128 / kKQ;         // columns of a 128-column step per decode warp
+constexpr int kCols = kKW / 2;         // TMEM columns (BF16 pairs) per decode warp
+constexpr int kWarpW = kDecodeWarps;     // weight producer
+constexpr int kWarpX = kDecodeWarps + 1; // activation producer
+constexpr int kWarpM = kDecodeWarps + 2; // MMA issuer, tensor-memory owner
+constexpr int kThreads = (kDecodeWarps + 3) * 32;
+constexpr int kScrPitch = 2 * kKW + 16; // escape scratch row pitch (bytes): kKW BF16 + pad
+constexpr int kNA = 4;         // A buffers in tensor memory (64 columns each)
 
 constexpr int a128(int v) { return (v + 127) & ~127; }
 constexpr int a1024(int v) { return (v + 1023) & ~1023; }
 
 template <int MT, bool Q8>
 struct TcSmem {
-    static constexpr int AE = 128 * 128;        // SWIZZLE_128B
-    static constexpr int B = Q8 ? 0 : 128 * 64; // SWIZZLE_64B
-    static constexpr int XSUB = MT * 128;       // one 64-column sub-tile, SWIZZLE_128B
-    static constexpr int X = 2 * XSUB;
+    // weight stage: AE (SWIZZLE_128B), B (SWIZZLE_64B), escape area
+    static constexpr int AE = 128 * 128;
+    static constexpr int B = Q8 ? 0 : 128 * 64;
     static constexpr int ESC_CAP = 512;
-    static constexpr int ESC = Q8 ? 0 : 16 + 4 * ESC_CAP;
+    static constexpr int ESC_GP = 16; // [lo, hi, -, -] u32, then the row-group index u16[16]
+    static constexpr int ESC_LIST = 48;
+    static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
     static constexpr int OFF_AE = 0;
     static constexpr int OFF_B = AE;
-    static constexpr int OFF_X = a1024(OFF_B + B);
-    static constexpr int OFF_ESC = OFF_X + X;
-    static constexpr int STAGE = a1024(OFF_ESC + ESC);
+    static constexpr int OFF_ESC = OFF_B + B;
+    static constexpr int WSTAGE = a1024(OFF_ESC + ESC);
+    // activation stage: two 64-column sub-tiles of MT rows, SWIZZLE_128B
+    static constexpr int XSUB = MT * 128;
+    static constexpr int XSTAGE = 2 * XSUB;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * 32 * kScrPitch;
-    static constexpr int ST_RAW = (212 * 1024 - SCR) / STAGE;
-    static constexpr int STAGES = ST_RAW > 6 ? 6 : ST_RAW;
-    static constexpr int OFF_SCR = STAGES * STAGE;
+    static constexpr int BUDGET = 212 * 1024 - SCR;
+    static constexpr int XST = (MT <= 32) ? 4 : 3; // activation slots
+    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE) / WSTAGE;
+    static constexpr int WST = WST_RAW > 8 ? 8 : WST_RAW; // weight slots
+    static constexpr int OFF_X = WST * WSTAGE;
+    static constexpr int OFF_SCR = OFF_X + XST * XSTAGE;
     static constexpr int BARS = a128(OFF_SCR + SCR);
-    // full, aready, empty per stage; acc_full, acc_empty, final, stall
-    static constexpr int NBARS = 3 * STAGES + 4;
+    // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
+    // acc_full, acc_empty, final, stall
+    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4;
     static constexpr int TOTAL = BARS + 8 * NBARS + 32 + 1024; // + slack to align the base
-    static constexpr int TX_BYTES = AE + B + X;
-    static constexpr uint32_t D_COL = STAGES * 64;
+    static constexpr int W_TX = AE + B;
+    static constexpr uint32_t D_COL = kNA * 64;
     static_assert(D_COL + MT <= 512, "tensor memory budget");
+    static_assert(WST >= 3, "weight ring too shallow");
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmArgs &a,
@@ -75,22 +99,44 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
-// Four BF16x2 words (k pairs 0..3 of a group of 8) from the group's two AE
-// words and its B word.
-template <bool Q8>
-__device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint32_t bw,
-                                             uint32_t eb2, uint32_t *out)
+// One BF16x2 pair from the AE word holding its two bytes and the B word of its
+// group of 8 (bit layout as in the CUDA-core kernel):
+// sign | (ebase + E) << 7 | (A & 7) << 4 | B per 16-bit lane.
+template <int I, bool Q8>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, uint32_t eb2)
 {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t src = (i < 2) ? a_lo : a_hi;
-        uint32_t p;
-        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(src), "r"(0u), "r"((i & 1) ? 0xB3A2u : 0x9180u));
-        uint32_t r = (p & 0x80708070u) | ((p & 0x000F000Fu) * 128u + eb2);
-        if (!Q8)
-            r |= (bw >> (4 * i)) & 0x000F000Fu;
-        out[i] = r;
+    uint32_t p, t, r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(p) : "r"(ae_word), "n"((I & 1) ? 0xB3A2 : 0x9180));
+    asm("and.b32 %0, %1, 0x000F000F;" : "=r"(t) : "r"(p));
+    asm("mad.lo.u32 %0, %1, 128, %2;" : "=r"(t) : "r"(t), "r"(eb2));
+    asm("lop3.b32 %0, %1, 0x80708070, %2, 0xEA;" : "=r"(r) : "r"(p), "r"(t)); // (p & m) | t
+    if (!Q8) {
+        uint32_t b = bw;
+        if (I)
+            asm("shr.b32 %0, %1, %2;" : "=r"(b) : "r"(bw), "n"(4 * I));
+        asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(b), "r"(r)); // (b & m) | r
     }
+    return r;
+}
+
+template <bool Q8>
+__device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint32_t bw, uint32_t eb2,
+                                             uint32_t *out)
+{
+    out[0] = decode_pair<0, Q8>(a_lo, bw, eb2);
+    out[1] = decode_pair<1, Q8>(a_lo, bw, eb2);
+    out[2] = decode_pair<2, Q8>(a_hi, bw, eb2);
+    out[3] = decode_pair<3, Q8>(a_hi, bw, eb2);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t (&v)[N])
+{
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 32)
+        tmem_st32(taddr, v);
+    else
+        tmem_st16(taddr, v);
 }
 
 template <int MT, bool Q8>
@@ -100,20 +146,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_x)
 {
     using L = TcSmem<MT, Q8>;
-    constexpr int STAGES = L::STAGES;
+    constexpr int WST = L::WST, XST = L::XST;
     constexpr uint32_t IDESC = idesc_bf16_f32(128, MT);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // swizzled TMA tiles need 1024-byte aligned shared addresses
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
-    const uint32_t full0 = smem_u32(bars);
-    const uint32_t aready0 = smem_u32(bars + STAGES);
-    const uint32_t empty0 = smem_u32(bars + 2 * STAGES);
-    const uint32_t acc_full = smem_u32(bars + 3 * STAGES);
-    const uint32_t acc_empty = smem_u32(bars + 3 * STAGES + 1);
-    const uint32_t final_bar = smem_u32(bars + 3 * STAGES + 2);
-    const uint32_t stall_bar = smem_u32(bars + 3 * STAGES + 3);
+    const uint32_t w_full0 = smem_u32(bars);
+    const uint32_t w_empty0 = smem_u32(bars + WST);
+    const uint32_t x_full0 = smem_u32(bars + 2 * WST);
+    const uint32_t x_empty0 = smem_u32(bars + 2 * WST + XST);
+    const uint32_t a_full0 = smem_u32(bars + 2 * WST + 2 * XST);
+    const uint32_t a_empty0 = smem_u32(bars + 2 * WST + 2 * XST + kNA);
+    const uint32_t acc_full = smem_u32(bars + 2 * WST + 2 * XST + 2 * kNA);
+    const uint32_t acc_empty = acc_full + 8;
+    const uint32_t final_bar = acc_full + 16;
+    const uint32_t stall_bar = acc_full + 24;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + L::NBARS);
     volatile int *seg_last = abort_flag + 1;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
@@ -125,10 +174,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nk = a.n_kstep;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(aready0 + 8 * s, kDecodeWarps);
-            mbar_init(empty0 + 8 * s, kDecodeWarps + 1);
+        for (int s = 0; s < WST; ++s) {
+            mbar_init(w_full0 + 8 * s, Q8 ? 1 : 33);
+            mbar_init(w_empty0 + 8 * s, kDecodeWarps);
+        }
+        for (int s = 0; s < XST; ++s) {
+            mbar_init(x_full0 + 8 * s, 1);
+            mbar_init(x_empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < kNA; ++b) {
+            mbar_init(a_full0 + 8 * b, kDecodeWarps);
+            mbar_init(a_empty0 + 8 * b, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kDecodeWarps);
@@ -138,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *seg_last = 0;
         fence_barrier_init();
     }
-    if (warp == kDecodeWarps + 1) {
+    if (warp == kWarpM) {
         tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), 512);
         tmem_relinquish();
     }
@@ -147,40 +203,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kDecodeWarps) {
-        // ------------------------------ producer ------------------------------
+    if (warp == kWarpW) {
+        // --------------------------- weight producer ---------------------------
         if (lane == 0) {
             prefetch_tmap(&tm_ae);
-            prefetch_tmap(&tm_x);
             if (!Q8)
                 prefetch_tmap(&tm_b);
         }
         int win = -1;
         uint32_t my_lo = 0, my_hi = 0;
         int issued = 0;
+        int rb = it0 / nk, ks = it0 % nk, s = 0;
+        uint32_t ph = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
-            const bool ok = __all_sync(0xffffffffu, wait_or_abort(empty0 + 8 * s, ph ^ 1, a, abort_flag));
+            const bool ok = __all_sync(0xffffffffu, wait_or_abort(w_empty0 + 8 * s, ph ^ 1, a, abort_flag));
             if (!ok)
                 break;
-            const int gi = it0 + it, rb = gi / nk, ks = gi % nk;
             const int row0 = rb * 128, k0 = ks * 128;
-            uint8_t *st = smem + s * L::STAGE;
-            const uint32_t fb = full0 + 8 * s;
+            uint8_t *st = smem + s * L::WSTAGE;
+            const uint32_t fb = w_full0 + 8 * s;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, L::TX_BYTES);
+                mbar_arrive_expect_tx(fb, L::W_TX);
                 tma_load_2d(smem_u32(st + L::OFF_AE), &tm_ae, k0, row0, fb);
                 if (!Q8)
                     tma_load_2d(smem_u32(st + L::OFF_B), &tm_b, k0 / 2, row0, fb);
-                tma_load_2d(smem_u32(st + L::OFF_X), &tm_x, k0, 0, fb);
-                tma_load_2d(smem_u32(st + L::OFF_X + L::XSUB), &tm_x, k0 + 64, 0, fb);
             }
             if (!Q8) {
                 const int t = rb * a.tiles_c + (k0 >> 8);
-                uint32_t *hdr = reinterpret_cast<uint32_t *>(st + L::OFF_ESC);
+                uint8_t *esc_area = st + L::OFF_ESC;
                 if (lane < 2)
-                    cp_async_4(smem_u32(hdr + lane), a.tile_ptr + t + lane);
+                    cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
+                else if (lane < 4)
+                    cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
+                                a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
                 if (win < 0 || it - win >= 32) {
                     win = it;
                     const int gj = it0 + it + lane;
@@ -193,44 +248,93 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t lo = __shfl_sync(0xffffffffu, my_lo, it - win);
                 const uint32_t hi = __shfl_sync(0xffffffffu, my_hi, it - win);
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
+                uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
-                    cp_async_4(smem_u32(hdr + 4 + idx), a.esc + lo + idx);
+                    cp_async_4(smem_u32(list + idx), a.esc + lo + idx);
                 cp_async_arrive_noinc(fb);
             }
             issued = it + 1;
+            if (++ks == nk) {
+                ks = 0;
+                ++rb;
+            }
+            if (++s == WST) {
+                s = 0;
+                ph ^= 1;
+            }
         }
-        for (int it = issued - 1; it >= 0 && it >= issued - STAGES; --it)
-            mbar_wait(full0 + 8 * (it % STAGES), (it / STAGES) & 1, 1000000000ull);
-    } else if (warp == kDecodeWarps + 1) {
-        // ------------------------------ MMA issuer ----------------------------
+        // drain: every copy this warp started must land before the CTA exits
+        for (int it = issued - 1; it >= 0 && it >= issued - WST; --it)
+            mbar_wait(w_full0 + 8 * (it % WST), (it / WST) & 1, 1000000000ull);
+    } else if (warp == kWarpX) {
+        // ------------------------- activation producer -------------------------
+        if (lane == 0) {
+            prefetch_tmap(&tm_x);
+            int issued = 0;
+            int ks = it0 % nk, s = 0;
+            uint32_t ph = 0;
+            for (int it = 0; it < n_it; ++it) {
+                if (!wait_or_abort(x_empty0 + 8 * s, ph ^ 1, a, abort_flag))
+                    break;
+                const int k0 = ks * 128;
+                uint8_t *xs = smem + L::OFF_X + s * L::XSTAGE;
+                const uint32_t fb = x_full0 + 8 * s;
+                mbar_arrive_expect_tx(fb, L::XSTAGE);
+                tma_load_2d(smem_u32(xs), &tm_x, k0, 0, fb);
+                tma_load_2d(smem_u32(xs + L::XSUB), &tm_x, k0 + 64, 0, fb);
+                issued = it + 1;
+                if (++ks == nk)
+                    ks = 0;
+                if (++s == XST) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            for (int it = issued - 1; it >= 0 && it >= issued - XST; --it)
+                mbar_wait(x_full0 + 8 * (it % XST), (it / XST) & 1, 1000000000ull);
+        }
+        __syncwarp();
+    } else if (warp == kWarpM) {
+        // ------------------------------ MMA issuer -----------------------------
         if (lane == 0) {
             int seg = 0;
+            int ks = it0 % nk, sx = 0, b = 0;
+            uint32_t phx = 0, pha = 0;
             for (int it = 0; it < n_it; ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
-                const int gi = it0 + it, ks = gi % nk;
                 const bool seg_start = (it == 0) || (ks == 0);
                 const bool seg_end = (ks == nk - 1) || (it == n_it - 1);
                 bool ok = true;
                 if (seg_start && seg > 0)
                     ok = wait_or_abort(acc_empty, (seg - 1) & 1, a, abort_flag);
-                ok = wait_or_abort(aready0 + 8 * s, ph, a, abort_flag) && ok;
+                ok = wait_or_abort(a_full0 + 8 * b, pha, a, abort_flag) && ok;
+                ok = wait_or_abort(x_full0 + 8 * sx, phx, a, abort_flag) && ok;
                 tc_fence_after();
                 if (ok) {
-                    const uint8_t *st = smem + s * L::STAGE;
-                    const uint32_t xs = smem_u32(st + L::OFF_X);
+                    const uint32_t xs = smem_u32(smem + L::OFF_X + sx * L::XSTAGE);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint32_t b_addr = xs + (j >> 2) * L::XSUB + (j & 3) * 32;
                         const uint64_t bdesc = smem_desc_sw128(b_addr, 1024);
-                        tc_mma_ts(tmem + L::D_COL, tmem + s * 64 + j * 8, bdesc, IDESC,
+                        tc_mma_ts(tmem + L::D_COL, tmem + b * 64 + j * 8, bdesc, IDESC,
                                   (j > 0 || !seg_start) ? 1u : 0u);
                     }
                 }
-                tc_commit(empty0 + 8 * s);
+                // each commit arrives once every MMA issued so far has completed
+                tc_commit(a_empty0 + 8 * b);
+                tc_commit(x_empty0 + 8 * sx);
                 if (seg_end) {
                     tc_commit(acc_full);
                     ++seg;
+                }
+                if (++ks == nk)
+                    ks = 0;
+                if (++sx == XST) {
+                    sx = 0;
+                    phx ^= 1;
+                }
+                if (++b == kNA) {
+                    b = 0;
+                    pha ^= 1;
                 }
             }
             tc_commit(final_bar);
@@ -239,125 +343,178 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------ decode warps --------------------------
-        const int q = warp & 3, h = warp >> 2;
+        // warp (q, c): rows 32q..32q+31 of the block (= TMEM lanes), columns
+        // [kKW c, kKW c + kKW) of each 128-column step
+        const int q = warp & 3, c = warp >> 2;
         const int row = 32 * q + lane; // this thread's row in the block = TMEM lane
         const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t rlo = static_cast<uint32_t>(32 * q);
         uint32_t eb2 = 0;
         int cur_rb = -1, seg = 0;
+        int rb = it0 / nk, ks = it0 % nk, s = 0, b = 0;
+        uint32_t ph = 0, pha = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1;
-            bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
+            // window base of a new row block: start the load before waiting
+            uint32_t e_pre = 1u;
+            if (rb != cur_rb && rb * 128 + row < a.N)
+                e_pre = __ldg(a.ebase + rb * 128 + row);
+            bool ok = wait_or_abort(w_full0 + 8 * s, ph, a, abort_flag);
             if (a.inject_stall)
                 ok = wait_or_abort(stall_bar, 0, a, abort_flag) && ok;
+            // After an abort the loop keeps its shape (every warp still meets
+            // every barrier) but works on stale data and reads nothing
+            // through addresses taken from shared memory.
             ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
-            const int gi = it0 + it, rb = gi / nk, ks = gi % nk;
             const int row0 = rb * 128, k0 = ks * 128;
-            const uint8_t *st = smem + s * L::STAGE;
+            const uint8_t *st = smem + s * L::WSTAGE;
             if (rb != cur_rb) {
                 cur_rb = rb;
-                const int n = row0 + row;
-                const uint32_t e = (n < a.N) ? __ldg(a.ebase + n) : 1u;
-                eb2 = (e << 7) | (e << 23);
+                eb2 = (e_pre << 7) | (e_pre << 23);
             }
 
-            // raw planes of this row, columns [64h, 64h + 64) of the step
-            uint32_t v[32];
+            // 1. raw planes of this row: kKW AE bytes (16-byte chunks, 128-byte
+            //    swizzle) and kKW/2 B bytes (64-byte swizzle)
+            constexpr int NA_CH = kKW / 16, NB_W = kKW / 8; // AE chunks, B words
+            uint4 aq[NA_CH];
+            uint32_t bwords[NB_W];
             {
                 const uint8_t *ae_row = st + L::OFF_AE + row * 128;
                 const uint8_t *b_row = st + L::OFF_B + row * 64;
-                uint4 bq[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+#pragma unroll
+                for (int i = 0; i < NA_CH; ++i)
+                    aq[i] = *reinterpret_cast<const uint4 *>(ae_row + (((NA_CH * c + i) ^ (row & 7)) << 4));
+#pragma unroll
+                for (int i = 0; i < NB_W; ++i)
+                    bwords[i] = 0u;
                 if (!Q8) {
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int c = (2 * h + i) ^ ((row >> 1) & 3);
-                        bq[i] = *reinterpret_cast<const uint4 *>(b_row + c * 16);
+                    for (int i = 0; i < NB_W / 4; ++i) {
+                        const uint4 w4 = *reinterpret_cast<const uint4 *>(
+                            b_row + ((((NB_W / 4) * c + i) ^ ((row >> 1) & 3)) << 4));
+                        bwords[4 * i] = w4.x;
+                        bwords[4 * i + 1] = w4.y;
+                        bwords[4 * i + 2] = w4.z;
+                        bwords[4 * i + 3] = w4.w;
                     }
-                }
-                const uint32_t bwords[8] = {bq[0].x, bq[0].y, bq[0].z, bq[0].w,
-                                            bq[1].x, bq[1].y, bq[1].z, bq[1].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = (4 * h + i) ^ (row & 7);
-                    const uint4 aq = *reinterpret_cast<const uint4 *>(ae_row + c * 16);
-                    decode_group<Q8>(aq.x, aq.y, Q8 ? 0u : bwords[2 * i], eb2, v + 8 * i);
-                    decode_group<Q8>(aq.z, aq.w, Q8 ? 0u : bwords[2 * i + 1], eb2, v + 8 * i + 4);
                 }
             }
 
+            // 2. does any escape fall in this warp's 32 rows x kKW columns?  Only
+            //    then is the stage kept until the patch has read the list.
+            bool any = false;
+            uint32_t list_lb = 0, list_ub = 0, esc_lo = 0, esc_cnt = 0;
+            const uint32_t kb = static_cast<uint32_t>((k0 & 255) + kKW * c);
             if (!Q8) {
-                // escapes inside this warp's 32 rows x 64 columns: patch through
-                // a per-warp scratch tile in shared memory
-                const uint32_t *hdr = reinterpret_cast<const uint32_t *>(st + L::OFF_ESC);
-                const uint32_t lo = hdr[0], hi = hdr[1];
+                const uint8_t *esc_area = st + L::OFF_ESC;
+                const uint32_t lo = *reinterpret_cast<const uint32_t *>(esc_area);
+                const uint32_t hi = *reinterpret_cast<const uint32_t *>(esc_area + 4);
                 const uint32_t cnt = ok ? hi - lo : 0u;
-                const uint32_t *list = (cnt <= static_cast<uint32_t>(L::ESC_CAP)) ? hdr + 4 : a.esc + lo;
-                const uint32_t kb = static_cast<uint32_t>((k0 & 255) + 64 * h);
-                const uint32_t rlo = static_cast<uint32_t>(32 * q);
-                bool any = false;
-                for (uint32_t j = 0; j < cnt; j += 32) {
-                    const uint32_t idx = j + lane;
-                    const uint32_t e = idx < cnt ? list[idx] : 0xFFFFFFFFu;
-                    const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
-                    const bool hit = idx < cnt && r7 - rlo < 32u && k8 - kb < 64u;
-                    any |= __any_sync(0xffffffffu, hit);
-                }
-                if (any) {
-                    uint8_t *scr = smem + L::OFF_SCR + warp * 32 * kScrPitch;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(scr + lane * kScrPitch + c * 16) =
-                            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                    __syncwarp();
-                    for (uint32_t j = 0; j < cnt; j += 32) {
-                        const uint32_t idx = j + lane;
-                        const uint32_t e = idx < cnt ? list[idx] : 0xFFFFFFFFu;
-                        const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
-                        if (idx < cnt && r7 - rlo < 32u && k8 - kb < 64u)
-                            *reinterpret_cast<uint16_t *>(scr + (r7 - rlo) * kScrPitch + (k8 - kb) * 2) =
-                                static_cast<uint16_t>(e & 0xFFFFu);
+                esc_lo = lo;
+                esc_cnt = cnt;
+                if (cnt) {
+                    const uint16_t *gp = reinterpret_cast<const uint16_t *>(esc_area + L::ESC_GP);
+                    list_lb = gp[4 * q];
+                    list_ub = (q == 3) ? cnt : gp[4 * q + 4];
+                    if (list_ub > cnt)
+                        list_ub = cnt;
+                    auto hit = [&](uint32_t e) {
+                        return (e >> 24) - rlo < 32u && ((e >> 16) & 0xFFu) - kb < static_cast<uint32_t>(kKW);
+                    };
+                    if (cnt <= static_cast<uint32_t>(L::ESC_CAP)) {
+                        const uint32_t *list = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
+                        for (uint32_t j = list_lb; j < list_ub && !any; j += 32) {
+                            const uint32_t idx = j + lane;
+                            any = __any_sync(0xffffffffu, idx < list_ub && hit(list[idx]));
+                        }
+                    } else { // more entries than fit in the stage: read them from global memory
+                        const uint32_t *list = a.esc + lo;
+                        for (uint32_t j = list_lb; j < list_ub && !any; j += 32) {
+                            const uint32_t idx = j + lane;
+                            any = __any_sync(0xffffffffu, idx < list_ub && hit(__ldg(list + idx)));
+                        }
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 w4 = *reinterpret_cast<const uint4 *>(scr + lane * kScrPitch + c * 16);
-                        v[4 * c] = w4.x;
-                        v[4 * c + 1] = w4.y;
-                        v[4 * c + 2] = w4.z;
-                        v[4 * c + 3] = w4.w;
-                    }
-                    __syncwarp();
                 }
             }
+            // 3. without escapes here the stage is no longer needed: hand it back
+            if (!any) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(w_empty0 + 8 * s);
+            }
 
-            tmem_st32(tmem + t_lane + static_cast<uint32_t>(s * 64 + 32 * h), v);
+            // 4. decode to exact BF16 pairs
+            uint32_t v[kCols];
+#pragma unroll
+            for (int i = 0; i < NA_CH; ++i) {
+                decode_group<Q8>(aq[i].x, aq[i].y, bwords[2 * i], eb2, v + 8 * i);
+                decode_group<Q8>(aq[i].z, aq[i].w, bwords[2 * i + 1], eb2, v + 8 * i + 4);
+            }
+
+            // 5. patch escapes through this warp's scratch tile, then release
+            if (!Q8 && any) {
+                uint8_t *scr = smem + L::OFF_SCR + warp * 32 * kScrPitch;
+#pragma unroll
+                for (int i = 0; i < kCols / 4; ++i)
+                    *reinterpret_cast<uint4 *>(scr + lane * kScrPitch + i * 16) =
+                        make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                __syncwarp();
+                auto put = [&](uint32_t e) {
+                    const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
+                    if (r7 - rlo < 32u && k8 - kb < static_cast<uint32_t>(kKW))
+                        *reinterpret_cast<uint16_t *>(scr + (r7 - rlo) * kScrPitch + (k8 - kb) * 2) =
+                            static_cast<uint16_t>(e & 0xFFFFu);
+                };
+                if (esc_cnt <= static_cast<uint32_t>(L::ESC_CAP)) {
+                    const uint32_t *list = reinterpret_cast<const uint32_t *>(st + L::OFF_ESC + L::ESC_LIST);
+                    for (uint32_t j = list_lb + lane; j < list_ub; j += 32)
+                        put(list[j]);
+                } else {
+                    for (uint32_t j = list_lb + lane; j < list_ub; j += 32)
+                        put(__ldg(a.esc + esc_lo + j));
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < kCols / 4; ++i) {
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(scr + lane * kScrPitch + i * 16);
+                    v[4 * i] = w4.x;
+                    v[4 * i + 1] = w4.y;
+                    v[4 * i + 2] = w4.z;
+                    v[4 * i + 3] = w4.w;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(w_empty0 + 8 * s);
+            }
+
+            // 6. into tensor memory, once the MMA is done with this A buffer
+            wait_or_abort(a_empty0 + 8 * b, pha ^ 1, a, abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            tmem_store(tmem + t_lane + static_cast<uint32_t>(b * 64 + kCols * c), v);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(aready0 + 8 * s);
-                mbar_arrive(empty0 + 8 * s);
-            }
+            if (lane == 0)
+                mbar_arrive(a_full0 + 8 * b);
 
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- accumulators of this row block are final: read them out ----
                 wait_or_abort(acc_full, seg & 1, a, abort_flag);
                 __syncwarp();
                 tc_fence_after();
-                constexpr int HALF = MT / 2;
-                float out[HALF];
-                const uint32_t dcol = tmem + t_lane + L::D_COL + h * HALF;
-                if constexpr (HALF == 32) {
-                    uint32_t d[32];
-                    tmem_ld32(dcol, d);
+                constexpr int PART = MT / kKQ; // accumulator columns read by this warp
+                float out[PART];
+                const uint32_t dcol = tmem + t_lane + L::D_COL + c * PART;
+                if constexpr (PART == 4) {
+                    uint32_t d[4];
+                    tmem_ld4(dcol, d);
                     tc_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
+                    for (int j = 0; j < 4; ++j)
                         out[j] = __uint_as_float(d[j]);
                 } else {
 #pragma unroll
-                    for (int c8 = 0; c8 < HALF / 8; ++c8) {
+                    for (int c8 = 0; c8 < PART / 8; ++c8) {
                         uint32_t d[8];
                         tmem_ld8(dcol + 8 * c8, d);
                         tc_wait_ld();
@@ -378,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
                 const int n = row0 + row;
 #pragma unroll
-                for (int j = 0; j < HALF; ++j) {
-                    const int m = h * HALF + j;
+                for (int j = 0; j < PART; ++j) {
+                    const int m = c * PART + j;
                     if (m < a.M) {
                         if (direct) {
                             if (n < a.N)
@@ -390,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!direct) {
+                    // the CTA barrier orders every thread's partial stores before
+                    // thread 0's GPU-scope fence and arrival, and thread 0's fence
+                    // after the last arrival before everyone's reads
                     named_bar_sync(1, kDecodeWarps * 32);
                     if (threadIdx.x == 0) {
                         __threadfence();
@@ -403,11 +563,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sk_reduce_block(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);
                 }
             }
+            if (++ks == nk) {
+                ks = 0;
+                ++rb;
+            }
+            if (++s == WST) {
+                s = 0;
+                ph ^= 1;
+            }
+            if (++b == kNA) {
+                b = 0;
+                pha ^= 1;
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kDecodeWarps + 1) {
+    if (warp == kWarpM) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

@@ -1,5 +1,6 @@
 // runtime.cu -- device side of the C ABI: upload of encoded matrices, TMA
 // descriptors, the per-stream GEMM workspace cache and kernel dispatch.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <map>
@@ -161,7 +162,10 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     if (!w->gemm_ok)
         return W12_ERR_UNSUPPORTED;
 
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    // Kernel choice, a function of M only (measured on GB300): the CUDA-core
+    // kernel for M <= 4; above that the tensor-core kernel, padding M to 16,
+    // 32 or 64 rows, is faster than packed FMAs for 8 rows.
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
     const bool tc = mt >= 16;
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
@@ -184,7 +188,12 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     a.total_iters = static_cast<int>(iters);
     a.limit_ns = g_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
-    const int grid = static_cast<int>(std::min<int64_t>(sm_count(cur), iters));
+    // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
+    // streams several times the weight bytes of the partial sums it writes
+    // (a 128 x 128 tensor-core step reads 24 KB of W12, its partial is M x 512 B)
+    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 11) / 12) : 1;
+    const int64_t want = std::max<int64_t>(a.n_rowblk, iters / min_iters);
+    const int grid = static_cast<int>(std::min<int64_t>(sm_count(cur), std::min<int64_t>(iters, want)));
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters, &a.epoch);
