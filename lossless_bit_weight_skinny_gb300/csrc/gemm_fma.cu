@@ -9,42 +9,46 @@
 // one persistent CTA per SM (stream-K), and row blocks shared by several CTAs
 // are combined by the last contributor in a fixed order.
 //
-// CTA = CW consumer warps + 1 producer warp.  The producer streams each
-// block's AE bytes, B words and x slice with TMA into a ring of shared-memory
-// stages, and copies the tile's escape entries and row-group index next to
-// them with cp.async.  Consumer warp w owns RW rows of the block; lane l owns
-// columns 8l..8l+7 of the 256-column step and keeps the products of its rows
-// in registers until the row block ends, then the warp reduces across lanes.
+// CTA = CW consumer warps + a producer warp + an escape warp.  The producer
+// streams each block's AE bytes, B words and x slice with TMA into a ring of
+// shared-memory stages, and copies the tile's escape entries next to them with
+// cp.async.  Consumer warp w owns RW rows of the block; lane l owns columns
+// 8l..8l+7 of the 256-column step and keeps the products of its rows in
+// registers until the row block ends, then the warp reduces across lanes.
 //
 // Escapes: the main loop multiplies every slot as decoded -- an escaped slot
-// holds the placeholder +-2^(ebase-127) -- and has no branches.  After each
-// step the warp walks its own escapes (a contiguous run of the tile's sorted
-// list) and accumulates, per output, the two exact-order correction sums
-// sum(-x * placeholder) and sum(x * exact value), added to the output in that
-// order at the end.  With a single non-zero product (one-hot x) this gives the
-// exact escaped value back, Inf/NaN escapes propagate, and otherwise the
-// result is the same sum in another order.
+// holds the placeholder +-2^(ebase-127) -- and has no branches and no escape
+// work at all.  The escape warp walks each stage's list and keeps, per output,
+// the two correction sums sum(-x * placeholder) and sum(x * exact value) in
+// shared memory; the consumers add them to the output in that order at the
+// end of the row block.  With a single non-zero product (one-hot x) this gives
+// the exact escaped value back, Inf/NaN escapes propagate, and otherwise the
+// result is the same sum in another (fixed) order.
 #include "kernels.cuh"
 
 namespace w12 {
 namespace {
 
 #ifndef W12_FMA_CW
-#define W12_FMA_CW 8 // consumer warps of the M <= 4 kernels (8 or 16)
+#define W12_FMA_CW 0 // consumer warps (8 or 16); 0 = 16 for M = 1, 8 otherwise
 #endif
 #ifndef W12_FMA_MIXED
 #define W12_FMA_MIXED 1 // M <= 2: BF16 x BF16 -> FP32 FMAs instead of packed FP32 FMAs
 #endif
 
+#ifndef W12_FMA_RBLK
+#define W12_FMA_RBLK 128 // rows per block (and per ring stage): 128 or 64
+#endif
+
 template <int MT>
 struct FmaShape {
-    static constexpr int RBLK = (MT <= 4) ? 128 : 64;         // rows per block
-    static constexpr int CW = (MT <= 4) ? W12_FMA_CW : 8;     // consumer warps
+    static constexpr int RBLK = W12_FMA_RBLK;                 // rows per block
+    static constexpr int CW = W12_FMA_CW ? W12_FMA_CW : (MT == 1 ? 16 : 8); // consumer warps
     static constexpr int RW = RBLK / CW;                      // rows per consumer warp
-    static constexpr int THREADS = (CW + 1) * 32;
+    static constexpr int THREADS = (CW + 2) * 32; // + producer + escape warp
     // registers per thread for one resident CTA: each of the 4 SM sub-partitions
     // has 16K registers and holds ceil(warps / 4) of the CTA's warps
-    static constexpr int PER_SMSP = (CW + 1 + 3) / 4;
+    static constexpr int PER_SMSP = (CW + 2 + 3) / 4;
     static constexpr int MAXREG_RAW = (16384 / (32 * PER_SMSP)) & ~7;
     static constexpr int MAXREG = MAXREG_RAW > 255 ? 255 : MAXREG_RAW;
     static_assert(RW % 8 == 0 && RBLK % CW == 0, "warps own whole 8-row escape groups");
@@ -59,21 +63,25 @@ struct FmaSmem {
     static constexpr int AE = S::RBLK * 256;
     static constexpr int B = Q8 ? 0 : S::RBLK * 128;
     static constexpr int X = MT * 256 * 2;
-    static constexpr int ESC_CAP = 512;
-    // escape area: [lo, hi, -, -] u32 | row-group index u16[16] | entries
-    static constexpr int ESC_GP = 16;
-    static constexpr int ESC_LIST = 48;
+    static constexpr int ESC_CAP = 256; // more entries in a tile are read from global memory
+    // escape area: [lo, hi, -, -] u32 | entries
+    static constexpr int ESC_LIST = 16;
     static constexpr int ESC = Q8 ? 0 : ESC_LIST + ESC_CAP * 4;
     static constexpr int OFF_AE = 0;
     static constexpr int OFF_B = r128(AE);
     static constexpr int OFF_X = OFF_B + r128(B);
     static constexpr int OFF_ESC = OFF_X + r128(X);
     static constexpr int STAGE = r1024(OFF_ESC + ESC);
-    static constexpr int STAGES_RAW = (212 * 1024) / STAGE;
+    static constexpr int CORR = Q8 ? 0 : 2 * 2 * S::RBLK * MT * 4; // correction sums
+    static constexpr int BUDGET = 227 * 1024 - 2048;
+    static constexpr int STAGES_RAW = (BUDGET - CORR) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int TX_BYTES = AE + B + X;
-    static constexpr int BARS = STAGES * STAGE; // barrier area offset
-    static constexpr int TOTAL = BARS + 8 * (2 * STAGES + 1) + 16 + 1024; // + slack to align the base
+    static constexpr int OFF_CORR = STAGES * STAGE;
+    static constexpr int BARS = OFF_CORR + CORR;         // barrier area offset
+    static constexpr int NBARS = 2 * STAGES + 1 + 4;     // full, empty, stall, corr_full/empty
+    static constexpr int TOTAL = BARS + 8 * NBARS + 16 + 1024; // + slack to align the base
+    static_assert(STAGES >= 3 && TOTAL <= 227 * 1024, "shared memory budget");
 };
 
 // Bounded wait that also gives up as soon as another warp has aborted.
@@ -201,14 +209,20 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     constexpr int V = RW * MT;           // per-lane partial sums
     constexpr int VPL = V >= 32 ? V / 32 : 1;
     constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : 3;
+    constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warp
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * STAGES + 1);
-    volatile int *seg_last = abort_flag + 1;
+    // full, empty [STAGES]; stall; corr_full, corr_empty [2]
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t stall_bar = smem_u32(bars + 2 * STAGES);
+    const uint32_t corr_full0 = stall_bar + 8, corr_empty0 = stall_bar + 24;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + L::NBARS);
+    volatile int *seg_last = abort_flag + 1;
+    // escape corrections of the current row block, double buffered:
+    // [buffer][neg, pos][RBLK * MT]
+    float *corr = reinterpret_cast<float *>(smem + L::OFF_CORR);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grid = gridDim.x, cta = blockIdx.x;
@@ -219,16 +233,21 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(empty0 + 8 * s, CW);
+            mbar_init(empty0 + 8 * s, Q8 ? CW : CW + 1);
         }
         mbar_init(stall_bar, 1);
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(corr_full0 + 8 * d, 32);
+            mbar_init(corr_empty0 + 8 * d, CW);
+        }
         *abort_flag = 0;
         *seg_last = 0;
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_launch_dependents();
 
-    if (warp == CW) {
+    if (warp == WARP_P) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             prefetch_tmap(&tm_ae);
@@ -248,21 +267,31 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int row0 = rb * RBLK, k0 = ks * 256;
             uint8_t *st = smem + s * L::STAGE;
             const uint32_t fb = full0 + 8 * s;
+            // The first ring's worth of weights streams before the previous
+            // kernel in the stream has finished; activations, which it may have
+            // written, only after it has (every write of this kernel follows an
+            // activation load).
+            const int pre = n_it < STAGES ? n_it : STAGES;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::TX_BYTES);
                 tma_load_2d(smem_u32(st + L::OFF_AE), &tm_ae, k0, row0, fb);
                 if (!Q8)
                     tma_load_2d(smem_u32(st + L::OFF_B), &tm_b, k0 / 2, row0, fb);
-                tma_load_2d(smem_u32(st + L::OFF_X), &tm_x, k0, 0, fb);
+                if (it >= pre)
+                    tma_load_2d(smem_u32(st + L::OFF_X), &tm_x, k0, 0, fb);
+                if (it == pre - 1) {
+                    pdl_wait_prior_grid();
+                    for (int j = 0; j < pre; ++j)
+                        tma_load_2d(smem_u32(smem + j * L::STAGE + L::OFF_X), &tm_x,
+                                    ((it0 + j) % nk) * 256, 0, full0 + 8 * j);
+                }
             }
             if (!Q8) {
-                const int t = (row0 / 128) * a.tiles_c + ks;
+                // the tile's entry range, then its entries (up to ESC_CAP)
                 uint8_t *esc_area = st + L::OFF_ESC;
                 if (lane < 2)
-                    cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
-                else if (lane < 4)
-                    cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
-                                a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
+                    cp_async_4(smem_u32(esc_area + 4 * lane),
+                               a.tile_ptr + (row0 / 128) * a.tiles_c + ks + lane);
                 if (win < 0 || it - win >= 32) {
                     win = it;
                     const int gj = it0 + it + lane;
@@ -295,24 +324,115 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int s = it % STAGES;
             mbar_wait(full0 + 8 * s, (it / STAGES) & 1, 1000000000ull);
         }
+    } else if (warp == WARP_E) {
+        // ---------------------------- escape warp -----------------------------
+        // Per stage, the tile's entries 32 at a time, one per lane: the two
+        // products -x * placeholder and x * exact value for each activation
+        // row, summed per output row by a segmented scan over the lanes (the
+        // list is sorted by row), then added to the row's correction sums.
+        // Fixed order throughout, so results are reproducible.
+        if (!Q8) {
+            int seg = 0;
+            int rb = it0 / nk, ks = it0 % nk, s = 0;
+            uint32_t ph = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const bool seg_start = (it == 0) || (ks == 0);
+                const bool seg_end = (ks == nk - 1) || (it == n_it - 1);
+                const int db = seg & 1;
+                float *cneg = corr + db * (2 * RBLK * MT), *cpos = cneg + RBLK * MT;
+                if (seg_start) {
+                    // buffer db was last read by the consumers at the end of segment seg - 2
+                    if (seg >= 2)
+                        wait_or_abort(corr_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
+                    for (int i = lane; i < 2 * RBLK * MT; i += 32)
+                        cneg[i] = 0.f;
+                    __syncwarp();
+                }
+                bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                const int row0 = rb * RBLK;
+                const uint8_t *st = smem + s * L::STAGE;
+                if (ok) {
+                    const uint8_t *esc_area = st + L::OFF_ESC;
+                    const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
+                    const uint32_t cnt = lohi.y - lohi.x;
+                    const bool big = cnt > static_cast<uint32_t>(L::ESC_CAP);
+                    const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
+                    const uint32_t rbase = static_cast<uint32_t>(row0 & 127);
+                    for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
+                        const uint32_t j = j0 + static_cast<uint32_t>(lane);
+                        uint32_t e = 0;
+                        if (j < cnt) {
+                            if (big)
+                                e = __ldg(a.esc + lohi.x + j);
+                            else
+                                e = list_s[j];
+                        }
+                        const uint32_t r = (e >> 24) - rbase; // row in the block
+                        const bool in = j < cnt && r < static_cast<uint32_t>(RBLK) &&
+                                        row0 + static_cast<int>(r) < a.N;
+                        const uint32_t k8 = (e >> 16) & 0xFFu;
+                        const uint32_t eb = in ? __ldg(a.ebase + row0 + r) : 0u;
+                        const float wph = __uint_as_float(((e & 0x8000u) << 16) | (eb << 23));
+                        const float wex = __uint_as_float((e & 0xFFFFu) << 16);
+                        float pn[MT], pp[MT];
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const uint32_t xb = *reinterpret_cast<const uint16_t *>(st + L::OFF_X + m * 512 + k8 * 2);
+                            const float xv = __uint_as_float(xb << 16);
+                            pn[m] = in ? -(xv * wph) : 0.f; // both products are exact in FP32
+                            pp[m] = in ? xv * wex : 0.f;
+                        }
+                        const uint32_t key = in ? r : 256u + static_cast<uint32_t>(lane);
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const uint32_t kp = __shfl_up_sync(0xffffffffu, key, d);
+                            const bool take = lane >= d && kp == key;
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                const float an = __shfl_up_sync(0xffffffffu, pn[m], d);
+                                const float ap = __shfl_up_sync(0xffffffffu, pp[m], d);
+                                if (take) {
+                                    pn[m] = an + pn[m];
+                                    pp[m] = ap + pp[m];
+                                }
+                            }
+                        }
+                        const uint32_t kn = __shfl_down_sync(0xffffffffu, key, 1);
+                        if (in && (lane == 31 || kn != key)) {
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) {
+                                cneg[r * MT + m] += pn[m];
+                                cpos[r * MT + m] += pp[m];
+                            }
+                        }
+                        __syncwarp();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty0 + 8 * s);
+                if (seg_end) {
+                    mbar_arrive(corr_full0 + 8 * db); // all 32 lanes: their sums are visible
+                    ++seg;
+                }
+                if (++ks == nk) {
+                    ks = 0;
+                    ++rb;
+                }
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
     } else {
         // ------------------------------ consumers -----------------------------
         const int wrow = warp * RW;
         float acc[MT <= 2 ? 1 : RW][MT <= 2 ? 1 : MT];
         float2 acc2[MT <= 2 ? RW : 1][MT <= 2 ? MT : 1];
         uint32_t eb2[RW];
-        // the (row, m) outputs whose escape corrections this lane keeps:
-        // index i = r * MT + m, i = lane (V <= 32) or 2 lane + q (V = 64)
-        float cneg[VPL], cpos[VPL];
-        uint32_t cph[VPL]; // placeholder magnitude bits of the pair's row (eb << 23)
-        int cr[VPL], cm[VPL];
-#pragma unroll
-        for (int q = 0; q < VPL; ++q) {
-            const int i = (V >= 32) ? lane * VPL + q : lane;
-            cr[q] = (i < V) ? i / MT : -1; // -1: this lane keeps no output
-            cm[q] = (i < V) ? i % MT : 0;
-        }
-        int cur_rb = -1;
+        int cur_rb = -1, seg = 0;
         int rb = it0 / nk, ks = it0 % nk; // (row block, k step) of iteration it
         int s = 0;
         uint32_t ph = 0;
@@ -324,13 +444,11 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 if (lane < RW && n < a.N)
                     e_pre = __ldg(a.ebase + n);
             }
-            bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
+            wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
             if (a.inject_stall)
-                ok = wait_or_abort(stall_bar, 0, a, abort_flag) && ok;
+                wait_or_abort(stall_bar, 0, a, abort_flag);
             // After an abort the loop keeps its shape (every warp still meets
-            // every named barrier) but works on stale data and reads nothing
-            // through addresses taken from shared memory.
-            ok = __all_sync(0xffffffffu, ok);
+            // every barrier) but works on stale data.
             const int row0 = rb * RBLK;
             const uint8_t *st = smem + s * L::STAGE;
 
@@ -350,12 +468,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 for (int r = 0; r < RW; ++r) {
                     const uint32_t er = __shfl_sync(0xffffffffu, e, r);
                     eb2[r] = (er << 7) | (er << 23);
-                }
-#pragma unroll
-                for (int q = 0; q < VPL; ++q) {
-                    cneg[q] = 0.f;
-                    cpos[q] = 0.f;
-                    cph[q] = __shfl_sync(0xffffffffu, e, cr[q] & 31) << 23;
                 }
             }
 
@@ -378,61 +490,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 }
             }
 
-            if (!Q8) {
-                // this warp's escapes: its RW rows are whole 8-row groups of the tile
-                const uint8_t *esc_area = st + L::OFF_ESC;
-                const uint32_t lo = *reinterpret_cast<const uint32_t *>(esc_area);
-                const uint32_t hi = *reinterpret_cast<const uint32_t *>(esc_area + 4);
-                const uint32_t cnt = ok ? hi - lo : 0u;
-                if (cnt) {
-                    const uint16_t *gp = reinterpret_cast<const uint16_t *>(esc_area + L::ESC_GP);
-                    const int g = ((row0 & 127) + wrow) >> 3; // first 8-row group of this warp
-                    const uint32_t lb = gp[g];
-                    const uint32_t ub = (g + RW / 8 >= 16) ? cnt : gp[g + RW / 8];
-                    // entries are fetched 4 at a time (independent loads), then
-                    // applied strictly in list order
-                    const uint32_t pend = ub < cnt ? ub : cnt;
-                    const bool in_smem = cnt <= static_cast<uint32_t>(L::ESC_CAP);
-                    const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
-                    const uint32_t *list_g = a.esc + lo; // when more than fit in the stage
-                    const int rbase = (row0 & 127) + wrow;
-                    for (uint32_t p = lb; p < pend; p += 4) {
-                        uint32_t e[4];
-                        if (in_smem) {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                e[u] = (p + u < pend) ? list_s[p + u] : 0xFFFFFFFFu;
-                        } else {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                e[u] = (p + u < pend) ? __ldg(list_g + p + u) : 0xFFFFFFFFu;
-                        }
-                        float xv[4][VPL];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-#pragma unroll
-                            for (int q = 0; q < VPL; ++q) {
-                                const uint32_t k8 = (e[u] >> 16) & 0xFFu;
-                                const uint32_t xb =
-                                    *reinterpret_cast<const uint16_t *>(st + L::OFF_X + cm[q] * 512 + k8 * 2);
-                                xv[u][q] = __uint_as_float(xb << 16);
-                            }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int r = static_cast<int>(e[u] >> 24) - rbase; // 255 - .. for padding
-                            const float wex = __uint_as_float((e[u] & 0xFFFFu) << 16);
-#pragma unroll
-                            for (int q = 0; q < VPL; ++q) {
-                                if (cr[q] == r) {
-                                    const float wph = __uint_as_float(((e[u] & 0x8000u) << 16) | cph[q]);
-                                    cneg[q] = fmaf(xv[u][q], -wph, cneg[q]);
-                                    cpos[q] = fmaf(xv[u][q], wex, cpos[q]);
-                                }
-                            }
-                        }
-                    }
-                }
-            }
             // For M = 1 the warp's raw planes fit in registers: load them all and
             // hand the stage back to the producer before computing on them, so
             // the refill overlaps the arithmetic.  Larger M reads them row by
@@ -498,7 +555,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     mbar_arrive(empty0 + 8 * s);
             }
 
-
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- the row block ends here for this CTA: reduce and store ----
                 float v[V];
@@ -512,6 +568,12 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                             v[r * MT + m] = acc[r][m];
                     }
                 XReduce<V, 16>::run(v, lane);
+                // this segment's escape corrections (complete once the escape
+                // warp has passed the segment's last stage)
+                const int db = seg & 1;
+                if (!Q8)
+                    wait_or_abort(corr_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
+                const float *cneg = corr + db * (2 * RBLK * MT), *cpos = cneg + RBLK * MT;
                 const int c_first = sk_owner(rb * nk, grid, a.total_iters);
                 const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
                 const bool writer = (V >= 32) || ((lane & ((32 >> LOGV) - 1)) == 0);
@@ -520,14 +582,11 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
 #pragma unroll
                 for (int q = 0; q < VPL; ++q) {
                     const int idx = (V >= 32) ? lane * VPL + q : (lane >> (5 - LOGV));
-                    float cn = cneg[q], cp = cpos[q];
-                    if constexpr (V < 32) {
-                        cn = __shfl_sync(0xffffffffu, cneg[0], idx);
-                        cp = __shfl_sync(0xffffffffu, cpos[0], idx);
-                    }
-                    // the placeholder products out first, then the exact ones in
-                    const float total = (v[q] + cn) + cp;
                     const int r = idx / MT, m = idx % MT;
+                    // the placeholder products out first, then the exact ones in
+                    float total = v[q];
+                    if (!Q8)
+                        total = (total + cneg[(wrow + r) * MT + m]) + cpos[(wrow + r) * MT + m];
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
                         if (direct) {
@@ -538,6 +597,12 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                         }
                     }
                 }
+                if (!Q8) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(corr_empty0 + 8 * db);
+                }
+                ++seg;
                 if (!direct) {
                     // the CTA barrier orders every thread's partial stores before
                     // thread 0's GPU-scope fence and arrival (cumulativity), and
@@ -582,13 +647,12 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtens
             return e;
         attr_done = true;
     }
-    kern<<<grid, FmaShape<MT>::THREADS, L::TOTAL, st>>>(a, *tm_ae, *tm_b, *tm_x);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, FmaShape<MT>::THREADS, L::TOTAL, st, a, *tm_ae, *tm_b, *tm_x);
 }
 
 } // namespace
 
-int fma_rows_blk(int mt) { return mt <= 4 ? 128 : 64; }
+int fma_rows_blk(int) { return W12_FMA_RBLK; }
 
 int fma_smem_bytes(int mt, bool q8)
 {

@@ -1,53 +1,59 @@
-// gemm_tc.cu -- W12 skinny GEMM for 5..64 activation rows on the tcgen05
-// tensor cores.
+// gemm_tc.cu -- W12 skinny GEMM on the tcgen05 tensor cores (activation rows
+// padded to MT = 16, 32 or 64).
 //
 // The product is computed transposed: D[n][m] = sum_k W[n][k] x[m][k], with the
 // decoded weight tile as the MMA "A" operand (128 output channels x 16 k per
-// instruction) and the activation tile as "B" (MT = 16, 32 or 64 rows, zero
-// padded), FP32 accumulators in tensor memory.  This is the Blackwell form of
-// decoding W12 records on the fly and feeding them to the tensor cores
-// (SpecPilot, Figure 5(b) caption): instead of a register operand, the decode
-// warps write the exact BF16 weights straight into tensor memory with
-// tcgen05.st and the MMA reads A from there, so decoded weights never touch
-// shared memory.
+// instruction) and the activation tile as "B" (MT rows, zero padded), FP32
+// accumulators in tensor memory.  This is the Blackwell form of decoding W12
+// records on the fly and feeding them to the tensor cores (SpecPilot, Figure
+// 5(b) caption): instead of a register operand, the decode warps write the
+// exact BF16 weights straight into tensor memory with tcgen05.st and the MMA
+// reads A from there, so decoded weights never touch shared memory.
+//
+// Work unit: 128 rows x 256 columns, exactly one escape tile.  The (row block,
+// k step) units are split evenly over one persistent CTA per SM (stream-K);
+// row blocks shared by several CTAs are combined by the last contributor in a
+// fixed order.
 //
 // CTA = 16 decode warps + a weight-TMA warp + an activation-TMA warp + an MMA
 // warp, over three independent rings:
-//   * weights (AE, B, escapes) in shared memory: a decode warp copies its share
-//     of a stage into registers and releases the slot at once, so the weight
-//     stream never waits for the tensor cores;
-//   * activations (the B operand) in shared memory, released by the MMA;
-//   * decoded weights (the A operand) in tensor memory, released by the MMA.
-// Work split and split-K fix-up are the stream-K scheme of the CUDA-core
-// kernel, over blocks of 128 rows x 128 columns (half an escape tile).
+//   * weights (AE, B, the tile's escape entries) in shared memory;
+//   * activations (the MMA's B operand) in shared memory, released by the MMA;
+//   * decoded weights (the A operand, 128 TMEM columns per unit), released by
+//     the MMA.
+// Decode warp (q, c) owns rows 32q..32q+31 of the unit (its TMEM lane
+// quadrant) and columns 64c..64c+63.  Each thread decodes 64 weights of its
+// row into 32 BF16x2 registers and stores them with one tcgen05.st.  Escapes
+// are then patched in tensor memory: the warp finds the entries of its
+// quadrant that fall in its columns with one ballot, and for each rewrites the
+// one 32-bit column holding the slot (load, replace the 16-bit half in the
+// owning lane, store back; every other lane writes its own value back).
+// Accumulators are double buffered so that the epilogue of one row block
+// overlaps the first products of the next.
 #include "kernels.cuh"
 
 namespace w12 {
 namespace {
 
-#ifndef W12_TC_DECODE_WARPS
-#define W12_TC_DECODE_WARPS 16
-#endif
-constexpr int kDecodeWarps = W12_TC_DECODE_WARPS; // 8 or 16
-constexpr int kKQ = kDecodeWarps / 4;  // decode warps per 32-row quadrant
-constexpr int kKW = 128 / kKQ;         // columns of a 128-column step per decode warp
-constexpr int kCols = kKW / 2;         // TMEM columns (BF16 pairs) per decode warp
+constexpr int kDecodeWarps = 16;
 constexpr int kWarpW = kDecodeWarps;     // weight producer
 constexpr int kWarpX = kDecodeWarps + 1; // activation producer
 constexpr int kWarpM = kDecodeWarps + 2; // MMA issuer, tensor-memory owner
 constexpr int kThreads = (kDecodeWarps + 3) * 32;
-constexpr int kScrPitch = 2 * kKW + 16; // escape scratch row pitch (bytes): kKW BF16 + pad
-constexpr int kNA = 4;         // A buffers in tensor memory (64 columns each)
+constexpr int kNA = 3;                   // A buffers in tensor memory, 128 columns each
+constexpr uint32_t kDCol = kNA * 128;    // two accumulator buffers of 64 columns
+static_assert(kTcKStep == 256 && kTcRows == 128, "one unit = one escape tile");
 
-constexpr int a128(int v) { return (v + 127) & ~127; }
 constexpr int a1024(int v) { return (v + 1023) & ~1023; }
 
 template <int MT, bool Q8>
 struct TcSmem {
-    // weight stage: AE (SWIZZLE_128B), B (SWIZZLE_64B), escape area
-    static constexpr int AE = 128 * 128;
-    static constexpr int B = Q8 ? 0 : 128 * 64;
-    static constexpr int ESC_CAP = 512;
+    // weight stage: AE as two 128-column halves and B, each 128 rows of 128
+    // bytes with the 128-byte swizzle, then the escape area
+    static constexpr int AE_HALF = 128 * 128;
+    static constexpr int AE = 2 * AE_HALF;
+    static constexpr int B = Q8 ? 0 : 128 * 128;
+    static constexpr int ESC_CAP = 256; // more entries in a tile are read from global memory
     static constexpr int ESC_GP = 16; // [lo, hi, -, -] u32, then the row-group index u16[16]
     static constexpr int ESC_LIST = 48;
     static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
@@ -55,25 +61,23 @@ struct TcSmem {
     static constexpr int OFF_B = AE;
     static constexpr int OFF_ESC = OFF_B + B;
     static constexpr int WSTAGE = a1024(OFF_ESC + ESC);
-    // activation stage: two 64-column sub-tiles of MT rows, SWIZZLE_128B
+    // activation stage: four 64-column sub-tiles of MT rows, 128-byte swizzle
     static constexpr int XSUB = MT * 128;
-    static constexpr int XSTAGE = 2 * XSUB;
-    static constexpr int SCR = Q8 ? 0 : kDecodeWarps * 32 * kScrPitch;
-    static constexpr int BUDGET = 212 * 1024 - SCR;
-    static constexpr int XST = (MT <= 32) ? 4 : 3; // activation slots
+    static constexpr int XSTAGE = 4 * XSUB;
+    static constexpr int XST = (MT <= 32) ? 3 : 2; // activation slots
+    static constexpr int BUDGET = 227 * 1024 - 2048;
     static constexpr int WST_RAW = (BUDGET - XST * XSTAGE) / WSTAGE;
-    static constexpr int WST = WST_RAW > 8 ? 8 : WST_RAW; // weight slots
+    static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight slots
     static constexpr int OFF_X = WST * WSTAGE;
-    static constexpr int OFF_SCR = OFF_X + XST * XSTAGE;
-    static constexpr int BARS = a128(OFF_SCR + SCR);
+    static constexpr int BARS = OFF_X + XST * XSTAGE;
     // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
-    // acc_full, acc_empty, final, stall
-    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4;
+    // acc_full, acc_empty [2]; final, stall
+    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4 + 2;
     static constexpr int TOTAL = BARS + 8 * NBARS + 32 + 1024; // + slack to align the base
     static constexpr int W_TX = AE + B;
-    static constexpr uint32_t D_COL = kNA * 64;
-    static_assert(D_COL + MT <= 512, "tensor memory budget");
+    static_assert(kDCol + 2 * 64 <= 512, "tensor memory budget");
     static_assert(WST >= 3, "weight ring too shallow");
+    static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmArgs &a,
@@ -99,9 +103,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
-// One BF16x2 pair from the AE word holding its two bytes and the B word of its
-// group of 8 (bit layout as in the CUDA-core kernel):
-// sign | (ebase + E) << 7 | (A & 7) << 4 | B per 16-bit lane.
+// One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
+// holding those two bytes and its B word:
+//   PRMT spreads the two AE bytes into two 16-bit lanes, replicating each
+//   byte's sign into the lane's high byte; then per lane
+//   sign (bit 15) | (ebase + E) << 7 | (A & 7) << 4 | B.
 template <int I, bool Q8>
 __device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, uint32_t eb2)
 {
@@ -119,6 +125,7 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, u
     return r;
 }
 
+// 8 weights (AE bytes of the group as two words, its B word) -> 4 BF16x2 pairs.
 template <bool Q8>
 __device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint32_t bw, uint32_t eb2,
                                              uint32_t *out)
@@ -129,18 +136,27 @@ __device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint3
     out[3] = decode_pair<3, Q8>(a_hi, bw, eb2);
 }
 
-template <int N>
-__device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t (&v)[N])
+// Replace the BF16 of escape entry e (row r7 of the unit, column k8) in the A
+// buffer at `abuf` (column = k8 / 2, lane quadrant base `t_lane`).  Warp-wide:
+// every lane reads and writes back its own lane of that column.
+__device__ __forceinline__ void patch_entry(uint32_t e, uint32_t abuf, uint32_t t_lane, uint32_t rlo,
+                                            int lane)
 {
-    static_assert(N == 16 || N == 32, "16 or 32 columns");
-    if constexpr (N == 32)
-        tmem_st32(taddr, v);
-    else
-        tmem_st16(taddr, v);
+    const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
+    const uint32_t addr = abuf + t_lane + (k8 >> 1);
+    uint32_t v = tmem_ld1(addr);
+    tc_wait_ld();
+    if (static_cast<uint32_t>(lane) == r7 - rlo) {
+        const uint32_t bits = e & 0xFFFFu;
+        v = (k8 & 1u) ? ((v & 0x0000FFFFu) | (bits << 16)) : ((v & 0xFFFF0000u) | bits);
+    }
+    tmem_st1(addr, v);
+    tc_wait_st(); // a later patch of the same column reads this value
 }
 
+// 19 warps: 5 per SM sub-partition, whose 16K registers allow 102 per thread
 template <int MT, bool Q8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(96)
     gemm_tc_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
                    const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_x)
@@ -159,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_empty0 = smem_u32(bars + 2 * WST + XST);
     const uint32_t a_full0 = smem_u32(bars + 2 * WST + 2 * XST);
     const uint32_t a_empty0 = smem_u32(bars + 2 * WST + 2 * XST + kNA);
-    const uint32_t acc_full = smem_u32(bars + 2 * WST + 2 * XST + 2 * kNA);
-    const uint32_t acc_empty = acc_full + 8;
-    const uint32_t final_bar = acc_full + 16;
-    const uint32_t stall_bar = acc_full + 24;
+    const uint32_t acc_full0 = smem_u32(bars + 2 * WST + 2 * XST + 2 * kNA);
+    const uint32_t acc_empty0 = acc_full0 + 16;
+    const uint32_t final_bar = acc_full0 + 32;
+    const uint32_t stall_bar = acc_full0 + 40;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + L::NBARS);
     volatile int *seg_last = abort_flag + 1;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
@@ -186,8 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(a_full0 + 8 * b, kDecodeWarps);
             mbar_init(a_empty0 + 8 * b, 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kDecodeWarps);
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(acc_full0 + 8 * d, 1);
+            mbar_init(acc_empty0 + 8 * d, kDecodeWarps);
+        }
         mbar_init(final_bar, 1);
         mbar_init(stall_bar, 1);
         *abort_flag = 0;
@@ -202,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
 
     if (warp == kWarpW) {
         // --------------------------- weight producer ---------------------------
@@ -219,28 +238,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = __all_sync(0xffffffffu, wait_or_abort(w_empty0 + 8 * s, ph ^ 1, a, abort_flag));
             if (!ok)
                 break;
-            const int row0 = rb * 128, k0 = ks * 128;
+            const int row0 = rb * 128, k0 = ks * 256;
             uint8_t *st = smem + s * L::WSTAGE;
             const uint32_t fb = w_full0 + 8 * s;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::W_TX);
                 tma_load_2d(smem_u32(st + L::OFF_AE), &tm_ae, k0, row0, fb);
+                tma_load_2d(smem_u32(st + L::OFF_AE + L::AE_HALF), &tm_ae, k0 + 128, row0, fb);
                 if (!Q8)
                     tma_load_2d(smem_u32(st + L::OFF_B), &tm_b, k0 / 2, row0, fb);
             }
             if (!Q8) {
-                const int t = rb * a.tiles_c + (k0 >> 8);
+                const int t = rb * a.tiles_c + ks;
                 uint8_t *esc_area = st + L::OFF_ESC;
                 if (lane < 2)
                     cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
                 else if (lane < 4)
                     cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
                                 a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
+                // the tile bounds of the next 32 units, one per lane
                 if (win < 0 || it - win >= 32) {
                     win = it;
                     const int gj = it0 + it + lane;
                     if (gj < it0 + n_it) {
-                        const int tj = (gj / nk) * a.tiles_c + ((gj % nk) * 128 >> 8);
+                        const int tj = (gj / nk) * a.tiles_c + gj % nk;
                         my_lo = __ldg(a.tile_ptr + tj);
                         my_hi = __ldg(a.tile_ptr + tj + 1);
                     }
@@ -270,18 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------- activation producer -------------------------
         if (lane == 0) {
             prefetch_tmap(&tm_x);
+            // weights stream before the previous kernel in the stream has
+            // finished; activations, which it may have written, only after it
+            // has (every write of this kernel follows an activation load)
+            pdl_wait_prior_grid();
             int issued = 0;
             int ks = it0 % nk, s = 0;
             uint32_t ph = 0;
             for (int it = 0; it < n_it; ++it) {
                 if (!wait_or_abort(x_empty0 + 8 * s, ph ^ 1, a, abort_flag))
                     break;
-                const int k0 = ks * 128;
+                const int k0 = ks * 256;
                 uint8_t *xs = smem + L::OFF_X + s * L::XSTAGE;
                 const uint32_t fb = x_full0 + 8 * s;
                 mbar_arrive_expect_tx(fb, L::XSTAGE);
-                tma_load_2d(smem_u32(xs), &tm_x, k0, 0, fb);
-                tma_load_2d(smem_u32(xs + L::XSUB), &tm_x, k0 + 64, 0, fb);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tma_load_2d(smem_u32(xs + j * L::XSUB), &tm_x, k0 + 64 * j, 0, fb);
                 issued = it + 1;
                 if (++ks == nk)
                     ks = 0;
@@ -303,27 +329,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; it < n_it; ++it) {
                 const bool seg_start = (it == 0) || (ks == 0);
                 const bool seg_end = (ks == nk - 1) || (it == n_it - 1);
+                const int db = seg & 1;
                 bool ok = true;
-                if (seg_start && seg > 0)
-                    ok = wait_or_abort(acc_empty, (seg - 1) & 1, a, abort_flag);
+                // accumulator buffer db was last read by the epilogue of segment seg - 2
+                if (seg_start && seg >= 2)
+                    ok = wait_or_abort(acc_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
                 ok = wait_or_abort(a_full0 + 8 * b, pha, a, abort_flag) && ok;
                 ok = wait_or_abort(x_full0 + 8 * sx, phx, a, abort_flag) && ok;
                 tc_fence_after();
                 if (ok) {
                     const uint32_t xs = smem_u32(smem + L::OFF_X + sx * L::XSTAGE);
+                    const uint32_t d = tmem + kDCol + 64 * db;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         const uint32_t b_addr = xs + (j >> 2) * L::XSUB + (j & 3) * 32;
                         const uint64_t bdesc = smem_desc_sw128(b_addr, 1024);
-                        tc_mma_ts(tmem + L::D_COL, tmem + b * 64 + j * 8, bdesc, IDESC,
-                                  (j > 0 || !seg_start) ? 1u : 0u);
+                        tc_mma_ts(d, tmem + b * 128 + j * 8, bdesc, IDESC, (j > 0 || !seg_start) ? 1u : 0u);
                     }
                 }
                 // each commit arrives once every MMA issued so far has completed
                 tc_commit(a_empty0 + 8 * b);
                 tc_commit(x_empty0 + 8 * sx);
                 if (seg_end) {
-                    tc_commit(acc_full);
+                    tc_commit(acc_full0 + 8 * db);
                     ++seg;
                 }
                 if (++ks == nk)
@@ -343,12 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------ decode warps --------------------------
-        // warp (q, c): rows 32q..32q+31 of the block (= TMEM lanes), columns
-        // [kKW c, kKW c + kKW) of each 128-column step
         const int q = warp & 3, c = warp >> 2;
-        const int row = 32 * q + lane; // this thread's row in the block = TMEM lane
+        const int row = 32 * q + lane; // this thread's row in the unit = TMEM lane
         const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t rlo = static_cast<uint32_t>(32 * q);
+        const uint32_t kb = static_cast<uint32_t>(64 * c);
         uint32_t eb2 = 0;
         int cur_rb = -1, seg = 0;
         int rb = it0 / nk, ks = it0 % nk, s = 0, b = 0;
@@ -365,132 +392,113 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every barrier) but works on stale data and reads nothing
             // through addresses taken from shared memory.
             ok = __all_sync(0xffffffffu, ok);
-            const int row0 = rb * 128, k0 = ks * 128;
+            const int row0 = rb * 128;
             const uint8_t *st = smem + s * L::WSTAGE;
             if (rb != cur_rb) {
                 cur_rb = rb;
                 eb2 = (e_pre << 7) | (e_pre << 23);
             }
 
-            // 1. raw planes of this row: kKW AE bytes (16-byte chunks, 128-byte
-            //    swizzle) and kKW/2 B bytes (64-byte swizzle)
-            constexpr int NA_CH = kKW / 16, NB_W = kKW / 8; // AE chunks, B words
-            uint4 aq[NA_CH];
-            uint32_t bwords[NB_W];
+            // 1. raw planes of this row's 64 columns: four 16-byte AE chunks
+            //    and two B chunks (128-byte swizzle: chunk j of row r sits at
+            //    j ^ (r & 7))
+            uint4 aq[4], bq[2];
             {
-                const uint8_t *ae_row = st + L::OFF_AE + row * 128;
-                const uint8_t *b_row = st + L::OFF_B + row * 64;
+                const uint8_t *ae_row = st + L::OFF_AE + (c >> 1) * L::AE_HALF + row * 128;
 #pragma unroll
-                for (int i = 0; i < NA_CH; ++i)
-                    aq[i] = *reinterpret_cast<const uint4 *>(ae_row + (((NA_CH * c + i) ^ (row & 7)) << 4));
-#pragma unroll
-                for (int i = 0; i < NB_W; ++i)
-                    bwords[i] = 0u;
+                for (int i = 0; i < 4; ++i)
+                    aq[i] = *reinterpret_cast<const uint4 *>(ae_row + ((((c & 1) * 4 + i) ^ (row & 7)) << 4));
                 if (!Q8) {
+                    const uint8_t *b_row = st + L::OFF_B + row * 128;
 #pragma unroll
-                    for (int i = 0; i < NB_W / 4; ++i) {
-                        const uint4 w4 = *reinterpret_cast<const uint4 *>(
-                            b_row + ((((NB_W / 4) * c + i) ^ ((row >> 1) & 3)) << 4));
-                        bwords[4 * i] = w4.x;
-                        bwords[4 * i + 1] = w4.y;
-                        bwords[4 * i + 2] = w4.z;
-                        bwords[4 * i + 3] = w4.w;
-                    }
+                    for (int i = 0; i < 2; ++i)
+                        bq[i] = *reinterpret_cast<const uint4 *>(b_row + (((2 * c + i) ^ (row & 7)) << 4));
+                } else {
+                    bq[0] = bq[1] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
 
-            // 2. does any escape fall in this warp's 32 rows x kKW columns?  Only
-            //    then is the stage kept until the patch has read the list.
-            bool any = false;
-            uint32_t list_lb = 0, list_ub = 0, esc_lo = 0, esc_cnt = 0;
-            const uint32_t kb = static_cast<uint32_t>((k0 & 255) + kKW * c);
-            if (!Q8) {
+            // 2. escape entries of this warp's quadrant (rows 32q..32q+31) in
+            //    its columns: up to 32 are taken into registers (one per lane)
+            //    and the stage is handed back at once; with more the stage is
+            //    kept until they have been applied
+            uint32_t my_e = 0, hits = 0, q_lb = 0, q_ub = 0, esc_lo = 0;
+            bool many = false, big = false;
+            if (!Q8 && ok) {
                 const uint8_t *esc_area = st + L::OFF_ESC;
-                const uint32_t lo = *reinterpret_cast<const uint32_t *>(esc_area);
-                const uint32_t hi = *reinterpret_cast<const uint32_t *>(esc_area + 4);
-                const uint32_t cnt = ok ? hi - lo : 0u;
-                esc_lo = lo;
-                esc_cnt = cnt;
+                const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
+                const uint32_t cnt = lohi.y - lohi.x;
+                esc_lo = lohi.x;
                 if (cnt) {
                     const uint16_t *gp = reinterpret_cast<const uint16_t *>(esc_area + L::ESC_GP);
-                    list_lb = gp[4 * q];
-                    list_ub = (q == 3) ? cnt : gp[4 * q + 4];
-                    if (list_ub > cnt)
-                        list_ub = cnt;
-                    auto hit = [&](uint32_t e) {
-                        return (e >> 24) - rlo < 32u && ((e >> 16) & 0xFFu) - kb < static_cast<uint32_t>(kKW);
-                    };
-                    if (cnt <= static_cast<uint32_t>(L::ESC_CAP)) {
+                    q_lb = min(static_cast<uint32_t>(gp[4 * q]), cnt);
+                    q_ub = (q == 3) ? cnt : min(static_cast<uint32_t>(gp[4 * q + 4]), cnt);
+                    big = cnt > static_cast<uint32_t>(L::ESC_CAP);
+                    const uint32_t n_q = q_ub > q_lb ? q_ub - q_lb : 0u;
+                    if (n_q > 32 || (big && n_q)) {
+                        many = true;
+                    } else if (n_q) {
                         const uint32_t *list = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
-                        for (uint32_t j = list_lb; j < list_ub && !any; j += 32) {
-                            const uint32_t idx = j + lane;
-                            any = __any_sync(0xffffffffu, idx < list_ub && hit(list[idx]));
-                        }
-                    } else { // more entries than fit in the stage: read them from global memory
-                        const uint32_t *list = a.esc + lo;
-                        for (uint32_t j = list_lb; j < list_ub && !any; j += 32) {
-                            const uint32_t idx = j + lane;
-                            any = __any_sync(0xffffffffu, idx < list_ub && hit(__ldg(list + idx)));
-                        }
+                        const bool valid = static_cast<uint32_t>(lane) < n_q;
+                        my_e = valid ? list[q_lb + lane] : 0u;
+                        hits = __ballot_sync(0xffffffffu, valid && ((my_e >> 16) & 0xFFu) - kb < 64u);
                     }
                 }
             }
-            // 3. without escapes here the stage is no longer needed: hand it back
-            if (!any) {
+            if (!many) {
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(w_empty0 + 8 * s);
             }
 
-            // 4. decode to exact BF16 pairs
-            uint32_t v[kCols];
+            // 3. decode to exact BF16 pairs (escaped slots hold their placeholder)
+            uint32_t v[32];
+            {
+                const uint32_t bw[8] = {bq[0].x, bq[0].y, bq[0].z, bq[0].w,
+                                        bq[1].x, bq[1].y, bq[1].z, bq[1].w};
 #pragma unroll
-            for (int i = 0; i < NA_CH; ++i) {
-                decode_group<Q8>(aq[i].x, aq[i].y, bwords[2 * i], eb2, v + 8 * i);
-                decode_group<Q8>(aq[i].z, aq[i].w, bwords[2 * i + 1], eb2, v + 8 * i + 4);
+                for (int i = 0; i < 4; ++i) {
+                    decode_group<Q8>(aq[i].x, aq[i].y, bw[2 * i], eb2, v + 8 * i);
+                    decode_group<Q8>(aq[i].z, aq[i].w, bw[2 * i + 1], eb2, v + 8 * i + 4);
+                }
             }
 
-            // 5. patch escapes through this warp's scratch tile, then release
-            if (!Q8 && any) {
-                uint8_t *scr = smem + L::OFF_SCR + warp * 32 * kScrPitch;
-#pragma unroll
-                for (int i = 0; i < kCols / 4; ++i)
-                    *reinterpret_cast<uint4 *>(scr + lane * kScrPitch + i * 16) =
-                        make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                __syncwarp();
-                auto put = [&](uint32_t e) {
-                    const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
-                    if (r7 - rlo < 32u && k8 - kb < static_cast<uint32_t>(kKW))
-                        *reinterpret_cast<uint16_t *>(scr + (r7 - rlo) * kScrPitch + (k8 - kb) * 2) =
-                            static_cast<uint16_t>(e & 0xFFFFu);
-                };
-                if (esc_cnt <= static_cast<uint32_t>(L::ESC_CAP)) {
-                    const uint32_t *list = reinterpret_cast<const uint32_t *>(st + L::OFF_ESC + L::ESC_LIST);
-                    for (uint32_t j = list_lb + lane; j < list_ub; j += 32)
-                        put(list[j]);
-                } else {
-                    for (uint32_t j = list_lb + lane; j < list_ub; j += 32)
-                        put(__ldg(a.esc + esc_lo + j));
-                }
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < kCols / 4; ++i) {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(scr + lane * kScrPitch + i * 16);
-                    v[4 * i] = w4.x;
-                    v[4 * i + 1] = w4.y;
-                    v[4 * i + 2] = w4.z;
-                    v[4 * i + 3] = w4.w;
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(w_empty0 + 8 * s);
-            }
-
-            // 6. into tensor memory, once the MMA is done with this A buffer
+            // 4. into tensor memory, once the MMA is done with this A buffer,
+            //    then the escapes of this warp's columns
             wait_or_abort(a_empty0 + 8 * b, pha ^ 1, a, abort_flag);
             __syncwarp();
             tc_fence_after();
-            tmem_store(tmem + t_lane + static_cast<uint32_t>(b * 64 + kCols * c), v);
+            const uint32_t abuf = tmem + static_cast<uint32_t>(b * 128);
+            tmem_st32(abuf + t_lane + kb / 2, v);
+            if (hits != 0u || many) {
+                tc_wait_st();
+                if (!many) {
+                    while (hits) {
+                        const int src = __ffs(hits) - 1;
+                        hits &= hits - 1;
+                        patch_entry(__shfl_sync(0xffffffffu, my_e, src), abuf, t_lane, rlo, lane);
+                    }
+                } else {
+                    const uint32_t *list_s =
+                        reinterpret_cast<const uint32_t *>(st + L::OFF_ESC + L::ESC_LIST);
+                    for (uint32_t j = q_lb; j < q_ub; j += 32) {
+                        const uint32_t idx = j + static_cast<uint32_t>(lane);
+                        const bool valid = idx < q_ub;
+                        uint32_t e = 0;
+                        if (valid)
+                            e = big ? __ldg(a.esc + esc_lo + idx) : list_s[idx];
+                        uint32_t h = __ballot_sync(0xffffffffu, valid && ((e >> 16) & 0xFFu) - kb < 64u);
+                        while (h) {
+                            const int src = __ffs(h) - 1;
+                            h &= h - 1;
+                            patch_entry(__shfl_sync(0xffffffffu, e, src), abuf, t_lane, rlo, lane);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(w_empty0 + 8 * s);
+                }
+            }
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -499,34 +507,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- accumulators of this row block are final: read them out ----
-                wait_or_abort(acc_full, seg & 1, a, abort_flag);
+                const int db = seg & 1;
+                wait_or_abort(acc_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
                 __syncwarp();
                 tc_fence_after();
-                constexpr int PART = MT / kKQ; // accumulator columns read by this warp
+                constexpr int PART = MT / 4; // accumulator columns read by this warp
                 float out[PART];
-                const uint32_t dcol = tmem + t_lane + L::D_COL + c * PART;
-                if constexpr (PART == 4) {
-                    uint32_t d[4];
-                    tmem_ld4(dcol, d);
-                    tc_wait_ld();
+                const bool used = c * PART < a.M;
+                if (used) {
+                    const uint32_t dcol = tmem + t_lane + kDCol + 64 * db + c * PART;
+                    if constexpr (PART == 4) {
+                        uint32_t d[4];
+                        tmem_ld4(dcol, d);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        out[j] = __uint_as_float(d[j]);
-                } else {
-#pragma unroll
-                    for (int c8 = 0; c8 < PART / 8; ++c8) {
+                        for (int j = 0; j < 4; ++j)
+                            out[j] = __uint_as_float(d[j]);
+                    } else if constexpr (PART == 8) {
                         uint32_t d[8];
-                        tmem_ld8(dcol + 8 * c8, d);
+                        tmem_ld8(dcol, d);
                         tc_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            out[8 * c8 + j] = __uint_as_float(d[j]);
+                            out[j] = __uint_as_float(d[j]);
+                    } else {
+                        uint32_t d[16];
+                        tmem_ld16(dcol, d);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            out[j] = __uint_as_float(d[j]);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(acc_empty);
+                    mbar_arrive(acc_empty0 + 8 * db);
                 ++seg;
 
                 const int c_first = sk_owner(rb * nk, grid, a.total_iters);
@@ -534,15 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool direct = (c_first == c_last);
                 const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
                 const int n = row0 + row;
+                if (used) {
 #pragma unroll
-                for (int j = 0; j < PART; ++j) {
-                    const int m = c * PART + j;
-                    if (m < a.M) {
-                        if (direct) {
-                            if (n < a.N)
-                                a.y[static_cast<size_t>(m) * a.N + n] = out[j];
-                        } else {
-                            a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = out[j];
+                    for (int j = 0; j < PART; ++j) {
+                        const int m = c * PART + j;
+                        if (m < a.M) {
+                            if (direct) {
+                                if (n < a.N)
+                                    a.y[static_cast<size_t>(m) * a.N + n] = out[j];
+                            } else {
+                                a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = out[j];
+                            }
                         }
                     }
                 }
@@ -598,8 +616,7 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtens
             return e;
         attr_done = true;
     }
-    kern<<<grid, kThreads, L::TOTAL, st>>>(a, *tm_ae, *tm_b, *tm_x);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kThreads, L::TOTAL, st, a, *tm_ae, *tm_b, *tm_x);
 }
 
 } // namespace

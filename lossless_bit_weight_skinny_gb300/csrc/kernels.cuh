@@ -120,6 +120,26 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
     }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream is finishing; it calls
+// pdl_wait_prior_grid() before touching anything that kernel may write.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t st, const GemmArgs &a,
+                       const CUtensorMap &t0, const CUtensorMap &t1, const CUtensorMap &t2)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, t0, t1, t2);
+}
+
 // Launchers (defined in gemm_fma.cu / gemm_tc.cu / decode.cu).
 cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
                             const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
@@ -130,8 +150,12 @@ cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap
 int fma_rows_blk(int mt);
 int fma_smem_bytes(int mt, bool q8);
 int tc_smem_bytes(int mt, bool q8);
+#ifndef W12_TC_MIN_M
+#define W12_TC_MIN_M 5 // smallest M sent to the tensor-core kernel (at most 5)
+#endif
+static_assert(W12_TC_MIN_M >= 1 && W12_TC_MIN_M <= 5, "the CUDA-core kernel covers M <= 4");
 constexpr int kFmaKStep = 256;
-constexpr int kTcKStep = 128;
+constexpr int kTcKStep = 256;
 constexpr int kTcRows = 128;
 
 cudaError_t launch_decode(const uint8_t *ebase, const uint8_t *ae, const uint8_t *b,

@@ -134,8 +134,8 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     if (!w->gemm_ok)
         return W12_ERR_UNSUPPORTED;
 
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    const bool tc = mt >= 16;
+    const bool tc = M >= W12_TC_MIN_M;
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     int sms = 0;

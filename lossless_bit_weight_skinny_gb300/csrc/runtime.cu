@@ -165,8 +165,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     // Kernel choice, a function of M only (measured on GB300): the CUDA-core
     // kernel for M <= 4; above that the tensor-core kernel, padding M to 16,
     // 32 or 64 rows, is faster than packed FMAs for 8 rows.
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 16 ? 16 : M <= 32 ? 32 : 64;
-    const bool tc = mt >= 16;
+    const bool tc = M >= W12_TC_MIN_M;
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     GemmArgs a{};
@@ -190,8 +190,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     a.inject_stall = g_inject_stall.load();
     // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
     // streams several times the weight bytes of the partial sums it writes
-    // (a 128 x 128 tensor-core step reads 24 KB of W12, its partial is M x 512 B)
-    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 11) / 12) : 1;
+    // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
+    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : 1;
     const int64_t want = std::max<int64_t>(a.n_rowblk, iters / min_iters);
     const int grid = static_cast<int>(std::min<int64_t>(sm_count(cur), std::min<int64_t>(iters, want)));
 
@@ -312,7 +312,7 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
         t = t && make_tmap(tmap_of(d->tm_b_fma128), U8, 1, d->b, K / 2, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
         t = t && make_tmap(tmap_of(d->tm_b_fma64), U8, 1, d->b, K / 2, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
         t = t && make_tmap(tmap_of(d->tm_ae_tc), U8, 1, d->ae, K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        t = t && make_tmap(tmap_of(d->tm_b_tc), U8, 1, d->b, K / 2, N, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+        t = t && make_tmap(tmap_of(d->tm_b_tc), U8, 1, d->b, K / 2, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         d->gemm_ok = t;
     }
     *out = d;
