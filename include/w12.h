@@ -138,8 +138,8 @@ w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device
  * and FP32 accumulation.  x: device BF16 [M][K], 16-byte aligned; y: device
  * FP32 [M][N], 16-byte aligned; both caller-owned.  1 <= M <= 64 (M = 0 is a
  * no-op), N and K must equal the handle's; K % 32 == 0 (else UNSUPPORTED).
- * Kernel choice is a function of M only: M <= 4 CUDA-core FMAs with warp
- * reductions, 5..64 tcgen05 tensor cores with TMEM accumulators.  Uses a
+ * Kernel choice is a function of M only: M <= 2 CUDA-core FMAs with warp
+ * reductions, 3..64 tcgen05 tensor cores with TMEM accumulators.  Uses a
  * library-owned workspace cached per (device, stream); the first call on a
  * stream allocates it (stream-ordered), so make that first call outside any
  * stream capture.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM,

@@ -9,7 +9,7 @@
 // one persistent CTA per SM (stream-K), and row blocks shared by several CTAs
 // are combined by the last contributor in a fixed order.
 //
-// CTA = CW consumer warps + a producer warp + an escape warp.  The producer
+// CTA = CW consumer warps + a producer warp + two escape warps.  The producer
 // streams each block's AE bytes, B words and x slice with TMA into a ring of
 // shared-memory stages, and copies the tile's escape entries next to them with
 // cp.async.  Consumer warp w owns RW rows of the block; lane l owns columns
@@ -18,10 +18,10 @@
 //
 // Escapes: the main loop multiplies every slot as decoded -- an escaped slot
 // holds the placeholder +-2^(ebase-127) -- and has no branches and no escape
-// work at all.  The escape warp walks each stage's list and keeps, per output,
-// the two correction sums sum(-x * placeholder) and sum(x * exact value) in
-// shared memory; the consumers add them to the output in that order at the
-// end of the row block.  With a single non-zero product (one-hot x) this gives
+// work at all.  The escape warps (even and odd units) walk each stage's list
+// and keep, per output, the two correction sums sum(-x * placeholder) and
+// sum(x * exact value) in shared memory; the consumers add them to the output
+// in that order at the end of the row block.  With a single non-zero product (one-hot x) this gives
 // the exact escaped value back, Inf/NaN escapes propagate, and otherwise the
 // result is the same sum in another (fixed) order.
 #include "kernels.cuh"
@@ -45,10 +45,10 @@ struct FmaShape {
     static constexpr int RBLK = W12_FMA_RBLK;                 // rows per block
     static constexpr int CW = W12_FMA_CW ? W12_FMA_CW : (MT == 1 ? 16 : 8); // consumer warps
     static constexpr int RW = RBLK / CW;                      // rows per consumer warp
-    static constexpr int THREADS = (CW + 2) * 32; // + producer + escape warp
+    static constexpr int THREADS = (CW + 3) * 32; // + producer + two escape warps
     // registers per thread for one resident CTA: each of the 4 SM sub-partitions
     // has 16K registers and holds ceil(warps / 4) of the CTA's warps
-    static constexpr int PER_SMSP = (CW + 2 + 3) / 4;
+    static constexpr int PER_SMSP = (CW + 3 + 3) / 4;
     static constexpr int MAXREG_RAW = (16384 / (32 * PER_SMSP)) & ~7;
     static constexpr int MAXREG = MAXREG_RAW > 255 ? 255 : MAXREG_RAW;
     static_assert(RW % 8 == 0 && RBLK % CW == 0, "warps own whole 8-row escape groups");
@@ -72,7 +72,9 @@ struct FmaSmem {
     static constexpr int OFF_X = OFF_B + r128(B);
     static constexpr int OFF_ESC = OFF_X + r128(X);
     static constexpr int STAGE = r1024(OFF_ESC + ESC);
-    static constexpr int CORR = Q8 ? 0 : 2 * 2 * S::RBLK * MT * 4; // correction sums
+    // per escape warp: correction sums [buffer][neg, pos][RBLK * MT], window bases
+    static constexpr int CORR_W = 2 * 2 * S::RBLK * MT * 4 + S::RBLK;
+    static constexpr int CORR = Q8 ? 0 : 2 * CORR_W;
     static constexpr int BUDGET = 227 * 1024 - 2048;
     static constexpr int STAGES_RAW = (BUDGET - CORR) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
@@ -197,6 +199,86 @@ struct XReduce {
     }
 };
 
+// Escape warp: NC chunks of 32 list entries starting at j1, one entry per
+// lane.  For each entry the products -x * placeholder and x * exact value of
+// every activation row; a segmented scan over the lanes sums them per output
+// row (the list is sorted by row), and each row's sum is added to its
+// correction totals in shared memory.  The chunks' loads and scans are
+// independent and interleaved; the additions happen in list order.
+template <int MT, int RBLK, int NC>
+__device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *list_s, bool big,
+                                           uint32_t lo, uint32_t cnt, uint32_t j1, uint32_t rbase,
+                                           int row0, const uint8_t *eb_s, const uint8_t *xs,
+                                           float *cneg, float *cpos, int lane)
+{
+    uint32_t e4[NC];
+#pragma unroll
+    for (int u = 0; u < NC; ++u) {
+        const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
+        e4[u] = 0u;
+        if (j < cnt) {
+            if (big)
+                e4[u] = __ldg(a.esc + lo + j);
+            else
+                e4[u] = list_s[j];
+        }
+    }
+    float pn[NC][MT], pp[NC][MT];
+    uint32_t key[NC], rr[NC];
+    bool in[NC];
+#pragma unroll
+    for (int u = 0; u < NC; ++u) {
+        const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
+        const uint32_t e = e4[u];
+        const uint32_t r = (e >> 24) - rbase; // row in the block
+        in[u] = j < cnt && r < static_cast<uint32_t>(RBLK) && row0 + static_cast<int>(r) < a.N;
+        rr[u] = r;
+        const uint32_t k8 = (e >> 16) & 0xFFu;
+        const uint32_t eb = in[u] ? eb_s[r] : 0u;
+        const float wph = __uint_as_float(((e & 0x8000u) << 16) | (eb << 23));
+        const float wex = __uint_as_float((e & 0xFFFFu) << 16);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint32_t xb = *reinterpret_cast<const uint16_t *>(xs + m * 512 + k8 * 2);
+            const float xv = __uint_as_float(xb << 16);
+            pn[u][m] = in[u] ? -(xv * wph) : 0.f; // both products are exact in FP32
+            pp[u][m] = in[u] ? xv * wex : 0.f;
+        }
+        key[u] = in[u] ? r : 256u + static_cast<uint32_t>(lane);
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+        for (int u = 0; u < NC; ++u) {
+            const uint32_t kp = __shfl_up_sync(0xffffffffu, key[u], d);
+            const bool take = lane >= d && kp == key[u];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float an = __shfl_up_sync(0xffffffffu, pn[u][m], d);
+                const float ap = __shfl_up_sync(0xffffffffu, pp[u][m], d);
+                if (take) {
+                    pn[u][m] = an + pn[u][m];
+                    pp[u][m] = ap + pp[u][m];
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NC; ++u) {
+        if (j1 + 32 * u >= cnt)
+            break;
+        const uint32_t kn = __shfl_down_sync(0xffffffffu, key[u], 1);
+        if (in[u] && (lane == 31 || kn != key[u])) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                cneg[rr[u] * MT + m] += pn[u][m];
+                cpos[rr[u] * MT + m] += pp[u][m];
+            }
+        }
+        __syncwarp();
+    }
+}
+
 template <int MT, bool Q8>
 __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     gemm_fma_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
@@ -209,7 +291,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     constexpr int V = RW * MT;           // per-lane partial sums
     constexpr int VPL = V >= 32 ? V / 32 : 1;
     constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : 3;
-    constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warp
+    constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warps WARP_E and WARP_E + 1
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -222,7 +304,8 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     volatile int *seg_last = abort_flag + 1;
     // escape corrections of the current row block, double buffered:
     // [buffer][neg, pos][RBLK * MT]
-    float *corr = reinterpret_cast<float *>(smem + L::OFF_CORR);
+    // escape warp E's correction sums: corr_of(E) + db * 2 * RBLK * MT
+    auto corr_of = [&](int e) { return reinterpret_cast<float *>(smem + L::OFF_CORR + e * L::CORR_W); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grid = gridDim.x, cta = blockIdx.x;
@@ -233,16 +316,23 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(empty0 + 8 * s, Q8 ? CW : CW + 1);
+            mbar_init(empty0 + 8 * s, Q8 ? CW : CW + 2);
         }
         mbar_init(stall_bar, 1);
         for (int d = 0; d < 2; ++d) {
-            mbar_init(corr_full0 + 8 * d, 32);
+            mbar_init(corr_full0 + 8 * d, 64);
             mbar_init(corr_empty0 + 8 * d, CW);
         }
         *abort_flag = 0;
         *seg_last = 0;
         fence_barrier_init();
+    }
+    // escape-list bounds of the producer's first 64 units, loaded while the
+    // CTA sets up
+    uint32_t w_lo = 0, w_hi = 0, w_nlo = 0, w_nhi = 0;
+    if (!Q8 && warp == WARP_P) {
+        load_tile_window(a, it0, n_it, 0, lane, RBLK, w_lo, w_hi);
+        load_tile_window(a, it0, n_it, 32, lane, RBLK, w_nlo, w_nhi);
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -255,8 +345,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             if (!Q8)
                 prefetch_tmap(&tm_b);
         }
-        int win = -1;
-        uint32_t my_lo = 0, my_hi = 0;
         int issued = 0;
         int rb = it0 / nk, ks = it0 % nk, s = 0;
         uint32_t ph = 0;
@@ -292,17 +380,13 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 if (lane < 2)
                     cp_async_4(smem_u32(esc_area + 4 * lane),
                                a.tile_ptr + (row0 / 128) * a.tiles_c + ks + lane);
-                if (win < 0 || it - win >= 32) {
-                    win = it;
-                    const int gj = it0 + it + lane;
-                    if (gj < it0 + n_it) {
-                        const int tj = ((gj / nk) * RBLK / 128) * a.tiles_c + gj % nk;
-                        my_lo = __ldg(a.tile_ptr + tj);
-                        my_hi = __ldg(a.tile_ptr + tj + 1);
-                    }
+                if (it > 0 && (it & 31) == 0) { // next window; prefetch the one after
+                    w_lo = w_nlo;
+                    w_hi = w_nhi;
+                    load_tile_window(a, it0, n_it, it + 32, lane, RBLK, w_nlo, w_nhi);
                 }
-                const uint32_t lo = __shfl_sync(0xffffffffu, my_lo, it - win);
-                const uint32_t hi = __shfl_sync(0xffffffffu, my_hi, it - win);
+                const uint32_t lo = __shfl_sync(0xffffffffu, w_lo, it & 31);
+                const uint32_t hi = __shfl_sync(0xffffffffu, w_hi, it & 31);
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
                 uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
@@ -324,13 +408,17 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int s = it % STAGES;
             mbar_wait(full0 + 8 * s, (it / STAGES) & 1, 1000000000ull);
         }
-    } else if (warp == WARP_E) {
-        // ---------------------------- escape warp -----------------------------
-        // Per stage, the tile's entries 32 at a time, one per lane: the two
-        // products -x * placeholder and x * exact value for each activation
-        // row, summed per output row by a segmented scan over the lanes (the
-        // list is sorted by row), then added to the row's correction sums.
-        // Fixed order throughout, so results are reproducible.
+    } else if (warp == WARP_E || warp == WARP_E + 1) {
+        // ---------------------------- escape warps ----------------------------
+        // Escape warp E takes the units of parity E.  Per unit, the tile's
+        // entries 32 at a time, one per lane: the two products -x * placeholder
+        // and x * exact value for each activation row, summed per output row
+        // by a segmented scan over the lanes (the list is sorted by row), then
+        // added to the row's correction sums of this warp.  Fixed order
+        // throughout, so results are reproducible.
+        const int ew = warp - WARP_E;
+        float *const corr = corr_of(ew);
+        uint8_t *const eb_s = reinterpret_cast<uint8_t *>(corr + 2 * 2 * RBLK * MT); // window bases
         if (!Q8) {
             int seg = 0;
             int rb = it0 / nk, ks = it0 % nk, s = 0;
@@ -346,74 +434,35 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                         wait_or_abort(corr_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
                     for (int i = lane; i < 2 * RBLK * MT; i += 32)
                         cneg[i] = 0.f;
+                    for (int r = lane; r < RBLK; r += 32)
+                        eb_s[r] = rb * RBLK + r < a.N ? __ldg(a.ebase + rb * RBLK + r) : 0;
                     __syncwarp();
                 }
                 bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 const int row0 = rb * RBLK;
                 const uint8_t *st = smem + s * L::STAGE;
-                if (ok) {
+                if (ok && ((it0 + it) & 1) == ew) {
                     const uint8_t *esc_area = st + L::OFF_ESC;
                     const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
                     const uint32_t cnt = lohi.y - lohi.x;
                     const bool big = cnt > static_cast<uint32_t>(L::ESC_CAP);
                     const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
                     const uint32_t rbase = static_cast<uint32_t>(row0 & 127);
-                    for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
-                        const uint32_t j = j0 + static_cast<uint32_t>(lane);
-                        uint32_t e = 0;
-                        if (j < cnt) {
-                            if (big)
-                                e = __ldg(a.esc + lohi.x + j);
-                            else
-                                e = list_s[j];
-                        }
-                        const uint32_t r = (e >> 24) - rbase; // row in the block
-                        const bool in = j < cnt && r < static_cast<uint32_t>(RBLK) &&
-                                        row0 + static_cast<int>(r) < a.N;
-                        const uint32_t k8 = (e >> 16) & 0xFFu;
-                        const uint32_t eb = in ? __ldg(a.ebase + row0 + r) : 0u;
-                        const float wph = __uint_as_float(((e & 0x8000u) << 16) | (eb << 23));
-                        const float wex = __uint_as_float((e & 0xFFFFu) << 16);
-                        float pn[MT], pp[MT];
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const uint32_t xb = *reinterpret_cast<const uint16_t *>(st + L::OFF_X + m * 512 + k8 * 2);
-                            const float xv = __uint_as_float(xb << 16);
-                            pn[m] = in ? -(xv * wph) : 0.f; // both products are exact in FP32
-                            pp[m] = in ? xv * wex : 0.f;
-                        }
-                        const uint32_t key = in ? r : 256u + static_cast<uint32_t>(lane);
-#pragma unroll
-                        for (int d = 1; d < 32; d <<= 1) {
-                            const uint32_t kp = __shfl_up_sync(0xffffffffu, key, d);
-                            const bool take = lane >= d && kp == key;
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const float an = __shfl_up_sync(0xffffffffu, pn[m], d);
-                                const float ap = __shfl_up_sync(0xffffffffu, pp[m], d);
-                                if (take) {
-                                    pn[m] = an + pn[m];
-                                    pp[m] = ap + pp[m];
-                                }
-                            }
-                        }
-                        const uint32_t kn = __shfl_down_sync(0xffffffffu, key, 1);
-                        if (in && (lane == 31 || kn != key)) {
-#pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                cneg[r * MT + m] += pn[m];
-                                cpos[r * MT + m] += pp[m];
-                            }
-                        }
-                        __syncwarp();
+                    for (uint32_t j1 = 0; j1 < cnt; j1 += 128) {
+                        if (cnt - j1 <= 32)
+                            esc_chunks<MT, RBLK, 1>(a, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                                                    st + L::OFF_X, cneg, cpos, lane);
+                        else
+                            esc_chunks<MT, RBLK, 4>(a, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                                                    st + L::OFF_X, cneg, cpos, lane);
                     }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(empty0 + 8 * s);
                 if (seg_end) {
-                    mbar_arrive(corr_full0 + 8 * db); // all 32 lanes: their sums are visible
+                    mbar_arrive(corr_full0 + 8 * db); // all 64 lanes: their sums are visible
                     ++seg;
                 }
                 if (++ks == nk) {
@@ -573,7 +622,8 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 const int db = seg & 1;
                 if (!Q8)
                     wait_or_abort(corr_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
-                const float *cneg = corr + db * (2 * RBLK * MT), *cpos = cneg + RBLK * MT;
+                const float *cneg0 = corr_of(0) + db * (2 * RBLK * MT), *cpos0 = cneg0 + RBLK * MT;
+                const float *cneg1 = corr_of(1) + db * (2 * RBLK * MT), *cpos1 = cneg1 + RBLK * MT;
                 const int c_first = sk_owner(rb * nk, grid, a.total_iters);
                 const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
                 const bool writer = (V >= 32) || ((lane & ((32 >> LOGV) - 1)) == 0);
@@ -585,8 +635,10 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     const int r = idx / MT, m = idx % MT;
                     // the placeholder products out first, then the exact ones in
                     float total = v[q];
-                    if (!Q8)
-                        total = (total + cneg[(wrow + r) * MT + m]) + cpos[(wrow + r) * MT + m];
+                    if (!Q8) {
+                        const int i = (wrow + r) * MT + m;
+                        total = (total + (cneg0[i] + cneg1[i])) + (cpos0[i] + cpos1[i]);
+                    }
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
                         if (direct) {

@@ -49,27 +49,34 @@ constexpr int a1024(int v) { return (v + 1023) & ~1023; }
 template <int MT, bool Q8>
 struct TcSmem {
     // weight stage: AE as two 128-column halves and B, each 128 rows of 128
-    // bytes with the 128-byte swizzle, then the escape area
+    // bytes with the 128-byte swizzle
     static constexpr int AE_HALF = 128 * 128;
     static constexpr int AE = 2 * AE_HALF;
     static constexpr int B = Q8 ? 0 : 128 * 128;
-    static constexpr int ESC_CAP = 256; // more entries in a tile are read from global memory
-    static constexpr int ESC_GP = 16; // [lo, hi, -, -] u32, then the row-group index u16[16]
-    static constexpr int ESC_LIST = 48;
-    static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
     static constexpr int OFF_AE = 0;
     static constexpr int OFF_B = AE;
-    static constexpr int OFF_ESC = OFF_B + B;
-    static constexpr int WSTAGE = a1024(OFF_ESC + ESC);
+    static constexpr int WSTAGE = a1024(AE + B);
+    // the unit's escape area, one per weight stage in a ring of its own:
+    // [lo, hi, -, -] u32, the row-group index u16[16], up to ESC_CAP entries
+    // (a tile with more is read from global memory)
+    static constexpr int ESC_CAP = 256;
+    static constexpr int ESC_GP = 16;
+    static constexpr int ESC_LIST = 48;
+    static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
     // activation stage: four 64-column sub-tiles of MT rows, 128-byte swizzle
     static constexpr int XSUB = MT * 128;
     static constexpr int XSTAGE = 4 * XSUB;
     static constexpr int XST = (MT <= 32) ? 3 : 2; // activation slots
+    // per decode warp: one row of 32 BF16 pairs, for patching escapes
+    static constexpr int SCR_PITCH = 144;
+    static constexpr int SCR = Q8 ? 0 : kDecodeWarps * SCR_PITCH;
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE) / WSTAGE;
+    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + ESC);
     static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight slots
     static constexpr int OFF_X = WST * WSTAGE;
-    static constexpr int BARS = OFF_X + XST * XSTAGE;
+    static constexpr int OFF_ESC = OFF_X + XST * XSTAGE;
+    static constexpr int OFF_SCR = OFF_ESC + WST * ESC;
+    static constexpr int BARS = (OFF_SCR + SCR + 15) & ~15;
     // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
     // acc_full, acc_empty [2]; final, stall
     static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4 + 2;
@@ -136,23 +143,71 @@ __device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint3
     out[3] = decode_pair<3, Q8>(a_hi, bw, eb2);
 }
 
-// Replace the BF16 of escape entry e (row r7 of the unit, column k8) in the A
-// buffer at `abuf` (column = k8 / 2, lane quadrant base `t_lane`).  Warp-wide:
-// every lane reads and writes back its own lane of that column.
-__device__ __forceinline__ void patch_entry(uint32_t e, uint32_t abuf, uint32_t t_lane, uint32_t rlo,
-                                            int lane)
-{
-    const uint32_t r7 = e >> 24, k8 = (e >> 16) & 0xFFu;
-    const uint32_t addr = abuf + t_lane + (k8 >> 1);
-    uint32_t v = tmem_ld1(addr);
-    tc_wait_ld();
-    if (static_cast<uint32_t>(lane) == r7 - rlo) {
-        const uint32_t bits = e & 0xFFFFu;
-        v = (k8 & 1u) ? ((v & 0x0000FFFFu) | (bits << 16)) : ((v & 0xFFFF0000u) | bits);
+// Patch escapes into a decode thread's 32 BF16 pairs v (columns kb..kb+63 of
+// its row) before they go to tensor memory.  The list is sorted by row, so the
+// entries of one row are consecutive: the owning lane parks its pairs in the
+// warp's scratch row, the lanes holding that row's entries overwrite the
+// escaped 16-bit slots there, and the owner takes the pairs back before the
+// next row's lane parks its own.
+struct EscPatcher {
+    uint8_t *scr;   // this warp's scratch row
+    uint32_t rlo;   // first row of the warp's quadrant
+    uint32_t kb;    // first column of the warp's quarter
+    int lane;
+    int cur = -1;   // lane whose pairs are parked
+
+    __device__ __forceinline__ void park(uint32_t (&v)[32]) const
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4 *>(scr + 16 * i) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
-    tmem_st1(addr, v);
-    tc_wait_st(); // a later patch of the same column reads this value
-}
+    __device__ __forceinline__ void take(uint32_t (&v)[32]) const
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(scr + 16 * i);
+            v[4 * i] = w.x;
+            v[4 * i + 1] = w.y;
+            v[4 * i + 2] = w.z;
+            v[4 * i + 3] = w.w;
+        }
+    }
+    // One chunk of entries, one per lane (e); h: the lanes whose entry lies in
+    // this warp's quarter.  Row by row in list order: the row's lane parks its
+    // pairs, then every lane holding an entry of that row writes its slot.
+    __device__ __forceinline__ void apply(uint32_t e, uint32_t h, uint32_t (&v)[32])
+    {
+        const int mine_row = static_cast<int>((e >> 24) - rlo);
+        const bool hit = (h >> lane) & 1u;
+        while (h) {
+            const int owner = static_cast<int>((__shfl_sync(0xffffffffu, e, __ffs(h) - 1) >> 24) - rlo);
+            if (owner != cur) {
+                if (lane == cur)
+                    take(v);
+                __syncwarp();
+                if (lane == owner)
+                    park(v);
+                __syncwarp();
+                cur = owner;
+            }
+            const bool mine = hit && mine_row == owner;
+            if (mine)
+                *reinterpret_cast<uint16_t *>(scr + 2 * (((e >> 16) & 0xFFu) - kb)) =
+                    static_cast<uint16_t>(e & 0xFFFFu);
+            h &= ~__ballot_sync(0xffffffffu, mine);
+            __syncwarp();
+        }
+    }
+    __device__ __forceinline__ void finish(uint32_t (&v)[32])
+    {
+        __syncwarp();
+        if (lane == cur)
+            take(v);
+        __syncwarp();
+        cur = -1;
+    }
+};
 
 // 19 warps: 5 per SM sub-partition, whose 16K registers allow 102 per thread
 template <int MT, bool Q8>
@@ -212,6 +267,13 @@ __global__ void __maxnreg__(96)
         *seg_last = 0;
         fence_barrier_init();
     }
+    // escape-list bounds of the producer's first 64 units, loaded while the
+    // CTA sets up
+    uint32_t w_lo = 0, w_hi = 0, w_nlo = 0, w_nhi = 0;
+    if (!Q8 && warp == kWarpW) {
+        load_tile_window(a, it0, n_it, 0, lane, 128, w_lo, w_hi);
+        load_tile_window(a, it0, n_it, 32, lane, 128, w_nlo, w_nhi);
+    }
     if (warp == kWarpM) {
         tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), 512);
         tmem_relinquish();
@@ -229,8 +291,6 @@ __global__ void __maxnreg__(96)
             if (!Q8)
                 prefetch_tmap(&tm_b);
         }
-        int win = -1;
-        uint32_t my_lo = 0, my_hi = 0;
         int issued = 0;
         int rb = it0 / nk, ks = it0 % nk, s = 0;
         uint32_t ph = 0;
@@ -250,24 +310,19 @@ __global__ void __maxnreg__(96)
             }
             if (!Q8) {
                 const int t = rb * a.tiles_c + ks;
-                uint8_t *esc_area = st + L::OFF_ESC;
+                uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
                 if (lane < 2)
                     cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
                 else if (lane < 4)
                     cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
                                 a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
-                // the tile bounds of the next 32 units, one per lane
-                if (win < 0 || it - win >= 32) {
-                    win = it;
-                    const int gj = it0 + it + lane;
-                    if (gj < it0 + n_it) {
-                        const int tj = (gj / nk) * a.tiles_c + gj % nk;
-                        my_lo = __ldg(a.tile_ptr + tj);
-                        my_hi = __ldg(a.tile_ptr + tj + 1);
-                    }
+                if (it > 0 && (it & 31) == 0) { // next window; prefetch the one after
+                    w_lo = w_nlo;
+                    w_hi = w_nhi;
+                    load_tile_window(a, it0, n_it, it + 32, lane, 128, w_nlo, w_nhi);
                 }
-                const uint32_t lo = __shfl_sync(0xffffffffu, my_lo, it - win);
-                const uint32_t hi = __shfl_sync(0xffffffffu, my_hi, it - win);
+                const uint32_t lo = __shfl_sync(0xffffffffu, w_lo, it & 31);
+                const uint32_t hi = __shfl_sync(0xffffffffu, w_hi, it & 31);
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
                 uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
@@ -425,7 +480,7 @@ __global__ void __maxnreg__(96)
             uint32_t my_e = 0, hits = 0, q_lb = 0, q_ub = 0, esc_lo = 0;
             bool many = false, big = false;
             if (!Q8 && ok) {
-                const uint8_t *esc_area = st + L::OFF_ESC;
+                const uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
                 const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
                 const uint32_t cnt = lohi.y - lohi.x;
                 esc_lo = lohi.x;
@@ -463,42 +518,47 @@ __global__ void __maxnreg__(96)
                 }
             }
 
-            // 4. into tensor memory, once the MMA is done with this A buffer,
-            //    then the escapes of this warp's columns
-            wait_or_abort(a_empty0 + 8 * b, pha ^ 1, a, abort_flag);
-            __syncwarp();
-            tc_fence_after();
-            const uint32_t abuf = tmem + static_cast<uint32_t>(b * 128);
-            tmem_st32(abuf + t_lane + kb / 2, v);
+            // 4. escapes of this warp's columns, patched in registers
             if (hits != 0u || many) {
-                tc_wait_st();
+                EscPatcher pt{smem + L::OFF_SCR + warp * L::SCR_PITCH, rlo, kb, lane};
                 if (!many) {
-                    while (hits) {
-                        const int src = __ffs(hits) - 1;
-                        hits &= hits - 1;
-                        patch_entry(__shfl_sync(0xffffffffu, my_e, src), abuf, t_lane, rlo, lane);
-                    }
+                    pt.apply(my_e, hits, v);
                 } else {
+                    // more than 32 entries in the quadrant (or in global memory):
+                    // four chunks of 32 fetched at a time
                     const uint32_t *list_s =
-                        reinterpret_cast<const uint32_t *>(st + L::OFF_ESC + L::ESC_LIST);
-                    for (uint32_t j = q_lb; j < q_ub; j += 32) {
-                        const uint32_t idx = j + static_cast<uint32_t>(lane);
-                        const bool valid = idx < q_ub;
-                        uint32_t e = 0;
-                        if (valid)
-                            e = big ? __ldg(a.esc + esc_lo + idx) : list_s[idx];
-                        uint32_t h = __ballot_sync(0xffffffffu, valid && ((e >> 16) & 0xFFu) - kb < 64u);
-                        while (h) {
-                            const int src = __ffs(h) - 1;
-                            h &= h - 1;
-                            patch_entry(__shfl_sync(0xffffffffu, e, src), abuf, t_lane, rlo, lane);
+                        reinterpret_cast<const uint32_t *>(smem + L::OFF_ESC + s * L::ESC + L::ESC_LIST);
+                    for (uint32_t j0 = q_lb; j0 < q_ub; j0 += 128) {
+                        uint32_t e4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t idx = j0 + 32 * u + static_cast<uint32_t>(lane);
+                            e4[u] = 0u;
+                            if (idx < q_ub) {
+                                if (big)
+                                    e4[u] = __ldg(a.esc + esc_lo + idx);
+                                else
+                                    e4[u] = list_s[idx];
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const bool valid = j0 + 32 * u + static_cast<uint32_t>(lane) < q_ub;
+                            pt.apply(e4[u], __ballot_sync(0xffffffffu, valid && ((e4[u] >> 16) & 0xFFu) - kb < 64u), v);
                         }
                     }
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(w_empty0 + 8 * s);
                 }
+                pt.finish(v);
             }
+
+            // 5. into tensor memory, once the MMA is done with this A buffer
+            wait_or_abort(a_empty0 + 8 * b, pha ^ 1, a, abort_flag);
+            __syncwarp();
+            tc_fence_after();
+            tmem_st32(tmem + static_cast<uint32_t>(b * 128) + t_lane + kb / 2, v);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();

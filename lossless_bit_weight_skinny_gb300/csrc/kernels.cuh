@@ -68,16 +68,32 @@ __device__ __forceinline__ bool sk_arrive(unsigned long long *ctr, uint32_t /*ep
     return true;
 }
 
+// Escape-list bounds of the units it0 + first + lane (one per lane; units of
+// 256 columns = one escape tile wide, row blocks of rows_blk <= 128 rows).
+__device__ __forceinline__ void load_tile_window(const GemmArgs &a, int it0, int n_it, int first,
+                                                 int lane, int rows_blk, uint32_t &lo, uint32_t &hi)
+{
+    if (first + lane < n_it) {
+        const int u = it0 + first + lane;
+        const int t = ((u / a.n_kstep) * rows_blk / 128) * a.tiles_c + u % a.n_kstep;
+        lo = __ldg(a.tile_ptr + t);
+        hi = __ldg(a.tile_ptr + t + 1);
+    }
+}
+
 __device__ __forceinline__ void report(int *status, int code)
 {
     atomicCAS(status, 0, code);
 }
 
-// The last contributor sums every partial of row block rb in contributor
-// order (fixed, so results are bitwise reproducible) and writes y.  Threads
-// [0, nthreads) of the CTA take part; each owns float4 groups of (m, 4 rows)
-// and fetches the contributors' values 4 at a time with independent 16-byte
-// loads (the sums still run in contributor order).
+// The last contributor sums every partial of row block rb and writes y.
+// Threads [0, nthreads) of the CTA take part (nthreads a multiple of 32).  Each
+// float4 group of (m, 4 rows) is given to P lanes of one warp (P a power of two,
+// up to 32, as many as the contributors and threads allow): lane j sums
+// contributors c_first + j, c_first + j + P, ... in order, with independent
+// 16-byte loads, and the P lanes then combine by a fixed butterfly.  The order
+// is fixed, so results are bitwise reproducible, and many contributors cost
+// one round of loads instead of one per contributor.
 __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int rows_blk, int grid,
                                                 int c_first, int c_last, int tid, int nthreads)
 {
@@ -85,38 +101,56 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
     const int groups = a.M * rows_blk / 4; // float4 groups per partial
     const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
     const float4 *base = reinterpret_cast<const float4 *>(a.partials);
+    const int n_contrib = c_last - c_first + 1;
     // the first contributor's slot index is 0 or 1; the others start in this
     // row block, so their slot is 2c
     const int slot_first = sk_slot(c_first, rb, grid, a.total_iters, a.n_kstep);
-    for (int g = tid; g < groups; g += nthreads) {
+    int P = 1;
+    while (P < 32 && P < n_contrib && 2 * P * groups <= nthreads)
+        P *= 2;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+    const int gpw = 32 / P; // groups per warp and pass
+    const int j = lane % P;
+    for (int gbase = warp * gpw; gbase < groups; gbase += nwarps * gpw) {
+        const int g = gbase + lane / P;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = c_first; c0 <= c_last; c0 += 4) {
-            float4 v[4];
+        if (g < groups) {
+            for (int c0 = c_first + j; c0 <= c_last; c0 += 4 * P) {
+                float4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + u;
-                if (c <= c_last) {
-                    const int slot = (c == c_first) ? slot_first : 2 * c;
-                    v[u] = __ldcg(base + slot * slot4 + g);
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + u * P;
+                    if (c <= c_last) {
+                        const int slot = (c == c_first) ? slot_first : 2 * c;
+                        v[u] = __ldcg(base + slot * slot4 + g);
+                    }
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (c0 + u <= c_last) {
-                    acc.x += v[u].x;
-                    acc.y += v[u].y;
-                    acc.z += v[u].z;
-                    acc.w += v[u].w;
+                for (int u = 0; u < 4; ++u) {
+                    if (c0 + u * P <= c_last) {
+                        acc.x += v[u].x;
+                        acc.y += v[u].y;
+                        acc.z += v[u].z;
+                        acc.w += v[u].w;
+                    }
                 }
             }
         }
-        const int m = (4 * g) / rows_blk, r = (4 * g) % rows_blk;
-        float *yp = a.y + static_cast<size_t>(m) * a.N + row0 + r;
-        const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int o = P >> 1; o >= 1; o >>= 1) {
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+        }
+        if (g < groups && j == 0) {
+            const int m = (4 * g) / rows_blk, r = (4 * g) % rows_blk;
+            float *yp = a.y + static_cast<size_t>(m) * a.N + row0 + r;
+            const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (row0 + r + q < a.N)
-                yp[q] = v4[q];
+            for (int q = 0; q < 4; ++q)
+                if (row0 + r + q < a.N)
+                    yp[q] = v4[q];
+        }
     }
 }
 
@@ -151,7 +185,7 @@ int fma_rows_blk(int mt);
 int fma_smem_bytes(int mt, bool q8);
 int tc_smem_bytes(int mt, bool q8);
 #ifndef W12_TC_MIN_M
-#define W12_TC_MIN_M 5 // smallest M sent to the tensor-core kernel (at most 5)
+#define W12_TC_MIN_M 3 // smallest M sent to the tensor-core kernel (at most 5)
 #endif
 static_assert(W12_TC_MIN_M >= 1 && W12_TC_MIN_M <= 5, "the CUDA-core kernel covers M <= 4");
 constexpr int kFmaKStep = 256;

@@ -163,8 +163,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
         return W12_ERR_UNSUPPORTED;
 
     // Kernel choice, a function of M only (measured on GB300): the CUDA-core
-    // kernel for M <= 4; above that the tensor-core kernel, padding M to 16,
-    // 32 or 64 rows, is faster than packed FMAs for 8 rows.
+    // kernel for M <= 2; from 3 rows on, the tensor-core kernel (M padded to
+    // 16, 32 or 64) is faster than four FMAs per weight.
     const bool tc = M >= W12_TC_MIN_M;
     const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);

@@ -91,8 +91,22 @@ def test_decode_bit_exact(w12, name):
 
 # ---- GEMM parity on small shapes (several tiles and ragged tails) ---------------
 
+def _flooded_rows():
+    """Rows whose window a single huge outlier drags up: row 130 (and 300, of
+    negative sign) escape almost entirely, row 131 and 40 partly, so single
+    tiles hold far more entries than the staged list and one row owns most of
+    them."""
+    W = WL.projection_weights(384, 2048, seed=27)
+    W[130, 7] = 0x7180  # +2^100: every other weight of the row is below the window
+    W[300, 2000] = 0xEC80  # -2^90
+    W[131, 900] = 0x4300  # +128: weights under 2^-8 escape
+    W[40, 5] = 0x4280  # +64
+    return W
+
+
 SHAPES = {
     "tiny_512x256": lambda: WL.tiny_weights(1)[0],
+    "flooded_384x2048": _flooded_rows,
     "ragged_300x800": lambda: WL.projection_weights(300, 800, seed=7, outlier_frac=2e-3),
     "heavy_640x1024": lambda: WL.heavy_weights(640, 1024, seed=9),
     "rows_200x4096": lambda: WL.projection_weights(200, 4096, seed=10),
