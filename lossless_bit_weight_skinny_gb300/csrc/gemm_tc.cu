@@ -626,16 +626,11 @@ __global__ void __maxnreg__(96)
                 }
                 if (!direct) {
                     // the CTA barrier orders every thread's partial stores before
-                    // thread 0's GPU-scope fence and arrival, and thread 0's fence
-                    // after the last arrival before everyone's reads
+                    // thread 0's release-acquire arrival (cumulativity), and that
+                    // arrival before everyone's reads of the other partials
                     named_bar_sync(1, kDecodeWarps * 32);
-                    if (threadIdx.x == 0) {
-                        __threadfence();
-                        const bool last = sk_arrive(a.counters + rb, a.epoch, c_last - c_first + 1);
-                        if (last)
-                            __threadfence();
-                        *seg_last = last ? 1 : 0;
-                    }
+                    if (threadIdx.x == 0)
+                        *seg_last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1 : 0;
                     named_bar_sync(1, kDecodeWarps * 32);
                     if (*seg_last)
                         sk_reduce_block(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);

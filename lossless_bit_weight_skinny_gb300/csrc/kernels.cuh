@@ -2,6 +2,7 @@
 // the stream-K work split, the deterministic split-K fix-up and the
 // bounded-wait abort protocol.
 #pragma once
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -55,13 +56,18 @@ __device__ __forceinline__ int sk_slot(int c, int rb, int grid, int iters, int n
 
 // Register one arrival for row block rb; returns true for the last of `n`
 // contributors, which also resets the count to zero for the next launch (or a
-// replay of this one from a CUDA graph).  One atomicAdd per contributor: no
-// retry loop, so many CTAs sharing a row block do not serialise on the L2.
-// Every contributor arrives exactly once even after a timeout (the kernels
-// keep their loop shape), so the count always completes and resets.
-__device__ __forceinline__ bool sk_arrive(unsigned long long *ctr, uint32_t /*epoch*/, uint32_t n)
+// replay of this one from a CUDA graph).  One atomic per contributor, with
+// acquire-release semantics at GPU scope: it publishes this CTA's partial
+// sums (stored by its threads before the CTA barrier that precedes the call)
+// and, for the last contributor, makes every other contributor's partials
+// visible to the reads after the next CTA barrier.  No retry loop, so many
+// CTAs sharing a row block do not serialise on the L2.  Every contributor
+// arrives exactly once even after a timeout (the kernels keep their loop
+// shape), so the count always completes and resets.
+__device__ __forceinline__ bool sk_arrive(unsigned long long *ctr, uint32_t n)
 {
-    const unsigned long long old = atomicAdd(ctr, 1ull);
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
     if (old + 1 != n)
         return false;
     atomicExch(ctr, 0ull);
@@ -184,6 +190,9 @@ cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap
 int fma_rows_blk(int mt);
 int fma_smem_bytes(int mt, bool q8);
 int tc_smem_bytes(int mt, bool q8);
+#ifndef W12_FMA_MIN_ITERS
+#define W12_FMA_MIN_ITERS 1 // fewest units per CTA the CUDA-core grid aims for
+#endif
 #ifndef W12_TC_MIN_M
 #define W12_TC_MIN_M 3 // smallest M sent to the tensor-core kernel (at most 5)
 #endif
@@ -191,6 +200,38 @@ static_assert(W12_TC_MIN_M >= 1 && W12_TC_MIN_M <= 5, "the CUDA-core kernel cove
 constexpr int kFmaKStep = 256;
 constexpr int kTcKStep = 256;
 constexpr int kTcRows = 128;
+
+// Grid of one GEMM launch (host side).  The units (row block, k step) are
+// split evenly over the CTAs, one CTA per SM at most; a CTA's time is about
+// its unit count, plus the tail of combining partial row blocks.  Measured on
+// GB300, that tail costs about three units when CTA boundaries fall inside row
+// blocks at random (stream-K over every SM) and about one when every CTA holds
+// an equal share of a single row block (n_rowblk * c CTAs, c dividing the k
+// steps).  The cheaper of the two estimates is launched.
+#ifndef W12_GRID_ALIGNED
+#define W12_GRID_ALIGNED 1
+#endif
+inline int choose_grid(int64_t n_rowblk, int64_t n_kstep, int sms, int64_t min_iters)
+{
+    const int64_t iters = n_rowblk * n_kstep;
+    const int64_t want = std::max<int64_t>(n_rowblk, iters / std::max<int64_t>(min_iters, 1));
+    const int64_t plain = std::min<int64_t>(sms, std::min<int64_t>(iters, want));
+    if (!W12_GRID_ALIGNED)
+        return static_cast<int>(plain);
+    const int64_t upc = (iters + plain - 1) / plain; // units per CTA, rounded up
+    const bool plain_whole = iters % plain == 0 && (upc % n_kstep == 0 || n_kstep % upc == 0);
+    int64_t best = plain, best_cost = upc + (plain_whole ? (upc < n_kstep ? 1 : 0) : 3);
+    for (int64_t c = 1; c <= n_kstep && n_rowblk * c <= std::min<int64_t>(sms, want); ++c) {
+        if (n_kstep % c != 0)
+            continue;
+        const int64_t cost = n_kstep / c + (c > 1 ? 1 : 0);
+        if (cost < best_cost) {
+            best = n_rowblk * c;
+            best_cost = cost;
+        }
+    }
+    return static_cast<int>(best);
+}
 
 cudaError_t launch_decode(const uint8_t *ebase, const uint8_t *ae, const uint8_t *b,
                           const uint32_t *tile_ptr, const uint32_t *esc, uint16_t *out, int64_t N,

@@ -191,9 +191,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
     // streams several times the weight bytes of the partial sums it writes
     // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
-    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : 1;
-    const int64_t want = std::max<int64_t>(a.n_rowblk, iters / min_iters);
-    const int grid = static_cast<int>(std::min<int64_t>(sm_count(cur), std::min<int64_t>(iters, want)));
+    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : W12_FMA_MIN_ITERS;
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur), min_iters);
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters, &a.epoch);
