@@ -87,6 +87,7 @@ struct TcSmem {
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
+// Bounded wait that also gives up as soon as another warp has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmArgs &a,
                                               volatile int *abort_flag)
 {
@@ -378,6 +379,13 @@ __global__ void __maxnreg__(96)
     } else if (warp == kWarpM) {
         // ------------------------------ MMA issuer -----------------------------
         if (lane == 0) {
+            // shared-memory descriptor of each activation slot's first sub-tile;
+            // the 16 K-steps of a unit add a fixed offset (address field in
+            // 16-byte units: +2 per 16 columns, +XSUB/16 per 64-column sub-tile)
+            uint64_t xdesc[XST];
+#pragma unroll
+            for (int j = 0; j < XST; ++j)
+                xdesc[j] = smem_desc_sw128(smem_u32(smem + L::OFF_X + j * L::XSTAGE), 1024);
             int seg = 0;
             int ks = it0 % nk, sx = 0, b = 0;
             uint32_t phx = 0, pha = 0;
@@ -393,14 +401,18 @@ __global__ void __maxnreg__(96)
                 ok = wait_or_abort(x_full0 + 8 * sx, phx, a, abort_flag) && ok;
                 tc_fence_after();
                 if (ok) {
-                    const uint32_t xs = smem_u32(smem + L::OFF_X + sx * L::XSTAGE);
-                    const uint32_t d = tmem + kDCol + 64 * db;
+                    uint64_t bdesc = xdesc[0];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint32_t b_addr = xs + (j >> 2) * L::XSUB + (j & 3) * 32;
-                        const uint64_t bdesc = smem_desc_sw128(b_addr, 1024);
-                        tc_mma_ts(d, tmem + b * 128 + j * 8, bdesc, IDESC, (j > 0 || !seg_start) ? 1u : 0u);
-                    }
+                    for (int j = 1; j < XST; ++j)
+                        if (sx == j)
+                            bdesc = xdesc[j];
+                    const uint32_t d = tmem + kDCol + 64 * db;
+                    const uint32_t a0 = tmem + b * 128;
+                    tc_mma_ts(d, a0, bdesc, IDESC, seg_start ? 0u : 1u);
+#pragma unroll
+                    for (int j = 1; j < 16; ++j)
+                        tc_mma_ts_acc(d, a0 + j * 8,
+                                      bdesc + static_cast<uint64_t>((j >> 2) * (L::XSUB >> 4) + (j & 3) * 2), IDESC);
                 }
                 // each commit arrives once every MMA issued so far has completed
                 tc_commit(a_empty0 + 8 * b);
