@@ -1,4 +1,5 @@
-// gemm_fma.cu -- W12 skinny GEMM for M <= 4 activation rows on the CUDA cores.
+// gemm_fma.cu -- W12 skinny GEMM for M <= 4 activation rows on the CUDA cores
+// (the library sends it M <= 2; from 3 rows on the tensor-core kernel is faster).
 //
 // y[m][n] = sum_k x[m][k] * W[n][k], W decoded from its W12 planes to exact
 // BF16 values (SpecPilot, Figure 5(a) caption) in registers and accumulated in
