@@ -111,53 +111,17 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
-// One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
-// holding those two bytes and its B word:
-//   PRMT spreads the two AE bytes into two 16-bit lanes, replicating each byte's
-//   sign into the lane's high byte; then per lane
-//   sign (bit 15) | (ebase + E) << 7 | (A & 7) << 4 | B.
-// Written as explicit PTX so that it stays PRMT + LOP3/IMAD/LOP3 + SHF/LOP3.
-template <int I, bool Q8>
-__device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, uint32_t eb2)
-{
-    uint32_t p, t, r;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(p) : "r"(ae_word), "n"((I & 1) ? 0xB3A2 : 0x9180));
-    asm("and.b32 %0, %1, 0x000F000F;" : "=r"(t) : "r"(p));
-    asm("mad.lo.u32 %0, %1, 128, %2;" : "=r"(t) : "r"(t), "r"(eb2));
-    asm("lop3.b32 %0, %1, 0x80708070, %2, 0xEA;" : "=r"(r) : "r"(p), "r"(t)); // (p & m) | t
-    if (!Q8) {
-        uint32_t b = bw;
-        if (I)
-            asm("shr.b32 %0, %1, %2;" : "=r"(b) : "r"(bw), "n"(4 * I));
-        asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(b), "r"(r)); // (b & m) | r
-    }
-    return r;
-}
-
 // Decode 8 weights (AE bytes k..k+7, their B word) to FP32 values.
 template <bool Q8>
 __device__ __forceinline__ void decode8(uint2 ae, uint32_t bw, uint32_t eb2, float (&wf)[8])
 {
-    const uint32_t r0 = decode_pair<0, Q8>(ae.x, bw, eb2);
-    const uint32_t r1 = decode_pair<1, Q8>(ae.x, bw, eb2);
-    const uint32_t r2 = decode_pair<2, Q8>(ae.y, bw, eb2);
-    const uint32_t r3 = decode_pair<3, Q8>(ae.y, bw, eb2);
-    const uint32_t r[4] = {r0, r1, r2, r3};
+    uint32_t r[4];
+    decode_group<Q8>(ae.x, ae.y, bw, eb2, r);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         wf[2 * i] = __uint_as_float(r[i] << 16);
         wf[2 * i + 1] = __uint_as_float(r[i] & 0xFFFF0000u);
     }
-}
-
-// The same 8 weights left as four BF16x2 words.
-template <bool Q8>
-__device__ __forceinline__ void decode8_bf16x2(uint2 ae, uint32_t bw, uint32_t eb2, uint32_t (&r)[4])
-{
-    r[0] = decode_pair<0, Q8>(ae.x, bw, eb2);
-    r[1] = decode_pair<1, Q8>(ae.x, bw, eb2);
-    r[2] = decode_pair<2, Q8>(ae.y, bw, eb2);
-    r[3] = decode_pair<3, Q8>(ae.y, bw, eb2);
 }
 
 // acc.x += lo(w) * lo(x), acc.y += hi(w) * hi(x) on BF16 halves with FP32
@@ -569,7 +533,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 const uint32_t bw = bwr[r];
                 if constexpr (kMixed) {
                     uint32_t wr[4];
-                    decode8_bf16x2<Q8>(aw[r], bw, eb2[r], wr);
+                    decode_group<Q8>(aw[r].x, aw[r].y, bw, eb2[r], wr);
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
 #pragma unroll

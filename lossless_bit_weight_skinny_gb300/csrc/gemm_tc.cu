@@ -111,39 +111,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     }
 }
 
-// One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
-// holding those two bytes and its B word:
-//   PRMT spreads the two AE bytes into two 16-bit lanes, replicating each
-//   byte's sign into the lane's high byte; then per lane
-//   sign (bit 15) | (ebase + E) << 7 | (A & 7) << 4 | B.
-template <int I, bool Q8>
-__device__ __forceinline__ uint32_t decode_pair(uint32_t ae_word, uint32_t bw, uint32_t eb2)
-{
-    uint32_t p, t, r;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(p) : "r"(ae_word), "n"((I & 1) ? 0xB3A2 : 0x9180));
-    asm("and.b32 %0, %1, 0x000F000F;" : "=r"(t) : "r"(p));
-    asm("mad.lo.u32 %0, %1, 128, %2;" : "=r"(t) : "r"(t), "r"(eb2));
-    asm("lop3.b32 %0, %1, 0x80708070, %2, 0xEA;" : "=r"(r) : "r"(p), "r"(t)); // (p & m) | t
-    if (!Q8) {
-        uint32_t b = bw;
-        if (I)
-            asm("shr.b32 %0, %1, %2;" : "=r"(b) : "r"(bw), "n"(4 * I));
-        asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(b), "r"(r)); // (b & m) | r
-    }
-    return r;
-}
-
-// 8 weights (AE bytes of the group as two words, its B word) -> 4 BF16x2 pairs.
-template <bool Q8>
-__device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint32_t bw, uint32_t eb2,
-                                             uint32_t *out)
-{
-    out[0] = decode_pair<0, Q8>(a_lo, bw, eb2);
-    out[1] = decode_pair<1, Q8>(a_lo, bw, eb2);
-    out[2] = decode_pair<2, Q8>(a_hi, bw, eb2);
-    out[3] = decode_pair<3, Q8>(a_hi, bw, eb2);
-}
-
 // Patch escapes into a decode thread's 32 BF16 pairs v (columns kb..kb+63 of
 // its row) before they go to tensor memory.  The list is sorted by row, so the
 // entries of one row are consecutive: the owning lane parks its pairs in the
