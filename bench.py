@@ -5,7 +5,10 @@ with hidden 5120 / intermediate 17408 / 8 KV heads of 128 -- q 5120x5120,
 k 1024x5120, v 1024x5120, o 5120x5120, gate 17408x5120, up 17408x5120,
 down 5120x17408 -- with W ~ N(0, 0.02^2) x per-row U(0.5, 2) and 1e-4
 Student-t(2) x 0.5 outliers, x ~ N(0, 1).  One step = the 7 W12 GEMMs of one
-layer; steps rotate over several independently drawn layers, each ~0.5 GB of
+layer, launched as a decode step would: q/k/v read one activation vector and
+gate/up another, so k, v and up are launched input-ready (they may overlap the
+tail of the GEMM before them); q, o, gate and down wait for the kernel before
+them.  Steps rotate over several independently drawn layers, each ~0.5 GB of
 W12 data, so every step streams its weights from HBM (inputs > L2).
 
 Prints one JSON line (rank 0).  `--impl reference` times the scalar CPU oracle
@@ -34,6 +37,15 @@ WORKLOAD = ("single-row decode projections, M=1: q/o 5120x5120, k/v 1024x5120, g
             "17408x5120, down 5120x17408 (one dense layer; N(0,0.02^2) x U(0.5,2) rows, "
             "1e-4 Student-t(2)x0.5 outliers)")
 FALLBACK_HBM_GBS = 6800.0
+
+# Activations of one dense layer's projections: q, k and v read one vector,
+# gate and up another; o and down read the outputs of attention and of the MLP
+# activation.  In a decode step, the launches of k, v and up therefore find
+# their input complete before the preceding GEMM starts (input-ready launch);
+# q, o, gate and down wait for the kernel before them.
+ACT_GROUPS = {"qkv": 5120, "o": 5120, "gate_up": 5120, "down": 17408}
+PROJ_GROUP = {"q": "qkv", "k": "qkv", "v": "qkv", "o": "o", "gate": "gate_up", "up": "gate_up", "down": "down"}
+READY_IN_LAYER = {"k", "v", "up"}
 
 
 def _peaks():
@@ -171,21 +183,28 @@ def run_w12(args):
 
     layers = _make_layers(w12, torch, args.layers)
     M = 1
-    xs = {}
-    ys = {}
-    for name, N, K in WL.LAYER_PROJECTIONS:
-        xs[name] = torch.from_numpy(WL.activations(M, K, seed=7).view(np.int16)).cuda().view(torch.bfloat16)
-        ys[name] = torch.empty((M, N), dtype=torch.float32, device="cuda")
+
+    def acts(Mx, seed):
+        """One activation vector per group (q/k/v share one, gate/up another)."""
+        return {g: torch.from_numpy(WL.activations(Mx, K, seed=seed + gi).view(np.int16)).cuda()
+                .view(torch.bfloat16) for gi, (g, K) in enumerate(ACT_GROUPS.items())}
+
+    xs = acts(M, 7)
+    ys = {name: torch.empty((M, N), dtype=torch.float32, device="cuda") for name, N, K in WL.LAYER_PROJECTIONS}
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     n_proj = len(WL.LAYER_PROJECTIONS)
 
-    def step(i, ev=None):
+    def launch(mode, name, d, x, y):
+        ready = mode == "independent" or (mode == "layer" and name in READY_IN_LAYER)
+        w12.w12_gemm_ex(x, d, y, stream, input_ready=ready)
+
+    def step(i, ev=None, mode="layer"):
         layer = layers[i % len(layers)]
         for j, (name, d, st) in enumerate(layer):
             if ev is not None:
                 ev[j][0].record(stream)
-            w12.w12_gemm(xs[name], d, ys[name], stream)
+            launch(mode, name, d, xs[PROJ_GROUP[name]], ys[name])
             if ev is not None:
                 ev[j][1].record(stream)
 
@@ -200,8 +219,7 @@ def run_w12(args):
     # layers), with nothing between the GEMM launches so that each may overlap
     # the previous one's tail (programmatic dependent launch).  Right after it,
     # still on the same warm state, a second graph with an event pair around
-    # every launch gives each kernel's own duration for the roofline (without
-    # that overlap, so slightly pessimistic).
+    # every launch gives each kernel's own duration (without that overlap).
     G = args.graph_steps
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
@@ -215,7 +233,7 @@ def run_w12(args):
         graph_ev = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_ev, stream=stream):
             for i in range(G):
-                step(i, evs[i])
+                step(i, evs[i], mode="none")
         graph_ev.replay()
         torch.cuda.synchronize()
     except TypeError:
@@ -278,16 +296,12 @@ def run_w12(args):
     achieved_isolated = kern_bytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None
     traffic = _traffic("gemm_fma_m1", step_bytes / n_proj)
 
-    # the same layer at M = 32 and M = 64 (tensor-core path), shorter runs
-    by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
-    for Mx in (32, 64):
-        xm = {n: torch.from_numpy(WL.activations(Mx, K, seed=9).view(np.int16)).cuda().view(torch.bfloat16)
-              for n, N, K in WL.LAYER_PROJECTIONS}
-        ym = {n: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
-
+    def time_graph(Mx, xs_, ys_, mode, greps):
+        """Replay a G-step graph of the layer at Mx rows in launch mode `mode`;
+        returns ms per step."""
         def stepm(i):
             for name, d, st in layers[i % len(layers)]:
-                w12.w12_gemm(xm[name], d, ym[name], stream)
+                launch(mode, name, d, xs_[PROJ_GROUP[name]], ys_[name])
 
         for i in range(max(3, args.warmup // 4)):
             stepm(i)
@@ -299,24 +313,35 @@ def run_w12(args):
         gm.replay()
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        greps = max(2, args.steps // (4 * G))
-        nsteps = greps * G
         s0.record(stream)
         for _ in range(greps):
             gm.replay()
         s1.record(stream)
         torch.cuda.synchronize()
-        msm = s0.elapsed_time(s1)
         for layer in layers:
             for _, d, _ in layer:
                 assert w12.w12_dev_status(d) == 0
+        return s0.elapsed_time(s1) / (greps * G)
+
+    # the same step with every launch waiting for the previous kernel, and with
+    # every launch input-ready (the synthetic activations are all independent)
+    short = max(2, args.steps // (4 * G))
+    modes_us = {"layer": round(1e3 * ms / args.steps, 2),
+                "no_overlap": round(1e3 * time_graph(M, xs, ys, "none", short), 2),
+                "independent_inputs": round(1e3 * time_graph(M, xs, ys, "independent", short), 2)}
+
+    # the same layer at M = 32 and M = 64 (tensor-core path), shorter runs
+    by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
+    for Mx in (32, 64):
+        xm = acts(Mx, 9)
+        ym = {n: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
+        msm = time_graph(Mx, xm, ym, "layer", short)
         bm = _step_bytes(layers[0], Mx)
-        by_m[str(Mx)] = {"weight_GBps": round(bm * nsteps / (msm * 1e-3) / 1e9, 1),
-                         "us_per_layer": round(1e3 * msm / nsteps, 2)}
+        by_m[str(Mx)] = {"weight_GBps": round(bm / (msm * 1e-3) / 1e9, 1), "us_per_layer": round(1e3 * msm, 2)}
 
     # end to end through the host-buffer entry point: pinned x in, y out, per step
     xh = {n: torch.from_numpy(WL.activations(M, K, seed=7).view(np.int16)).pin_memory()
-          for n, N, K in WL.LAYER_PROJECTIONS}
+          for n, N, K in WL.LAYER_PROJECTIONS}  # the host entry copies each projection's own input
     yh = {n: torch.empty((M, N), dtype=torch.float32).pin_memory() for n, N, K in WL.LAYER_PROJECTIONS}
     xd = {n: torch.empty((M, K), dtype=torch.int16, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
 
@@ -363,7 +388,10 @@ def run_w12(args):
                 "workload": WORKLOAD,
                 "M": M,
                 "layers_rotated": args.layers,
-                "step": "7 GEMMs (q,k,v,o,gate,up,down) of one layer",
+                "step": "7 GEMMs (q,k,v,o,gate,up,down) of one layer; q/k/v share one activation "
+                        "vector and gate/up another; k, v and up launch input-ready (their input "
+                        "exists before the preceding GEMM starts), the others wait for the kernel "
+                        "before them",
                 "bytes_per_step": step_bytes,
                 "l2": "inputs larger than L2: each step streams ~0.5 GB of W12 weights",
                 "escape_fraction": round(sum(s["n_escapes"] for s in st_all)
@@ -373,6 +401,7 @@ def run_w12(args):
                 "parallelism": f"replicas x{world}",
             },
             "by_M": by_m,
+            "us_per_layer_by_launch_mode": modes_us,
             "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
             "roofline": {
                 "bound": "hbm",

@@ -157,6 +157,30 @@ w12_status w12_gemm(const void *x_bf16, const w12_dev *w, float *y, int M, int N
 w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
                            w12_stream_t stream);
 
+/* Flags of w12_gemm_ex. */
+enum {
+    W12_GEMM_Q8VIEW = 1,      /* the Q pass (as w12_gemm_q8view) instead of the exact GEMM */
+    W12_GEMM_INPUT_READY = 2  /* x was complete before the previous operation on the stream started */
+};
+
+/*
+ * w12_gemm / w12_gemm_q8view with flags.  Arguments, limits and errors are
+ * w12_gemm's; an unknown flag bit gives INVALID_ARG.
+ *
+ * Every GEMM launch may begin (streaming its weights) while the previous
+ * kernel on the stream is still finishing; by default it reads x only after
+ * that kernel has completed, since that kernel may have produced x.
+ * W12_GEMM_INPUT_READY is the caller's statement that x was complete before
+ * the previous operation on the stream started -- for instance several
+ * projections of one activation vector issued back to back, or inputs copied
+ * earlier.  The launch then reads x at once and overlaps the previous kernel's
+ * tail.  It still writes nothing (y, its workspace) before the previous kernel
+ * has completed, so the previous kernel may read or write y.  The flag has no
+ * counterpart on the pages: it is a launch-overlap mode of this library.
+ */
+w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                       unsigned flags, w12_stream_t stream);
+
 /*
  * End-to-end form of w12_gemm for host-resident activations: copies
  * x_host -> x_dev, runs w12_gemm into y_dev, copies y_dev -> y_host, all on

@@ -79,6 +79,7 @@ _sig("w12_dev_free", [_P], None)
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
+_sig("w12_gemm_ex", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_noalloc", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_last_cuda_error", [], ctypes.c_char_p)
@@ -93,8 +94,11 @@ EXPORTED = (
     "w12_validate", "w12_serialize", "w12_deserialize", "w12_save", "w12_load", "w12_upload",
     "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
-    "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error",
+    "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
 )
+
+W12_GEMM_Q8VIEW = 1
+W12_GEMM_INPUT_READY = 2
 
 
 class W12Error(RuntimeError):
@@ -276,6 +280,22 @@ def w12_gemm(x, d: Dev, y=None, stream=None):
 def w12_gemm_q8view(x, d: Dev, y=None, stream=None):
     """The Q pass: the same product over the 8-bit A+E view only."""
     return _gemm(_lib.w12_gemm_q8view, "w12_gemm_q8view", x, d, y, stream)
+
+
+def w12_gemm_ex(x, d: Dev, y=None, stream=None, q8view=False, input_ready=False):
+    """w12_gemm (or the Q pass) with flags; input_ready states that x was
+    complete before the previous operation on the stream started, so the
+    launch may read it at once and overlap that operation's tail."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, d.N), dtype=torch.float32, device=x.device)
+    flags = (W12_GEMM_Q8VIEW if q8view else 0) | (W12_GEMM_INPUT_READY if input_ready else 0)
+    _check(_lib.w12_gemm_ex(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
+                            flags, _stream_ptr(stream)), "w12_gemm_ex")
+    return y
 
 
 def w12_gemm_noalloc(x, d: Dev, y, stream=None):

@@ -37,19 +37,25 @@ namespace {
 #define W12_FMA_MIXED 1 // M <= 2: BF16 x BF16 -> FP32 FMAs instead of packed FP32 FMAs
 #endif
 
-#ifndef W12_FMA_RBLK
-#define W12_FMA_RBLK 128 // rows per block (and per ring stage): 128 or 64
+#ifndef W12_FMA_CPS
+#define W12_FMA_CPS 1 // CTAs per SM of the M = 1 kernel (1 or 2)
 #endif
+
 
 template <int MT>
 struct FmaShape {
-    static constexpr int RBLK = W12_FMA_RBLK;                 // rows per block
-    static constexpr int CW = W12_FMA_CW ? W12_FMA_CW : (MT == 1 ? 16 : 8); // consumer warps
+    // CTAs resident per SM: two for M = 1, so that the next kernel's CTAs can
+    // start streaming while this kernel's last ones finish; each then works
+    // on blocks of 64 rows (half an escape tile)
+    static constexpr int CPS = MT == 1 ? W12_FMA_CPS : 1;
+    static constexpr int RBLK = CPS == 2 ? 64 : 128;          // rows per block
+    static constexpr int CW = W12_FMA_CW ? W12_FMA_CW : (MT == 1 ? 16 / CPS : 8); // consumer warps
+    static constexpr int NE = CPS == 2 ? 1 : 2;               // escape warps
     static constexpr int RW = RBLK / CW;                      // rows per consumer warp
-    static constexpr int THREADS = (CW + 3) * 32; // + producer + two escape warps
-    // registers per thread for one resident CTA: each of the 4 SM sub-partitions
-    // has 16K registers and holds ceil(warps / 4) of the CTA's warps
-    static constexpr int PER_SMSP = (CW + 3 + 3) / 4;
+    static constexpr int THREADS = (CW + 1 + NE) * 32;        // + producer + escape warps
+    // registers per thread: each of the 4 SM sub-partitions has 16K registers
+    // and holds ceil(warps / 4) of the resident CTAs' warps
+    static constexpr int PER_SMSP = (CPS * (CW + 1 + NE) + 3) / 4;
     static constexpr int MAXREG_RAW = (16384 / (32 * PER_SMSP)) & ~7;
     static constexpr int MAXREG = MAXREG_RAW > 255 ? 255 : MAXREG_RAW;
     static_assert(RW % 8 == 0 && RBLK % CW == 0, "warps own whole 8-row escape groups");
@@ -75,8 +81,8 @@ struct FmaSmem {
     static constexpr int STAGE = r1024(OFF_ESC + ESC);
     // per escape warp: correction sums [buffer][neg, pos][RBLK * MT], window bases
     static constexpr int CORR_W = 2 * 2 * S::RBLK * MT * 4 + S::RBLK;
-    static constexpr int CORR = Q8 ? 0 : 2 * CORR_W;
-    static constexpr int BUDGET = 227 * 1024 - 2048;
+    static constexpr int CORR = Q8 ? 0 : S::NE * CORR_W;
+    static constexpr int BUDGET = (227 * 1024) / S::CPS - 2048;
     static constexpr int STAGES_RAW = (BUDGET - CORR) / STAGE;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int TX_BYTES = AE + B + X;
@@ -84,7 +90,7 @@ struct FmaSmem {
     static constexpr int BARS = OFF_CORR + CORR;         // barrier area offset
     static constexpr int NBARS = 2 * STAGES + 1 + 4;     // full, empty, stall, corr_full/empty
     static constexpr int TOTAL = BARS + 8 * NBARS + 16 + 1024; // + slack to align the base
-    static_assert(STAGES >= 3 && TOTAL <= 227 * 1024, "shared memory budget");
+    static_assert(STAGES >= 4 / S::CPS && TOTAL <= (227 * 1024) / S::CPS, "shared memory budget");
 };
 
 // Bounded wait that also gives up as soon as another warp has aborted.
@@ -256,7 +262,8 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     constexpr int V = RW * MT;           // per-lane partial sums
     constexpr int VPL = V >= 32 ? V / 32 : 1;
     constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : 3;
-    constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warps WARP_E and WARP_E + 1
+    constexpr int NE = S::NE;
+    constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warps WARP_E .. WARP_E + NE - 1
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -281,11 +288,11 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(empty0 + 8 * s, Q8 ? CW : CW + 2);
+            mbar_init(empty0 + 8 * s, Q8 ? CW : CW + NE);
         }
         mbar_init(stall_bar, 1);
         for (int d = 0; d < 2; ++d) {
-            mbar_init(corr_full0 + 8 * d, 64);
+            mbar_init(corr_full0 + 8 * d, 32 * NE);
             mbar_init(corr_empty0 + 8 * d, CW);
         }
         *abort_flag = 0;
@@ -322,9 +329,10 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const uint32_t fb = full0 + 8 * s;
             // The first ring's worth of weights streams before the previous
             // kernel in the stream has finished; activations, which it may have
-            // written, only after it has (every write of this kernel follows an
-            // activation load).
-            const int pre = n_it < STAGES ? n_it : STAGES;
+            // written, only after it has -- unless the caller declared them
+            // complete before that kernel started.  (Writes wait for the
+            // previous kernel in any case: see the row-block end.)
+            const int pre = a.x_ready ? 0 : (n_it < STAGES ? n_it : STAGES);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::TX_BYTES);
                 tma_load_2d(smem_u32(st + L::OFF_AE), &tm_ae, k0, row0, fb);
@@ -373,7 +381,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int s = it % STAGES;
             mbar_wait(full0 + 8 * s, (it / STAGES) & 1, 1000000000ull);
         }
-    } else if (warp == WARP_E || warp == WARP_E + 1) {
+    } else if (warp >= WARP_E && warp < WARP_E + NE) {
         // ---------------------------- escape warps ----------------------------
         // Escape warp E takes the units of parity E.  Per unit, the tile's
         // entries 32 at a time, one per lane: the two products -x * placeholder
@@ -407,7 +415,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 ok = __all_sync(0xffffffffu, ok);
                 const int row0 = rb * RBLK;
                 const uint8_t *st = smem + s * L::STAGE;
-                if (ok && ((it0 + it) & 1) == ew) {
+                if (ok && (NE == 1 || ((it0 + it) & 1) == ew)) {
                     const uint8_t *esc_area = st + L::OFF_ESC;
                     const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
                     const uint32_t cnt = lohi.y - lohi.x;
@@ -427,7 +435,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 if (lane == 0)
                     mbar_arrive(empty0 + 8 * s);
                 if (seg_end) {
-                    mbar_arrive(corr_full0 + 8 * db); // all 64 lanes: their sums are visible
+                    mbar_arrive(corr_full0 + 8 * db); // every escape lane: its sums are visible
                     ++seg;
                 }
                 if (++ks == nk) {
@@ -571,6 +579,9 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
 
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- the row block ends here for this CTA: reduce and store ----
+                // nothing is written before the previous kernel in the stream
+                // has completed (at once when the activation load waited for it)
+                pdl_wait_prior_grid();
                 float v[V];
 #pragma unroll
                 for (int r = 0; r < RW; ++r)
@@ -588,7 +599,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 if (!Q8)
                     wait_or_abort(corr_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
                 const float *cneg0 = corr_of(0) + db * (2 * RBLK * MT), *cpos0 = cneg0 + RBLK * MT;
-                const float *cneg1 = corr_of(1) + db * (2 * RBLK * MT), *cpos1 = cneg1 + RBLK * MT;
+                const float *cneg1 = corr_of(NE - 1) + db * (2 * RBLK * MT), *cpos1 = cneg1 + RBLK * MT;
                 const int c_first = sk_owner(rb * nk, grid, a.total_iters);
                 const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
                 const bool writer = (V >= 32) || ((lane & ((32 >> LOGV) - 1)) == 0);
@@ -602,7 +613,10 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     float total = v[q];
                     if (!Q8) {
                         const int i = (wrow + r) * MT + m;
-                        total = (total + (cneg0[i] + cneg1[i])) + (cpos0[i] + cpos1[i]);
+                        if constexpr (NE == 1)
+                            total = (total + cneg0[i]) + cpos0[i];
+                        else
+                            total = (total + (cneg0[i] + cneg1[i])) + (cpos0[i] + cpos1[i]);
                     }
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
@@ -664,7 +678,9 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtens
 
 } // namespace
 
-int fma_rows_blk(int) { return W12_FMA_RBLK; }
+int fma_rows_blk(int mt) { return mt == 1 ? FmaShape<1>::RBLK : FmaShape<2>::RBLK; }
+
+int fma_ctas_per_sm(int mt) { return mt == 1 ? FmaShape<1>::CPS : 1; }
 
 int fma_smem_bytes(int mt, bool q8)
 {

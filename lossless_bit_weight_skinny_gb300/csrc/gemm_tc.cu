@@ -316,8 +316,10 @@ __global__ void __maxnreg__(96)
             prefetch_tmap(&tm_x);
             // weights stream before the previous kernel in the stream has
             // finished; activations, which it may have written, only after it
-            // has (every write of this kernel follows an activation load)
-            pdl_wait_prior_grid();
+            // has -- unless the caller declared them complete before that
+            // kernel started (writes wait for it in any case: see the epilogue)
+            if (!a.x_ready)
+                pdl_wait_prior_grid();
             int issued = 0;
             int ks = it0 % nk, s = 0;
             uint32_t ph = 0;
@@ -546,6 +548,9 @@ __global__ void __maxnreg__(96)
 
             if (ks == nk - 1 || it == n_it - 1) {
                 // ---- accumulators of this row block are final: read them out ----
+                // nothing is written before the previous kernel in the stream
+                // has completed (at once when the activation load waited for it)
+                pdl_wait_prior_grid();
                 const int db = seg & 1;
                 wait_or_abort(acc_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
                 __syncwarp();

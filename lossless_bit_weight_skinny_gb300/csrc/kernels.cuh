@@ -32,6 +32,7 @@ struct GemmArgs {
     uint32_t epoch;                // call counter (diagnostic only)
     uint64_t limit_ns;             // bounded-wait limit
     int inject_stall;              // test hook: wait on a barrier nobody arrives on
+    int x_ready;                   // x was complete before the previous launch: load it at once
 };
 
 // One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
@@ -223,6 +224,7 @@ cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap
                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                            cudaStream_t st);
 int fma_rows_blk(int mt);
+int fma_ctas_per_sm(int mt);
 int fma_smem_bytes(int mt, bool q8);
 int tc_smem_bytes(int mt, bool q8);
 #ifndef W12_FMA_MIN_ITERS

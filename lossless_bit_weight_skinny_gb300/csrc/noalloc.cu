@@ -157,7 +157,7 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     a.n_kstep = static_cast<int>(ceil_div(K, kstep));
     const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
     const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sms, min_iters);
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sms * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     // the fixed array must hold the counters and the partial sums of this call
     if (iters > (int64_t(1) << 30) || static_cast<size_t>(a.n_rowblk) * 8 > kNoAllocCounterBytes ||
@@ -166,6 +166,7 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     a.total_iters = static_cast<int>(iters);
     a.limit_ns = 200ull * 1000 * 1000;
     a.inject_stall = 0;
+    a.x_ready = 0;
 
     unsigned char *scratch = nullptr;
     const w12_status s = noalloc_setup(dev, &scratch);

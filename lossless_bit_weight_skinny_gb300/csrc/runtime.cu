@@ -136,7 +136,7 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, int K,
-                     cudaStream_t st, bool q8)
+                     cudaStream_t st, bool q8, bool x_ready = false)
 {
     if (!w || M < 0)
         return W12_ERR_INVALID_ARG;
@@ -188,11 +188,12 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     a.total_iters = static_cast<int>(iters);
     a.limit_ns = g_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
+    a.x_ready = x_ready ? 1 : 0;
     // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
     // streams several times the weight bytes of the partial sums it writes
     // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
     const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur), min_iters);
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur) * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters, &a.epoch);
@@ -350,6 +351,15 @@ w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M
                            w12_stream_t stream)
 {
     return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                       unsigned flags, w12_stream_t stream)
+{
+    if (flags & ~static_cast<unsigned>(W12_GEMM_Q8VIEW | W12_GEMM_INPUT_READY))
+        return W12_ERR_INVALID_ARG;
+    return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream),
+                     (flags & W12_GEMM_Q8VIEW) != 0, (flags & W12_GEMM_INPUT_READY) != 0);
 }
 
 w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, float *y_dev,

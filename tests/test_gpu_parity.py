@@ -316,3 +316,44 @@ def test_timeout_reports_and_recovers(w12, M):
         w12.w12_debug_inject_stall(False)
         w12.w12_set_spin_limit(0)
     _check(_gemm(w12, d, x), x, Wdec, what="after timeout")
+
+
+def test_input_ready_chain(w12):
+    """Launches flagged input-ready read x at once and overlap the previous
+    kernel's tail, but write only after it has completed: a chain of them
+    (both kernels, split-K shapes, one y reused by consecutive launches) gives
+    bitwise the results of plain w12_gemm."""
+    import torch
+
+    cases = []
+    for name in ("rows_200x4096", "ragged_300x800", "heavy_640x1024", "flooded_384x2048"):
+        W, Wdec, Wq, d = _prepared(w12, name)
+        for M in (1, 2, 16, 64):
+            x = _xdev(WL.activations(M, W.shape[1], seed=4000 + M))
+            cases.append((d, x, w12.w12_gemm(x, d)))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ys = [torch.full_like(ref, float("nan")) for _, _, ref in cases]
+    shared = {}
+    for i, (d, x, ref) in enumerate(cases):
+        w12.w12_gemm_ex(x, d, ys[i], stream, input_ready=(i > 0))
+        # the same output buffer written by two consecutive launches
+        key = tuple(ref.shape)
+        if key in shared:
+            w12.w12_gemm_ex(x, d, shared[key], stream, input_ready=True)
+        else:
+            shared[key] = torch.full_like(ref, float("nan"))
+            w12.w12_gemm_ex(x, d, shared[key], stream, input_ready=True)
+        shared[key + ("last",)] = ref
+    torch.cuda.synchronize()
+    for i, (d, x, ref) in enumerate(cases):
+        assert w12.w12_dev_status(d) == 0
+        assert torch.equal(ys[i], ref), f"case {i}"
+    for key, buf in shared.items():
+        if key[-1] != "last":
+            assert torch.equal(buf, shared[key + ("last",)]), f"shared {key}"
+    # unknown flag bits are refused
+    d, x, ref = cases[0]
+    P = __import__("ctypes").c_void_p
+    assert w12.lib().w12_gemm_ex(P(x.data_ptr()), d.ptr, P(ys[0].data_ptr()), x.shape[0], d.N, x.shape[1],
+                                 8, P(stream.cuda_stream)) == 1
