@@ -39,7 +39,9 @@ constexpr int kDecodeWarps = 16;
 constexpr int kWarpW = kDecodeWarps;     // weight producer
 constexpr int kWarpX = kDecodeWarps + 1; // activation producer
 constexpr int kWarpM = kDecodeWarps + 2; // MMA issuer, tensor-memory owner
-constexpr int kThreads = (kDecodeWarps + 3) * 32;
+constexpr int kWarpE = kDecodeWarps + 3; // escape warp: sorts each unit's escapes per decode warp
+constexpr int kThreads = (kDecodeWarps + 4) * 32;
+constexpr int kPCap = 16;                // escapes per decode warp and unit kept in its list
 constexpr int kNA = 3;                   // A buffers in tensor memory, 128 columns each
 constexpr uint32_t kDCol = kNA * 128;    // two accumulator buffers of 64 columns
 static_assert(kTcKStep == 256 && kTcRows == 128, "one unit = one escape tile");
@@ -59,10 +61,17 @@ struct TcSmem {
     // the unit's escape area, one per weight stage in a ring of its own:
     // [lo, hi, -, -] u32, the row-group index u16[16], up to ESC_CAP entries
     // (a tile with more is read from global memory)
-    static constexpr int ESC_CAP = 256;
+    static constexpr int ESC_CAP = 128;
     static constexpr int ESC_GP = 16;
     static constexpr int ESC_LIST = 48;
     static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
+    // the escape warp's per-unit output, one per weight stage: entry count
+    // per decode warp u32[16], the unit's list start and length u32[2], then
+    // up to kPCap entries per decode warp (a larger count means "read the
+    // list yourself")
+    static constexpr int PL_LO = 64;
+    static constexpr int PL_LIST = 80;
+    static constexpr int PL = Q8 ? 0 : PL_LIST + 4 * kPCap * kDecodeWarps;
     // activation stage: four 64-column sub-tiles of MT rows, 128-byte swizzle
     static constexpr int XSUB = MT * 128;
     static constexpr int XSTAGE = 4 * XSUB;
@@ -71,15 +80,16 @@ struct TcSmem {
     static constexpr int SCR_PITCH = 144;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * SCR_PITCH;
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + ESC);
+    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + ESC + PL);
     static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight slots
     static constexpr int OFF_X = WST * WSTAGE;
     static constexpr int OFF_ESC = OFF_X + XST * XSTAGE;
     static constexpr int OFF_SCR = OFF_ESC + WST * ESC;
-    static constexpr int BARS = (OFF_SCR + SCR + 15) & ~15;
+    static constexpr int OFF_PL = OFF_SCR + SCR;
+    static constexpr int BARS = (OFF_PL + WST * PL + 15) & ~15;
     // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
-    // acc_full, acc_empty [2]; final, stall
-    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4 + 2;
+    // acc_full, acc_empty [2]; final, stall; pl_full, pl_empty [WST]
+    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4 + 2 + 2 * WST;
     static constexpr int TOTAL = BARS + 8 * NBARS + 32 + 1024; // + slack to align the base
     static constexpr int W_TX = AE + B;
     static_assert(kDCol + 2 * 64 <= 512, "tensor memory budget");
@@ -202,6 +212,7 @@ __global__ void __maxnreg__(96)
     const uint32_t acc_empty0 = acc_full0 + 16;
     const uint32_t final_bar = acc_full0 + 32;
     const uint32_t stall_bar = acc_full0 + 40;
+    const uint32_t pl_full0 = acc_full0 + 48, pl_empty0 = pl_full0 + 8 * WST;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + L::NBARS);
     volatile int *seg_last = abort_flag + 1;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(abort_flag + 2);
@@ -215,7 +226,9 @@ __global__ void __maxnreg__(96)
     if (threadIdx.x == 0) {
         for (int s = 0; s < WST; ++s) {
             mbar_init(w_full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(w_empty0 + 8 * s, kDecodeWarps);
+            mbar_init(w_empty0 + 8 * s, Q8 ? kDecodeWarps : kDecodeWarps + 1);
+            mbar_init(pl_full0 + 8 * s, 32);
+            mbar_init(pl_empty0 + 8 * s, 32 * kDecodeWarps);
         }
         for (int s = 0; s < XST; ++s) {
             mbar_init(x_full0 + 8 * s, 1);
@@ -405,6 +418,79 @@ __global__ void __maxnreg__(96)
             mbar_wait(final_bar, 0, 1000000000ull);
         }
         __syncwarp();
+    } else if (warp == kWarpE) {
+        // ------------------------------ escape warp ---------------------------
+        // Per unit, every escape entry goes to the list of the decode warp
+        // that owns its slot (row quadrant q = row / 32, column quarter c =
+        // column / 64): 32 entries at a time, one per lane, ranked within the
+        // lanes of the same target so that each list keeps the order of the
+        // tile's list (rows ascending).
+        if (!Q8) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int it = 0; it < n_it; ++it) {
+                bool ok = wait_or_abort(w_full0 + 8 * s, ph, a, abort_flag);
+                if (it >= WST)
+                    ok = wait_or_abort(pl_empty0 + 8 * s, ph ^ 1, a, abort_flag) && ok;
+                ok = __all_sync(0xffffffffu, ok);
+                uint8_t *pl = smem + L::OFF_PL + s * L::PL;
+                uint32_t *cnt_s = reinterpret_cast<uint32_t *>(pl);
+                uint32_t *lists = reinterpret_cast<uint32_t *>(pl + L::PL_LIST);
+                if (lane < kDecodeWarps)
+                    cnt_s[lane] = 0u;
+                __syncwarp();
+                if (ok) {
+                    const uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
+                    const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
+                    const uint32_t cnt = lohi.y - lohi.x;
+                    const bool big = cnt > static_cast<uint32_t>(L::ESC_CAP);
+                    const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
+                    if (lane == 0)
+                        *reinterpret_cast<uint2 *>(pl + L::PL_LO) = lohi;
+                    const uint32_t lt = (1u << lane) - 1u;
+                    for (uint32_t j1 = 0; j1 < cnt; j1 += 128) {
+                        uint32_t e4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
+                            e4[u] = 0u;
+                            if (j < cnt) {
+                                if (big)
+                                    e4[u] = __ldg(a.esc + lohi.x + j);
+                                else
+                                    e4[u] = list_s[j];
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (j1 + 32 * u >= cnt)
+                                break;
+                            const bool valid = j1 + 32 * u + static_cast<uint32_t>(lane) < cnt;
+                            const uint32_t e = e4[u];
+                            const uint32_t w = ((e >> 22) & 3u) * 4u + ((e >> 29) & 3u); // quarter * 4 + quadrant
+                            const uint32_t key = valid ? w : 64u + static_cast<uint32_t>(lane);
+                            const uint32_t peers = __match_any_sync(0xffffffffu, key);
+                            const uint32_t base = valid ? cnt_s[w] : 0u;
+                            const uint32_t pos = base + __popc(peers & lt);
+                            if (valid && pos < static_cast<uint32_t>(kPCap))
+                                lists[w * kPCap + pos] = e;
+                            __syncwarp();
+                            if (valid && (peers & lt) == 0u)
+                                cnt_s[w] = base + __popc(peers);
+                            __syncwarp();
+                        }
+                    }
+                }
+                __syncwarp();
+                mbar_arrive(pl_full0 + 8 * s); // every lane: its writes are visible
+                if (lane == 0)
+                    mbar_arrive(w_empty0 + 8 * s);
+                if (++s == WST) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
     } else {
         // ------------------------------ decode warps --------------------------
         const int q = warp & 3, c = warp >> 2;
@@ -454,38 +540,11 @@ __global__ void __maxnreg__(96)
                 }
             }
 
-            // 2. escape entries of this warp's quadrant (rows 32q..32q+31) in
-            //    its columns: up to 32 are taken into registers (one per lane)
-            //    and the stage is handed back at once; with more the stage is
-            //    kept until they have been applied
-            uint32_t my_e = 0, hits = 0, q_lb = 0, q_ub = 0, esc_lo = 0;
-            bool many = false, big = false;
-            if (!Q8 && ok) {
-                const uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
-                const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
-                const uint32_t cnt = lohi.y - lohi.x;
-                esc_lo = lohi.x;
-                if (cnt) {
-                    const uint16_t *gp = reinterpret_cast<const uint16_t *>(esc_area + L::ESC_GP);
-                    q_lb = min(static_cast<uint32_t>(gp[4 * q]), cnt);
-                    q_ub = (q == 3) ? cnt : min(static_cast<uint32_t>(gp[4 * q + 4]), cnt);
-                    big = cnt > static_cast<uint32_t>(L::ESC_CAP);
-                    const uint32_t n_q = q_ub > q_lb ? q_ub - q_lb : 0u;
-                    if (n_q > 32 || (big && n_q)) {
-                        many = true;
-                    } else if (n_q) {
-                        const uint32_t *list = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
-                        const bool valid = static_cast<uint32_t>(lane) < n_q;
-                        my_e = valid ? list[q_lb + lane] : 0u;
-                        hits = __ballot_sync(0xffffffffu, valid && ((my_e >> 16) & 0xFFu) - kb < 64u);
-                    }
-                }
-            }
-            if (!many) {
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(w_empty0 + 8 * s);
-            }
+            // 2. the stage is no longer needed: hand it back (this warp's
+            //    escapes come from the escape warp's list for it)
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(w_empty0 + 8 * s);
 
             // 3. decode to exact BF16 pairs (escaped slots hold their placeholder)
             uint32_t v[32];
@@ -499,40 +558,50 @@ __global__ void __maxnreg__(96)
                 }
             }
 
-            // 4. escapes of this warp's columns, patched in registers
-            if (hits != 0u || many) {
-                EscPatcher pt{smem + L::OFF_SCR + warp * L::SCR_PITCH, rlo, kb, lane};
-                if (!many) {
-                    pt.apply(my_e, hits, v);
+            // 4. escapes of this warp's rows and columns, patched in registers
+            if (!Q8) {
+                bool okp = wait_or_abort(pl_full0 + 8 * s, ph, a, abort_flag);
+                okp = __all_sync(0xffffffffu, okp) && ok;
+                const uint8_t *pl = smem + L::OFF_PL + s * L::PL;
+                const uint32_t n = okp ? reinterpret_cast<const uint32_t *>(pl)[warp] : 0u;
+                uint32_t my_e = 0u;
+                uint2 lohi = make_uint2(0u, 0u);
+                if (n <= static_cast<uint32_t>(kPCap)) {
+                    if (static_cast<uint32_t>(lane) < n)
+                        my_e = reinterpret_cast<const uint32_t *>(pl + L::PL_LIST)[warp * kPCap + lane];
                 } else {
-                    // more than 32 entries in the quadrant (or in global memory):
-                    // four chunks of 32 fetched at a time
-                    const uint32_t *list_s =
-                        reinterpret_cast<const uint32_t *>(smem + L::OFF_ESC + s * L::ESC + L::ESC_LIST);
-                    for (uint32_t j0 = q_lb; j0 < q_ub; j0 += 128) {
-                        uint32_t e4[4];
+                    lohi = *reinterpret_cast<const uint2 *>(pl + L::PL_LO);
+                }
+                mbar_arrive(pl_empty0 + 8 * s); // every lane, after its own reads
+                if (n != 0u) {
+                    EscPatcher pt{smem + L::OFF_SCR + warp * L::SCR_PITCH, rlo, kb, lane};
+                    if (n <= static_cast<uint32_t>(kPCap)) {
+                        pt.apply(my_e, n >= 32u ? 0xffffffffu : (1u << n) - 1u, v);
+                    } else {
+                        // more than the list holds: this quadrant's entries of the
+                        // tile from global memory, four chunks of 32 at a time
+                        const size_t t = static_cast<size_t>(rb) * a.tiles_c + ks;
+                        const uint32_t cnt = lohi.y - lohi.x;
+                        const uint32_t q_lb = min(static_cast<uint32_t>(__ldg(a.gptr + 16 * t + 4 * q)), cnt);
+                        const uint32_t q_ub =
+                            q == 3 ? cnt : min(static_cast<uint32_t>(__ldg(a.gptr + 16 * t + 4 * q + 4)), cnt);
+                        for (uint32_t j0 = q_lb; j0 < q_ub; j0 += 128) {
+                            uint32_t e4[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint32_t idx = j0 + 32 * u + static_cast<uint32_t>(lane);
-                            e4[u] = 0u;
-                            if (idx < q_ub) {
-                                if (big)
-                                    e4[u] = __ldg(a.esc + esc_lo + idx);
-                                else
-                                    e4[u] = list_s[idx];
+                            for (int u = 0; u < 4; ++u) {
+                                const uint32_t idx = j0 + 32 * u + static_cast<uint32_t>(lane);
+                                e4[u] = idx < q_ub ? __ldg(a.esc + lohi.x + idx) : 0u;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const bool valid = j0 + 32 * u + static_cast<uint32_t>(lane) < q_ub;
+                                pt.apply(e4[u],
+                                         __ballot_sync(0xffffffffu, valid && ((e4[u] >> 16) & 0xFFu) - kb < 64u), v);
                             }
                         }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const bool valid = j0 + 32 * u + static_cast<uint32_t>(lane) < q_ub;
-                            pt.apply(e4[u], __ballot_sync(0xffffffffu, valid && ((e4[u] >> 16) & 0xFFu) - kb < 64u), v);
-                        }
                     }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(w_empty0 + 8 * s);
+                    pt.finish(v);
                 }
-                pt.finish(v);
             }
 
             // 5. into tensor memory, once the MMA is done with this A buffer
