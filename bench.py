@@ -339,6 +339,48 @@ def run_w12(args):
         bm = _step_bytes(layers[0], Mx)
         by_m[str(Mx)] = {"weight_GBps": round(bm / (msm * 1e-3) / 1e9, 1), "us_per_layer": round(1e3 * msm, 2)}
 
+    # Two-level-verification pair on a 17408x5120 matrix: the Q pass over the
+    # 8-bit view at M = 64 (draft-tree nodes), then the exact pass at M = 16, for
+    # the projection draw (the gate projection of the first layer) and for a
+    # heavy-tailed draw (Student-t 1.5, ~1e-2 escapes).
+    tlv = {}
+    hheavy = w12.w12_encode(WL.heavy_weights(17408, 5120, seed=31))
+    wheavy = w12.w12_upload(hheavy)
+    x64 = torch.from_numpy(WL.activations(64, 5120, seed=41).view(np.int16)).cuda().view(torch.bfloat16)
+    x16 = torch.from_numpy(WL.activations(16, 5120, seed=42).view(np.int16)).cuda().view(torch.bfloat16)
+    y64 = torch.empty((64, 17408), dtype=torch.float32, device="cuda")
+    y16 = torch.empty((16, 17408), dtype=torch.float32, device="cuda")
+    for dist_name, dm in (("projection", layers[0][4][1]), ("heavy_tail", wheavy)):
+        def run(kind, dm=dm):
+            if kind in ("q8", "pair"):
+                w12.w12_gemm_ex(x64, dm, y64, stream, q8view=True)
+            if kind in ("exact", "pair"):
+                w12.w12_gemm_ex(x16, dm, y16, stream)
+
+        res = {}
+        for kind in ("q8", "exact", "pair"):
+            for _ in range(3):
+                run(kind)
+            torch.cuda.synchronize()
+            gt = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gt, stream=stream):
+                for _ in range(G):
+                    run(kind)
+            gt.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(short):
+                gt.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res[kind + "_us"] = round(1e3 * e0.elapsed_time(e1) / (short * G), 2)
+        assert w12.w12_dev_status(dm) == 0
+        res["q8_view_GBps"] = round((17408 * 5120 + 2 * 64 * 5120 + 4 * 64 * 17408) / (res["q8_us"] * 1e3), 1)
+        tlv[dist_name] = res
+    tlv["escape_fraction_heavy_tail"] = round(hheavy.stats()["escape_fraction"], 5)
+    del hheavy
+
     # End to end: every step copies its activations from pinned host memory
     # (one transfer: the four activation vectors of the layer, packed), runs
     # the seven GEMMs through the public entry point, and copies the seven
@@ -431,6 +473,7 @@ def run_w12(args):
             },
             "by_M": by_m,
             "us_per_layer_by_launch_mode": modes_us,
+            "two_level_verification_17408x5120": tlv,
             "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
             "roofline": {
                 "bound": "hbm",

@@ -41,7 +41,7 @@ constexpr int kWarpX = kDecodeWarps + 1; // activation producer
 constexpr int kWarpM = kDecodeWarps + 2; // MMA issuer, tensor-memory owner
 constexpr int kWarpE = kDecodeWarps + 3; // escape warp: sorts each unit's escapes per decode warp
 constexpr int kThreads = (kDecodeWarps + 4) * 32;
-constexpr int kPCap = 16;                // escapes per decode warp and unit kept in its list
+constexpr int kPCap = 24;                // escapes per decode warp and unit kept in its list
 constexpr int kNA = 3;                   // A buffers in tensor memory, 128 columns each
 constexpr uint32_t kDCol = kNA * 128;    // two accumulator buffers of 64 columns
 static_assert(kTcKStep == 256 && kTcRows == 128, "one unit = one escape tile");
@@ -58,17 +58,10 @@ struct TcSmem {
     static constexpr int OFF_AE = 0;
     static constexpr int OFF_B = AE;
     static constexpr int WSTAGE = a1024(AE + B);
-    // the unit's escape area, one per weight stage in a ring of its own:
-    // [lo, hi, -, -] u32, the row-group index u16[16], up to ESC_CAP entries
-    // (a tile with more is read from global memory)
-    static constexpr int ESC_CAP = 128;
-    static constexpr int ESC_GP = 16;
-    static constexpr int ESC_LIST = 48;
-    static constexpr int ESC = Q8 ? 0 : ESC_LIST + 4 * ESC_CAP;
-    // the escape warp's per-unit output, one per weight stage: entry count
-    // per decode warp u32[16], the unit's list start and length u32[2], then
-    // up to kPCap entries per decode warp (a larger count means "read the
-    // list yourself")
+    // the escape warp's per-unit output, in a ring as deep as the weights':
+    // entry count per decode warp u32[16], the unit's list start and end
+    // u32[2], then up to kPCap entries per decode warp (a larger count means
+    // "read the list yourself")
     static constexpr int PL_LO = 64;
     static constexpr int PL_LIST = 80;
     static constexpr int PL = Q8 ? 0 : PL_LIST + 4 * kPCap * kDecodeWarps;
@@ -80,11 +73,10 @@ struct TcSmem {
     static constexpr int SCR_PITCH = 144;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * SCR_PITCH;
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + ESC + PL);
+    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + PL);
     static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight slots
     static constexpr int OFF_X = WST * WSTAGE;
-    static constexpr int OFF_ESC = OFF_X + XST * XSTAGE;
-    static constexpr int OFF_SCR = OFF_ESC + WST * ESC;
+    static constexpr int OFF_SCR = OFF_X + XST * XSTAGE;
     static constexpr int OFF_PL = OFF_SCR + SCR;
     static constexpr int BARS = (OFF_PL + WST * PL + 15) & ~15;
     // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
@@ -225,8 +217,8 @@ __global__ void __maxnreg__(96)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < WST; ++s) {
-            mbar_init(w_full0 + 8 * s, Q8 ? 1 : 33);
-            mbar_init(w_empty0 + 8 * s, Q8 ? kDecodeWarps : kDecodeWarps + 1);
+            mbar_init(w_full0 + 8 * s, 1);
+            mbar_init(w_empty0 + 8 * s, kDecodeWarps);
             mbar_init(pl_full0 + 8 * s, 32);
             mbar_init(pl_empty0 + 8 * s, 32 * kDecodeWarps);
         }
@@ -251,7 +243,7 @@ __global__ void __maxnreg__(96)
     // escape-list bounds of the producer's first 64 units, loaded while the
     // CTA sets up
     uint32_t w_lo = 0, w_hi = 0, w_nlo = 0, w_nhi = 0;
-    if (!Q8 && warp == kWarpW) {
+    if (!Q8 && warp == kWarpE) {
         load_tile_window(a, it0, n_it, 0, lane, 128, w_lo, w_hi);
         load_tile_window(a, it0, n_it, 32, lane, 128, w_nlo, w_nhi);
     }
@@ -288,27 +280,6 @@ __global__ void __maxnreg__(96)
                 tma_load_2d(smem_u32(st + L::OFF_AE + L::AE_HALF), &tm_ae, k0 + 128, row0, fb);
                 if (!Q8)
                     tma_load_2d(smem_u32(st + L::OFF_B), &tm_b, k0 / 2, row0, fb);
-            }
-            if (!Q8) {
-                const int t = rb * a.tiles_c + ks;
-                uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
-                if (lane < 2)
-                    cp_async_4(smem_u32(esc_area + 4 * lane), a.tile_ptr + t + lane);
-                else if (lane < 4)
-                    cp_async_16(smem_u32(esc_area + L::ESC_GP + 16 * (lane - 2)),
-                                a.gptr + 16 * static_cast<size_t>(t) + 8 * (lane - 2));
-                if (it > 0 && (it & 31) == 0) { // next window; prefetch the one after
-                    w_lo = w_nlo;
-                    w_hi = w_nhi;
-                    load_tile_window(a, it0, n_it, it + 32, lane, 128, w_nlo, w_nhi);
-                }
-                const uint32_t lo = __shfl_sync(0xffffffffu, w_lo, it & 31);
-                const uint32_t hi = __shfl_sync(0xffffffffu, w_hi, it & 31);
-                const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
-                uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
-                for (uint32_t idx = lane; idx < cnt; idx += 32)
-                    cp_async_4(smem_u32(list + idx), a.esc + lo + idx);
-                cp_async_arrive_noinc(fb);
             }
             issued = it + 1;
             if (++ks == nk) {
@@ -420,71 +391,66 @@ __global__ void __maxnreg__(96)
         __syncwarp();
     } else if (warp == kWarpE) {
         // ------------------------------ escape warp ---------------------------
-        // Per unit, every escape entry goes to the list of the decode warp
-        // that owns its slot (row quadrant q = row / 32, column quarter c =
-        // column / 64): 32 entries at a time, one per lane, ranked within the
-        // lanes of the same target so that each list keeps the order of the
-        // tile's list (rows ascending).
+        // Per unit, every escape entry of the tile (read straight from global
+        // memory, up to 512 in one round of loads) goes to the list of the
+        // decode warp that owns its slot (row quadrant q = row / 32, column
+        // quarter c = column / 64): 32 entries at a time, one per lane, ranked
+        // within the lanes of the same target so that each list keeps the
+        // order of the tile's list (rows ascending).  It needs nothing from the
+        // weight stages and runs up to a ring ahead of the decode warps.
         if (!Q8) {
             int s = 0;
             uint32_t ph = 0;
+            const uint32_t lt = (1u << lane) - 1u;
             for (int it = 0; it < n_it; ++it) {
-                bool ok = wait_or_abort(w_full0 + 8 * s, ph, a, abort_flag);
+                if (it > 0 && (it & 31) == 0) { // next window of tile bounds; prefetch the one after
+                    w_lo = w_nlo;
+                    w_hi = w_nhi;
+                    load_tile_window(a, it0, n_it, it + 32, lane, 128, w_nlo, w_nhi);
+                }
+                const uint32_t lo = __shfl_sync(0xffffffffu, w_lo, it & 31);
+                const uint32_t hi = __shfl_sync(0xffffffffu, w_hi, it & 31);
+                const uint32_t cnt = hi >= lo ? hi - lo : 0u;
+                bool ok = true;
                 if (it >= WST)
-                    ok = wait_or_abort(pl_empty0 + 8 * s, ph ^ 1, a, abort_flag) && ok;
+                    ok = wait_or_abort(pl_empty0 + 8 * s, ph ^ 1, a, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 uint8_t *pl = smem + L::OFF_PL + s * L::PL;
                 uint32_t *cnt_s = reinterpret_cast<uint32_t *>(pl);
                 uint32_t *lists = reinterpret_cast<uint32_t *>(pl + L::PL_LIST);
                 if (lane < kDecodeWarps)
                     cnt_s[lane] = 0u;
+                if (lane == 0)
+                    *reinterpret_cast<uint2 *>(pl + L::PL_LO) = make_uint2(lo, lo + cnt);
                 __syncwarp();
-                if (ok) {
-                    const uint8_t *esc_area = smem + L::OFF_ESC + s * L::ESC;
-                    const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
-                    const uint32_t cnt = lohi.y - lohi.x;
-                    const bool big = cnt > static_cast<uint32_t>(L::ESC_CAP);
-                    const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
-                    if (lane == 0)
-                        *reinterpret_cast<uint2 *>(pl + L::PL_LO) = lohi;
-                    const uint32_t lt = (1u << lane) - 1u;
-                    for (uint32_t j1 = 0; j1 < cnt; j1 += 128) {
-                        uint32_t e4[4];
+                for (uint32_t j1 = 0; ok && j1 < cnt; j1 += 512) {
+                    uint32_t e16[16];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
-                            e4[u] = 0u;
-                            if (j < cnt) {
-                                if (big)
-                                    e4[u] = __ldg(a.esc + lohi.x + j);
-                                else
-                                    e4[u] = list_s[j];
-                            }
-                        }
+                    for (int u = 0; u < 16; ++u) {
+                        const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
+                        e16[u] = j < cnt ? __ldg(a.esc + lo + j) : 0u;
+                    }
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            if (j1 + 32 * u >= cnt)
-                                break;
-                            const bool valid = j1 + 32 * u + static_cast<uint32_t>(lane) < cnt;
-                            const uint32_t e = e4[u];
-                            const uint32_t w = ((e >> 22) & 3u) * 4u + ((e >> 29) & 3u); // quarter * 4 + quadrant
-                            const uint32_t key = valid ? w : 64u + static_cast<uint32_t>(lane);
-                            const uint32_t peers = __match_any_sync(0xffffffffu, key);
-                            const uint32_t base = valid ? cnt_s[w] : 0u;
-                            const uint32_t pos = base + __popc(peers & lt);
-                            if (valid && pos < static_cast<uint32_t>(kPCap))
-                                lists[w * kPCap + pos] = e;
-                            __syncwarp();
-                            if (valid && (peers & lt) == 0u)
-                                cnt_s[w] = base + __popc(peers);
-                            __syncwarp();
-                        }
+                    for (int u = 0; u < 16; ++u) {
+                        if (j1 + 32 * u >= cnt)
+                            break;
+                        const bool valid = j1 + 32 * u + static_cast<uint32_t>(lane) < cnt;
+                        const uint32_t e = e16[u];
+                        const uint32_t w = ((e >> 22) & 3u) * 4u + ((e >> 29) & 3u); // quarter * 4 + quadrant
+                        const uint32_t key = valid ? w : 64u + static_cast<uint32_t>(lane);
+                        const uint32_t peers = __match_any_sync(0xffffffffu, key);
+                        const uint32_t base = valid ? cnt_s[w] : 0u;
+                        const uint32_t pos = base + __popc(peers & lt);
+                        if (valid && pos < static_cast<uint32_t>(kPCap))
+                            lists[w * kPCap + pos] = e;
+                        __syncwarp();
+                        if (valid && (peers & lt) == 0u)
+                            cnt_s[w] = base + __popc(peers);
+                        __syncwarp();
                     }
                 }
                 __syncwarp();
                 mbar_arrive(pl_full0 + 8 * s); // every lane: its writes are visible
-                if (lane == 0)
-                    mbar_arrive(w_empty0 + 8 * s);
                 if (++s == WST) {
                     s = 0;
                     ph ^= 1;
