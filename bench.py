@@ -381,6 +381,44 @@ def run_w12(args):
     tlv["escape_fraction_heavy_tail"] = round(hheavy.stats()["escape_fraction"], 5)
     del hheavy
 
+    # Context, not the target: the same layers as dense BF16 weights through
+    # torch.matmul (cuBLAS), graph-timed the same way (the pages compare the
+    # W12 GEMM with cuBLAS at 1 and 32 rows).
+    dense = None
+    if not args.no_dense:
+        dlayers = [[(name, WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi).view(torch.bfloat16))
+                    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS)] for li in range(len(layers))]
+        dense = {"us_per_layer": {}, "w12_speedup": {}}
+        for Mx, w12_us in ((1, modes_us["layer"]), (32, by_m["32"]["us_per_layer"])):
+            xdn = {g: v for g, v in acts(Mx, 9 if Mx > 1 else 7).items()}
+
+            def stepd(i):
+                for name, Wd in dlayers[i % len(dlayers)]:
+                    torch.matmul(xdn[PROJ_GROUP[name]], Wd.t())
+
+            for i in range(3):
+                stepd(i)
+            torch.cuda.synchronize()
+            gd = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gd, stream=stream):
+                for i in range(G):
+                    stepd(i)
+            gd.replay()
+            torch.cuda.synchronize()
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            d0.record(stream)
+            for _ in range(short):
+                gd.replay()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            us = 1e3 * d0.elapsed_time(d1) / (short * G)
+            dense["us_per_layer"][str(Mx)] = round(us, 2)
+            dense["w12_speedup"][str(Mx)] = round(us / w12_us, 3)
+        dense["weight_bytes_per_layer"] = sum(2 * N * K for _, N, K in WL.LAYER_PROJECTIONS)
+        dense["note"] = "torch.matmul(x, W.t()) with BF16 W of the same seeds, BF16 out, one CUDA graph of G steps"
+        del dlayers
+        torch.cuda.empty_cache()
+
     # End to end: every step copies its activations from pinned host memory
     # (one transfer: the four activation vectors of the layer, packed), runs
     # the seven GEMMs through the public entry point, and copies the seven
@@ -474,6 +512,7 @@ def run_w12(args):
             "by_M": by_m,
             "us_per_layer_by_launch_mode": modes_us,
             "two_level_verification_17408x5120": tlv,
+            "dense_bf16_cublas": dense,
             "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
             "roofline": {
                 "bound": "hbm",
@@ -635,6 +674,7 @@ def main():
     ap.add_argument("--graph-steps", type=int, default=12)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense BF16 (cuBLAS) comparison")
     ap.add_argument("--case", default=None, help="profiling case: fma, fma2, fma4, tc16, tc32, tc, q8, q8m1")
     args = ap.parse_args()
     if args.warmup < 3:
