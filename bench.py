@@ -419,6 +419,25 @@ def run_w12(args):
         del dlayers
         torch.cuda.empty_cache()
 
+    # Conversion speed: one 17408x5120 BF16 matrix (178 MB) to W12, on the
+    # device (weights already there) and with the host encoder (all cores).
+    wconv = WL.projection_weights_torch(17408, 5120, seed=77)
+    t_dev = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        tc0 = time.perf_counter()
+        dconv = w12.w12_encode_device(wconv, stream)
+        t_dev.append(time.perf_counter() - tc0)
+        dconv.free()
+    whost = wconv.cpu().numpy().view(np.uint16)
+    tc0 = time.perf_counter()
+    hconv = w12.w12_encode(whost)
+    t_host = time.perf_counter() - tc0
+    del hconv, whost, wconv
+    convert = {"device_ms": round(1e3 * min(t_dev), 2), "host_ms": round(1e3 * t_host, 1),
+               "device_GBps_bf16_in": round(2 * 17408 * 5120 / min(t_dev) / 1e9, 1),
+               "host_cores": len(os.sched_getaffinity(0))}
+
     # End to end: every step copies its activations from pinned host memory
     # (one transfer: the four activation vectors of the layer, packed), runs
     # the seven GEMMs through the public entry point, and copies the seven
@@ -513,6 +532,7 @@ def run_w12(args):
             "us_per_layer_by_launch_mode": modes_us,
             "two_level_verification_17408x5120": tlv,
             "dense_bf16_cublas": dense,
+            "encode_17408x5120": convert,
             "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
             "roofline": {
                 "bound": "hbm",

@@ -130,6 +130,24 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out);
 /* Free a device handle (synchronises with the device first). */
 void w12_dev_free(w12_dev *d);
 
+/*
+ * Encode on the device: BF16 weights w_bf16 (device memory, [N][K] row-major,
+ * caller-owned) become a device handle whose arrays are byte-identical to
+ * w12_upload(w12_encode(...)) of the same weights [F5a] -- conversion of a
+ * checkpoint already on the GPU without a round trip through the host.  Runs
+ * on `stream` and synchronises with it (the handle's size depends on the
+ * number of escapes).  N = 0 or K = 0 gives an empty handle.  Errors:
+ * INVALID_ARG, UNSUPPORTED (N or K above 2^31), OOM, CUDA.
+ */
+w12_status w12_encode_device(const void *w_bf16, int64_t N, int64_t K, w12_stream_t stream, w12_dev **out);
+
+/*
+ * Copy a device handle's arrays back into a new host handle (for
+ * w12_serialize / w12_save of a matrix encoded on the device).  Synchronises
+ * with `stream`.  Errors: INVALID_ARG, OOM, CUDA.
+ */
+w12_status w12_download(const w12_dev *d, w12_stream_t stream, w12_host **out);
+
 /* Shape and device-byte count of a device handle. */
 w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device_bytes);
 

@@ -76,6 +76,8 @@ _sig("w12_save", [_P, ctypes.c_char_p])
 _sig("w12_load", [ctypes.c_char_p, ctypes.POINTER(_P)])
 _sig("w12_upload", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_free", [_P], None)
+_sig("w12_encode_device", [_P, _I64, _I64, _P, ctypes.POINTER(_P)])
+_sig("w12_download", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
@@ -95,6 +97,7 @@ EXPORTED = (
     "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
+    "w12_encode_device", "w12_download",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -258,6 +261,27 @@ def w12_upload(h: Host, stream=None) -> Dev:
     out = _P()
     _check(_lib.w12_upload(h.ptr, _stream_ptr(stream), ctypes.byref(out)), "w12_upload")
     return Dev(out.value, h.N, h.K, host=h)
+
+
+def w12_encode_device(w, stream=None) -> Dev:
+    """Encode a CUDA tensor of BF16 weights [N][K] (bfloat16 or its int16 /
+    uint16 bit view) on the device; the arrays equal w12_upload(w12_encode(w))."""
+    import torch
+    if not (isinstance(w, torch.Tensor) and w.is_cuda and w.dim() == 2 and w.is_contiguous() and w.element_size() == 2
+            and w.dtype in (torch.bfloat16, torch.int16, torch.uint16)):
+        raise TypeError("w must be a contiguous CUDA [N][K] tensor of BF16 (or its 16-bit pattern)")
+    N, K = w.shape
+    out = _P()
+    _check(_lib.w12_encode_device(ctypes.c_void_p(w.data_ptr()), N, K, _stream_ptr(stream), ctypes.byref(out)),
+           "w12_encode_device")
+    return Dev(out.value, N, K)
+
+
+def w12_download(d: Dev, stream=None) -> Host:
+    """The device handle's arrays copied into a new host handle."""
+    out = _P()
+    _check(_lib.w12_download(d.ptr, _stream_ptr(stream), ctypes.byref(out)), "w12_download")
+    return Host(out.value, d.N, d.K)
 
 
 def _gemm(fn, name, x, d: Dev, y=None, stream=None):

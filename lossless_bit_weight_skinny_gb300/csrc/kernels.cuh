@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "w12.h"
 
 namespace w12 {
 
@@ -269,6 +270,16 @@ inline int choose_grid(int64_t n_rowblk, int64_t n_kstep, int sms, int64_t min_i
     }
     return static_cast<int>(best);
 }
+
+} // namespace w12
+
+struct w12_dev;
+
+namespace w12 {
+
+// A device handle for an N x K matrix with room for n_esc escapes (runtime.cu):
+// one allocation, status word cleared on `st`, GEMM tensor maps built.
+w12_status dev_create(int64_t N, int64_t K, int64_t n_esc, cudaStream_t st, w12_dev **out);
 
 cudaError_t launch_decode(const uint8_t *ebase, const uint8_t *ae, const uint8_t *b,
                           const uint32_t *tile_ptr, const uint32_t *esc, uint16_t *out, int64_t N,

@@ -221,14 +221,15 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
 
 } // namespace
 
-extern "C" {
+namespace w12 {
 
-w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
+// A device handle for an N x K matrix with n_esc escapes: one allocation
+// holding every array (256-byte aligned), the status word cleared on
+// `stream`, and the TMA descriptors of both GEMM kernels when K allows them
+// (rows of both planes must start on 16-byte boundaries: K % 32 == 0).
+w12_status dev_create(int64_t N, int64_t K, int64_t n_esc, cudaStream_t st, w12_dev **out)
 {
-    if (!h || !out)
-        return W12_ERR_INVALID_ARG;
     *out = nullptr;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     w12_dev *d = new (std::nothrow) w12_dev;
     if (!d)
         return W12_ERR_OOM;
@@ -236,36 +237,17 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
         delete d;
         return W12_ERR_CUDA;
     }
-    d->N = h->N;
-    d->K = h->K;
-    d->T = num_tiles(h->N, h->K);
-    d->n_esc = static_cast<int64_t>(h->esc.size());
-    d->brow = b_row_bytes(h->K);
-    d->tiles_c = ceil_div(h->K, kTileCols);
+    d->N = N;
+    d->K = K;
+    d->T = num_tiles(N, K);
+    d->n_esc = n_esc;
+    d->brow = b_row_bytes(K);
+    d->tiles_c = ceil_div(K, kTileCols);
     auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
-    const size_t s_status = 256, s_ebase = up(h->ebase.size()), s_ae = up(h->ae.size()),
-                 s_b = up(h->b.size()), s_ptr = up(4 * h->tile_ptr.size()), s_esc = up(4 * h->esc.size()),
-                 s_gp = up(32 * static_cast<size_t>(d->T));
+    const size_t s_status = 256, s_ebase = up(static_cast<size_t>(N)), s_ae = up(static_cast<size_t>(N * K)),
+                 s_b = up(static_cast<size_t>(N * d->brow)), s_ptr = up(4 * static_cast<size_t>(d->T + 1)),
+                 s_esc = up(4 * static_cast<size_t>(n_esc)), s_gp = up(32 * static_cast<size_t>(d->T));
     d->bytes = s_status + s_ebase + s_ae + s_b + s_ptr + s_esc + s_gp;
-    // row-group index of every escape tile: gp[t][g] = entries of tile t whose
-    // row (within the tile) is below 8g, so the entries of rows [8g, 8g+8) are
-    // [gp[t][g], gp[t][g+1]) (gp[t][16] being the tile's count)
-    std::vector<uint16_t> gp;
-    try {
-        gp.assign(16 * static_cast<size_t>(d->T), 0);
-    } catch (...) {
-        delete d;
-        return W12_ERR_OOM;
-    }
-    for (int64_t t = 0; t < d->T; ++t) {
-        const uint32_t lo = h->tile_ptr[t], hi = h->tile_ptr[t + 1];
-        uint32_t i = lo;
-        for (int g = 0; g < 16; ++g) {
-            while (i < hi && (h->esc[i] >> 24) < static_cast<uint32_t>(8 * g))
-                ++i;
-            gp[16 * t + g] = static_cast<uint16_t>(i - lo);
-        }
-    }
     if (cudaMalloc(&d->base, d->bytes) != cudaSuccess) {
         cudaGetLastError();
         delete d;
@@ -285,7 +267,60 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
     d->esc = reinterpret_cast<uint32_t *>(p);
     p += s_esc;
     d->gptr = reinterpret_cast<uint16_t *>(p);
-    bool ok = cudaMemsetAsync(d->status, 0, 256, st) == cudaSuccess;
+    if (cudaMemsetAsync(d->status, 0, 256, st) != cudaSuccess) {
+        cudaFree(d->base);
+        delete d;
+        return W12_ERR_CUDA;
+    }
+    if (N > 0 && K >= 32 && K % 32 == 0) {
+        const uint64_t n = N, k = K;
+        const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        bool t = make_tmap(tmap_of(d->tm_ae_fma128), U8, 1, d->ae, k, n, 256, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_ae_fma64), U8, 1, d->ae, k, n, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_b_fma128), U8, 1, d->b, k / 2, n, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_b_fma64), U8, 1, d->b, k / 2, n, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+        t = t && make_tmap(tmap_of(d->tm_ae_tc), U8, 1, d->ae, k, n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        t = t && make_tmap(tmap_of(d->tm_b_tc), U8, 1, d->b, k / 2, n, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+        d->gemm_ok = t;
+    }
+    *out = d;
+    return W12_OK;
+}
+
+} // namespace w12
+
+extern "C" {
+
+w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
+{
+    if (!h || !out)
+        return W12_ERR_INVALID_ARG;
+    *out = nullptr;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    w12_dev *d = nullptr;
+    w12_status s = w12::dev_create(h->N, h->K, static_cast<int64_t>(h->esc.size()), st, &d);
+    if (s != W12_OK)
+        return s;
+    // row-group index of every escape tile: gp[t][g] = entries of tile t whose
+    // row (within the tile) is below 8g, so the entries of rows [8g, 8g+8) are
+    // [gp[t][g], gp[t][g+1]) (gp[t][16] being the tile's count)
+    std::vector<uint16_t> gp;
+    try {
+        gp.assign(16 * static_cast<size_t>(d->T), 0);
+    } catch (...) {
+        w12_dev_free(d);
+        return W12_ERR_OOM;
+    }
+    for (int64_t t = 0; t < d->T; ++t) {
+        const uint32_t lo = h->tile_ptr[t], hi = h->tile_ptr[t + 1];
+        uint32_t i = lo;
+        for (int g = 0; g < 16; ++g) {
+            while (i < hi && (h->esc[i] >> 24) < static_cast<uint32_t>(8 * g))
+                ++i;
+            gp[16 * t + g] = static_cast<uint16_t>(i - lo);
+        }
+    }
+    bool ok = true;
     auto cp = [&](void *dst, const void *src, size_t n) {
         if (n)
             ok = ok && cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
@@ -299,21 +334,8 @@ w12_status w12_upload(const w12_host *h, w12_stream_t stream, w12_dev **out)
     if (ok && !gp.empty())
         ok = cudaStreamSynchronize(st) == cudaSuccess; // gp is a local staging buffer
     if (!ok) {
-        cudaFree(d->base);
-        delete d;
+        w12_dev_free(d);
         return W12_ERR_CUDA;
-    }
-    // GEMM descriptors: rows of both planes must start on 16-byte boundaries
-    if (h->N > 0 && h->K >= 32 && h->K % 32 == 0) {
-        const uint64_t N = h->N, K = h->K;
-        const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-        bool t = make_tmap(tmap_of(d->tm_ae_fma128), U8, 1, d->ae, K, N, 256, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-        t = t && make_tmap(tmap_of(d->tm_ae_fma64), U8, 1, d->ae, K, N, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
-        t = t && make_tmap(tmap_of(d->tm_b_fma128), U8, 1, d->b, K / 2, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
-        t = t && make_tmap(tmap_of(d->tm_b_fma64), U8, 1, d->b, K / 2, N, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
-        t = t && make_tmap(tmap_of(d->tm_ae_tc), U8, 1, d->ae, K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        t = t && make_tmap(tmap_of(d->tm_b_tc), U8, 1, d->b, K / 2, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        d->gemm_ok = t;
     }
     *out = d;
     return W12_OK;
