@@ -30,7 +30,6 @@ struct GemmArgs {
     int n_rowblk;                  // row blocks
     int n_kstep;                   // k steps per row block
     int total_iters;               // n_rowblk * n_kstep
-    uint32_t epoch;                // call counter (diagnostic only)
     uint64_t limit_ns;             // bounded-wait limit
     int inject_stall;              // test hook: wait on a barrier nobody arrives on
     int x_ready;                   // x was complete before the previous launch: load it at once

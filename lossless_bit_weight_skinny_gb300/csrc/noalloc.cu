@@ -23,7 +23,6 @@
 //   * the first call on each device looks up the array's device address and
 //     clears its counters, then synchronises the device; make that first call
 //     before any stream capture.
-#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -49,7 +48,6 @@ namespace {
 
 std::mutex g_na_mu;
 void *g_na_ptr[64] = {nullptr}; // device address of the scratch, per device
-std::atomic<uint32_t> g_na_epoch{0};
 
 // Once per device, with that device current: fetch the array's device address
 // and clear the counters.
@@ -174,10 +172,6 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
         return s;
     a.counters = reinterpret_cast<unsigned long long *>(scratch);
     a.partials = reinterpret_cast<float *>(scratch + kNoAllocCounterBytes);
-    uint32_t ep = g_na_epoch.fetch_add(1) + 1;
-    if (ep == 0)
-        ep = g_na_epoch.fetch_add(1) + 1;
-    a.epoch = ep;
 
     CUtensorMap tmx;
     const bool okx = tc ? x_tmap(&tmx, x_bf16, M, K, 64, mt, CU_TENSOR_MAP_SWIZZLE_128B)

@@ -89,7 +89,6 @@ int sm_count(int dev)
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
-    uint32_t epoch = 0;
 };
 
 std::mutex g_ws_mu;
@@ -98,9 +97,9 @@ std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 constexpr size_t kCounterBytes = 1 << 16; // room for 8192 row blocks
 
 // Returns partial-sum and counter pointers for a call that needs `part_bytes`
-// of partial sums, and this call's epoch.
+// of partial sums.
 w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **partials,
-                         unsigned long long **counters, uint32_t *epoch)
+                         unsigned long long **counters)
 {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace &w = g_ws[{dev, st}];
@@ -127,9 +126,6 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
     }
     *counters = static_cast<unsigned long long *>(w.ptr);
     *partials = reinterpret_cast<float *>(static_cast<char *>(w.ptr) + kCounterBytes);
-    if (++w.epoch == 0)
-        w.epoch = 1;
-    *epoch = w.epoch;
     return W12_OK;
 }
 
@@ -196,7 +192,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur) * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
-    w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters, &a.epoch);
+    w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters);
     if (ws != W12_OK)
         return ws;
 
