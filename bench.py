@@ -381,6 +381,54 @@ def run_w12(args):
     tlv["escape_fraction_heavy_tail"] = round(hheavy.stats()["escape_fraction"], 5)
     del hheavy
 
+    # Fused projections (the same bytes, merged at encode time): q/k/v stacked
+    # into one 7168x5120 matrix and gate/up into one 34816x5120 matrix (every
+    # W12 row carries its own window, and the escape tiles are 128 rows high,
+    # so stacking rows is just a bigger matrix); one step = qkv, o, gate_up,
+    # down, each waiting for the kernel before it, as in a decode step.
+    def fused_layer(li):
+        out = []
+        for gname, parts in (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))):
+            ws = [WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi)
+                  for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS) if name in parts]
+            wcat = torch.cat(ws, 0) if len(ws) > 1 else ws[0]
+            out.append((gname, w12.w12_encode_device(wcat, stream)))
+            del ws, wcat
+        return out
+
+    flayers = [fused_layer(li) for li in range(len(layers))]
+    fx = {"qkv": xs["qkv"], "o": xs["o"], "gate_up": xs["gate_up"], "down": xs["down"]}
+    fy = {g: torch.empty((M, d.N), dtype=torch.float32, device="cuda") for g, d in flayers[0]}
+
+    def stepf(i):
+        for g, d in flayers[i % len(flayers)]:
+            w12.w12_gemm_ex(fx[g], d, fy[g], stream)
+
+    for i in range(3):
+        stepf(i)
+    torch.cuda.synchronize()
+    gf = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf, stream=stream):
+        for i in range(G):
+            stepf(i)
+    gf.replay()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(short):
+        gf.replay()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    f_us = 1e3 * f0.elapsed_time(f1) / (short * G)
+    fused = {"us_per_layer": round(f_us, 2), "weight_GBps": round(step_bytes / (f_us * 1e3), 1),
+             "step": "4 GEMMs: qkv 7168x5120, o 5120x5120, gate_up 34816x5120, down 5120x17408 "
+                     "(the layer's weights merged by rows at encode time, encoded on the device)"}
+    for fl in flayers:
+        for _, d in fl:
+            assert w12.w12_dev_status(d) == 0
+            d.free()
+    del flayers
+
     # Context, not the target: the same layers as dense BF16 weights through
     # torch.matmul (cuBLAS), graph-timed the same way (the pages compare the
     # W12 GEMM with cuBLAS at 1 and 32 rows).
@@ -533,6 +581,7 @@ def run_w12(args):
             "two_level_verification_17408x5120": tlv,
             "dense_bf16_cublas": dense,
             "encode_17408x5120": convert,
+            "fused_projections_m1": fused,
             "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
             "roofline": {
                 "bound": "hbm",
