@@ -163,6 +163,27 @@ def _step_bytes(layer, M):
     return tot
 
 
+def replica_aggregate(ms, rank_bytes, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: every rank streamed
+    `rank_bytes` in its own `ms` of timed region; the job's time is the slowest
+    rank's (max over ranks), its bytes the sum over ranks.  Returns
+    (max ms, GB/s of the whole job)."""
+    import torch
+
+    world = 1
+    if dist is not None:
+        world = dist.get_world_size()
+        t = torch.tensor([float(ms), float(rank_bytes)], dtype=torch.float64, device=device)
+        tm = t[:1].clone()
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        tb = t[1:].clone()
+        dist.all_reduce(tb, op=dist.ReduceOp.SUM)
+        ms, total = float(tm.item()), float(tb.item())
+    else:
+        total = float(rank_bytes)
+    return ms, total / (ms * 1e-3) / 1e9
+
+
 def run_w12(args):
     import torch
 
@@ -258,17 +279,12 @@ def run_w12(args):
             torch.cuda.synchronize()
     clocks = sampler.stop()
     args.steps = reps * G
-    ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    step_bytes = _step_bytes(layers[0], M)
+    ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * args.steps, dist, "cuda")
     for layer in layers:
         for _, d, _ in layer:
             assert w12.w12_dev_status(d) == 0, "device status after timing"
 
-    step_bytes = _step_bytes(layers[0], M)
-    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
     # per-launch durations of the dominant kernel (the M = 1 CUDA-core GEMM),
     # from the event pairs of the measurement replay
     kern_ms = 0.0

@@ -18,6 +18,8 @@ from .oracle import (  # noqa: F401
     row_ebase,
     num_tiles,
     b_row_bytes,
+    round_bf16,
+    silu_mul,
     TILE_ROWS,
     TILE_COLS,
 )

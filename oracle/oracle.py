@@ -38,7 +38,7 @@ def build(src: str = _SRC, build_dir: str = _BUILD, name: str = _LIB_NAME,
     if (not os.path.exists(out)) or os.path.getmtime(out) < os.path.getmtime(src):
         tmp = out + f".tmp{os.getpid()}"
         cmd = ["gcc", "-std=c99", "-O2", "-fno-fast-math", "-ffp-contract=off",
-               "-shared", "-fPIC", *extra_flags, src, "-o", tmp]
+               "-shared", "-fPIC", *extra_flags, src, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, out)
     return out
@@ -73,6 +73,10 @@ def _declare(lib):
     lib.orc_num_tiles.restype = _I64
     lib.orc_b_row_bytes.argtypes = [_I64]
     lib.orc_b_row_bytes.restype = _I64
+    lib.orc_round_bf16.argtypes = [_P, _I64, _P]
+    lib.orc_round_bf16.restype = None
+    lib.orc_silu_mul.argtypes = [_P, _I64, _I64, _P]
+    lib.orc_silu_mul.restype = None
     return lib
 
 
@@ -200,3 +204,24 @@ def num_tiles(N: int, K: int, lib=None) -> int:
 
 def b_row_bytes(K: int, lib=None) -> int:
     return int((lib or _get()).orc_b_row_bytes(K))
+
+
+def round_bf16(v, lib=None) -> np.ndarray:
+    """FP32 values -> BF16 bit patterns, round to nearest, ties to even."""
+    lib = lib or _get()
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    out = np.zeros(a.shape, dtype=np.uint16)
+    lib.orc_round_bf16(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def silu_mul(y, lib=None) -> np.ndarray:
+    """h[M][N/2] = silu(y[:, 0::2]) * y[:, 1::2] in float64 (gate/up rows interleaved)."""
+    lib = lib or _get()
+    a = np.ascontiguousarray(np.asarray(y, dtype=np.float64))
+    M, N = a.shape
+    if N % 2:
+        raise ValueError("silu_mul needs an even number of columns")
+    h = np.zeros((M, N // 2), dtype=np.float64)
+    lib.orc_silu_mul(_ptr(a), M, N, _ptr(h))
+    return h

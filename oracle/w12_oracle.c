@@ -42,7 +42,18 @@
  *      patch (zero-copy reading of the A+E byte, [KC3], [F7]);
  *   R10 GEMM reference: y[m][n] = sum_k x[m][k] * W[n][k] in double precision,
  *      summed in increasing k.
+ *
+ * Epilogues of the projections of a decode step (the pages time the
+ * projections of a dense layer -- q, k, v, o, gate, up, down -- and leave the
+ * work beside each GEMM open; these are the plainest readings):
+ *   R11 BF16 output: an FP32 result rounded to the nearest BF16, ties to the
+ *      even significand, values at or beyond the largest finite BF16 plus half
+ *      an ulp to infinity (IEEE 754 round-to-nearest-even);
+ *   R12 gated MLP: with the gate and up rows interleaved (row 2i = gate row i,
+ *      row 2i+1 = up row i), h[m][i] = silu(y[m][2i]) * y[m][2i+1], where
+ *      silu(g) = g / (1 + exp(-g)).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -419,6 +430,63 @@ void orc_abs_gemm(const uint16_t *x, const uint16_t *w, int64_t M, int64_t N, in
                 acc += p < 0 ? -p : p;
             }
             s[m * N + n] = acc;
+        }
+    }
+}
+
+/* ---- epilogues (R11, R12) ----------------------------------------------- */
+
+static double f32_bits_value(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * R11: the BF16 nearest to v.  The two candidates are v's bit pattern cut to
+ * 16 bits (toward zero) and the next BF16 away from zero; whichever is nearer
+ * wins, and a tie goes to the one whose last significand bit is 0.  Past the
+ * largest finite BF16 the next value away from zero is infinity, which counts
+ * as 2^128 in the comparison (the unbounded-exponent rounding of IEEE 754).
+ * A NaN gives a quiet NaN of the same sign.
+ */
+static uint16_t round_bf16_one(float v)
+{
+    uint32_t u, lo, hi;
+    double a, dlo, dhi;
+    memcpy(&u, &v, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    lo = u & 0xFFFF0000u;
+    if (lo == u)
+        return (uint16_t)(u >> 16);
+    hi = lo + 0x10000u;
+    a = fabs((double)v);
+    dlo = a - fabs(f32_bits_value(lo));
+    dhi = ((hi & 0x7F800000u) == 0x7F800000u ? ldexp(1.0, 128) : fabs(f32_bits_value(hi))) - a;
+    if (dlo < dhi)
+        return (uint16_t)(lo >> 16);
+    if (dhi < dlo)
+        return (uint16_t)(hi >> 16);
+    return (uint16_t)(((lo >> 16) & 1u) ? (hi >> 16) : (lo >> 16));
+}
+
+void orc_round_bf16(const float *v, int64_t n, uint16_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        out[i] = round_bf16_one(v[i]);
+}
+
+/* R12: h[m][i] = silu(y[m][2i]) * y[m][2i+1] for y [M][N], N even; h [M][N/2]. */
+void orc_silu_mul(const double *y, int64_t M, int64_t N, double *h)
+{
+    int64_t m, i;
+    for (m = 0; m < M; m++) {
+        for (i = 0; i < N / 2; i++) {
+            double g = y[m * N + 2 * i], u = y[m * N + 2 * i + 1];
+            h[m * (N / 2) + i] = g / (1.0 + exp(-g)) * u;
         }
     }
 }

@@ -265,6 +265,64 @@ def pin_gemm_exact_integers(lib=None):
         assert y[1, n] == float(sum(-v[k] if k % 2 == 0 else v[k] for k in range(K)))
 
 
+# ---- epilogues: BF16 output and the gated-MLP product ----------------------------
+
+def _f32(bits):
+    return np.asarray(bits, dtype=np.uint32).view(np.float32)
+
+
+def pin_round_bf16(lib=None):
+    """Round to nearest, ties to even: worked bit patterns (ties both ways,
+    sign, overflow, subnormals, infinities) and agreement with PyTorch's CPU
+    float32 -> bfloat16 conversion on random bit patterns."""
+    table = [
+        (0x3F800000, 0x3F80),  # exact
+        (0x3F808000, 0x3F80),  # 1 + 2^-8: tie, even stays
+        (0x3F818000, 0x3F82),  # 1 + 3*2^-8: tie, odd rounds up
+        (0x3F808001, 0x3F81),  # just above the tie
+        (0x3F807FFF, 0x3F80),  # just below the tie
+        (0xBF808001, 0xBF81),  # sign kept, magnitude rounded
+        (0xBF818000, 0xBF82),
+        (0x7F7F7FFF, 0x7F7F),  # largest finite BF16 stays
+        (0x7F7F8000, 0x7F80),  # its tie with 2^128 goes to infinity (even)
+        (0xFF7FFFFF, 0xFF80),  # largest finite FP32 overflows
+        (0x00008000, 0x0000),  # subnormal tie, even
+        (0x00018000, 0x0002),  # subnormal tie, odd rounds up
+        (0x80000001, 0x8000),
+        (0x7F800000, 0x7F80),
+        (0xFF800000, 0xFF80),
+    ]
+    got = O.round_bf16(_f32([t[0] for t in table]), lib=lib)
+    for (i, o), g in zip(table, got):
+        assert int(g) == o, (hex(i), hex(int(g)), hex(o))
+    nan = O.round_bf16(_f32([0x7FC00001, 0xFF800001]), lib=lib)
+    assert all((int(v) & 0x7F80) == 0x7F80 and (int(v) & 0x7F) for v in nan)
+    import torch
+
+    rng = np.random.Generator(np.random.PCG64(91))
+    bits = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]
+    want = torch.from_numpy(_f32(bits).copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.round_bf16(_f32(bits), lib=lib), want)
+
+
+def pin_silu_mul(lib=None):
+    """h = silu(gate) * up with gate/up interleaved by row: worked values, the
+    identity silu(g) - silu(-g) = g, and the large-|g| limits."""
+    e = np.exp(1.0)
+    y = np.array([[0.0, 5.0, 1.0, 2.0, -1.0, 3.0, 2.0, -0.5]])
+    want = [0.0, 2.0 * (1.0 / (1.0 + 1.0 / e)), 3.0 * (-1.0 / (1.0 + e)), -0.5 * (2.0 / (1.0 + np.exp(-2.0)))]
+    h = O.silu_mul(y, lib=lib)
+    assert h.shape == (1, 4)
+    assert np.allclose(h[0], want, rtol=1e-15, atol=0)
+    g = np.random.Generator(np.random.PCG64(92)).normal(0, 3, size=1000)
+    pos = O.silu_mul(np.stack([g, np.ones_like(g)], 1).reshape(1, -1), lib=lib)[0]
+    neg = O.silu_mul(np.stack([-g, np.ones_like(g)], 1).reshape(1, -1), lib=lib)[0]
+    assert np.allclose(pos - neg, g, rtol=1e-13, atol=1e-13)
+    big = O.silu_mul(np.array([[60.0, 1.0, -60.0, 1.0, -800.0, 1.0]]), lib=lib)[0]
+    assert big[0] == 60.0 and -1e-24 < big[1] < 0 and big[2] == 0.0
+
+
 # ---- the printed figures -------------------------------------------------------
 
 def printed_figures():
@@ -347,4 +405,6 @@ FAST_PINS = (
     pin_gemm_numpy,
     pin_gemm_one_hot,
     pin_gemm_exact_integers,
+    pin_round_bf16,
+    pin_silu_mul,
 )

@@ -42,6 +42,15 @@ MUTANTS = [
     ("gemm_float_accumulator", "            double acc = 0.0;\n            for (k = 0; k < K; k++)\n                acc +=",
      "            float acc = 0.0f;\n            for (k = 0; k < K; k++)\n                acc +="),
     ("abs_gemm_signed", "acc += p < 0 ? -p : p;", "acc += p;"),
+    ("round_ties_away", "return (uint16_t)(((lo >> 16) & 1u) ? (hi >> 16) : (lo >> 16));",
+     "return (uint16_t)(hi >> 16);"),
+    ("round_truncates", "    if (dlo < dhi)\n        return (uint16_t)(lo >> 16);",
+     "    if (1)\n        return (uint16_t)(lo >> 16);"),
+    ("round_never_overflows", "ldexp(1.0, 128)", "HUGE_VAL"),
+    ("silu_operands_swapped", "h[m * (N / 2) + i] = g / (1.0 + exp(-g)) * u;",
+     "h[m * (N / 2) + i] = u / (1.0 + exp(-u)) * g;"),
+    ("silu_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
+    ("silu_pairs_shifted", "u = y[m * N + 2 * i + 1];", "u = y[m * N + (2 * i + 3) % N];"),
 ]
 
 
