@@ -398,27 +398,34 @@ def run_w12(args):
     del hheavy
 
     # Fused projections (the same bytes, merged at encode time): q/k/v stacked
-    # into one 7168x5120 matrix and gate/up into one 34816x5120 matrix (every
-    # W12 row carries its own window, and the escape tiles are 128 rows high,
-    # so stacking rows is just a bigger matrix); one step = qkv, o, gate_up,
-    # down, each waiting for the kernel before it, as in a decode step.
+    # into one 7168x5120 matrix and gate/up interleaved by rows into one
+    # 34816x5120 matrix (every W12 row carries its own window, and the escape
+    # tiles are 128 rows high, so merging rows is just a bigger matrix).  One
+    # step = qkv (BF16 out), o (BF16 out), gate_up with the SiLU*mul epilogue
+    # writing BF16 h[M][17408], and down reading h: each launch waits for the
+    # kernel before it, and down consumes gate_up's output, as in a decode step.
     def fused_layer(li):
         out = []
         for gname, parts in (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))):
             ws = [WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi)
                   for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS) if name in parts]
-            wcat = torch.cat(ws, 0) if len(ws) > 1 else ws[0]
+            if gname == "gate_up":  # row 2i = gate row i, row 2i+1 = up row i
+                wcat = torch.stack(ws, 1).reshape(-1, ws[0].shape[1])
+            else:
+                wcat = torch.cat(ws, 0) if len(ws) > 1 else ws[0]
             out.append((gname, w12.w12_encode_device(wcat, stream)))
             del ws, wcat
         return out
 
     flayers = [fused_layer(li) for li in range(len(layers))]
-    fx = {"qkv": xs["qkv"], "o": xs["o"], "gate_up": xs["gate_up"], "down": xs["down"]}
-    fy = {g: torch.empty((M, d.N), dtype=torch.float32, device="cuda") for g, d in flayers[0]}
+    f_out = {"qkv": (7168, torch.bfloat16), "o": (5120, torch.bfloat16), "gate_up": (17408, torch.bfloat16),
+             "down": (5120, torch.float32)}
+    fy = {g: torch.empty((M, n), dtype=dt, device="cuda") for g, (n, dt) in f_out.items()}
+    fx = {"qkv": xs["qkv"], "o": xs["o"], "gate_up": xs["gate_up"], "down": fy["gate_up"]}
 
     def stepf(i):
         for g, d in flayers[i % len(flayers)]:
-            w12.w12_gemm_ex(fx[g], d, fy[g], stream)
+            w12.w12_gemm_ex(fx[g], d, fy[g], stream, out_bf16=(g != "down"), silu_mul=(g == "gate_up"))
 
     for i in range(3):
         stepf(i)
@@ -437,8 +444,10 @@ def run_w12(args):
     torch.cuda.synchronize()
     f_us = 1e3 * f0.elapsed_time(f1) / (short * G)
     fused = {"us_per_layer": round(f_us, 2), "weight_GBps": round(step_bytes / (f_us * 1e3), 1),
-             "step": "4 GEMMs: qkv 7168x5120, o 5120x5120, gate_up 34816x5120, down 5120x17408 "
-                     "(the layer's weights merged by rows at encode time, encoded on the device)"}
+             "step": "4 GEMMs: qkv 7168x5120 (BF16 out), o 5120x5120 (BF16 out), gate_up 34816x5120 "
+                     "(gate/up rows interleaved; SiLU*mul epilogue, BF16 h[1][17408] out), down "
+                     "5120x17408 reading h (FP32 out); merged at encode time, encoded on the device; "
+                     "GB/s counts the unfused layer's bytes"}
     for fl in flayers:
         for _, d in fl:
             assert w12.w12_dev_status(d) == 0

@@ -178,12 +178,28 @@ w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M
 /* Flags of w12_gemm_ex. */
 enum {
     W12_GEMM_Q8VIEW = 1,      /* the Q pass (as w12_gemm_q8view) instead of the exact GEMM */
-    W12_GEMM_INPUT_READY = 2  /* x was complete before the previous operation on the stream started */
+    W12_GEMM_INPUT_READY = 2, /* x was complete before the previous operation on the stream started */
+    W12_GEMM_OUT_BF16 = 4,    /* y is BF16: each FP32 result rounded to nearest, ties to even */
+    W12_GEMM_SILU_MUL = 8     /* gated-MLP product of row pairs (gate 2i, up 2i+1): y is [M][N/2] */
 };
 
 /*
  * w12_gemm / w12_gemm_q8view with flags.  Arguments, limits and errors are
- * w12_gemm's; an unknown flag bit gives INVALID_ARG.
+ * w12_gemm's, with y's element type and row length set by the flags: FP32
+ * [M][N] by default; BF16 under W12_GEMM_OUT_BF16; [M][N/2] under
+ * W12_GEMM_SILU_MUL.  An unknown flag bit gives INVALID_ARG.
+ *
+ * Epilogues of a decode step's projections (the pages time the projections of
+ * one dense layer -- q, k, v, o, gate, up, down -- and leave the work beside
+ * each GEMM open; these are the plain readings of that layer):
+ * - W12_GEMM_OUT_BF16 writes each FP32 result rounded to the nearest BF16,
+ *   ties to even (IEEE 754), so y can feed the next GEMM as its x.
+ * - W12_GEMM_SILU_MUL is for a gate and an up projection merged into one
+ *   matrix by interleaving their rows (row 2i = gate row i, row 2i+1 = up row
+ *   i; encode the merged BF16 matrix once): y[m][i] = silu(g) * u with g and u
+ *   the FP32 results of rows 2i and 2i+1 and silu(g) = g / (1 + e^-g), in
+ *   FP32.  N must be even (else SHAPE).  With W12_GEMM_OUT_BF16 as well, the
+ *   product is rounded to BF16 -- the down projection's input.
  *
  * Every GEMM launch may begin (streaming its weights) while the previous
  * kernel on the stream is still finishing; by default it reads x only after
@@ -196,7 +212,7 @@ enum {
  * has completed, so the previous kernel may read or write y.  The flag has no
  * counterpart on the pages: it is a launch-overlap mode of this library.
  */
-w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int N, int K,
                        unsigned flags, w12_stream_t stream);
 
 /*

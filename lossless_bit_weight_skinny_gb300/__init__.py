@@ -102,6 +102,8 @@ EXPORTED = (
 
 W12_GEMM_Q8VIEW = 1
 W12_GEMM_INPUT_READY = 2
+W12_GEMM_OUT_BF16 = 4
+W12_GEMM_SILU_MUL = 8
 
 
 class W12Error(RuntimeError):
@@ -306,17 +308,25 @@ def w12_gemm_q8view(x, d: Dev, y=None, stream=None):
     return _gemm(_lib.w12_gemm_q8view, "w12_gemm_q8view", x, d, y, stream)
 
 
-def w12_gemm_ex(x, d: Dev, y=None, stream=None, q8view=False, input_ready=False):
-    """w12_gemm (or the Q pass) with flags; input_ready states that x was
+def w12_gemm_ex(x, d: Dev, y=None, stream=None, q8view=False, input_ready=False, out_bf16=False,
+                silu_mul=False):
+    """w12_gemm (or the Q pass) with flags.  input_ready states that x was
     complete before the previous operation on the stream started, so the
-    launch may read it at once and overlap that operation's tail."""
+    launch may read it at once and overlap that operation's tail.  out_bf16
+    writes y as BF16 (round to nearest even); silu_mul treats rows 2i / 2i+1
+    as a gate / up pair and writes y[M][N/2] = silu(gate) * up."""
     import torch
     if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
         raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
     M, K = x.shape
+    cols = d.N // 2 if silu_mul else d.N
+    dt = torch.bfloat16 if out_bf16 else torch.float32
     if y is None:
-        y = torch.empty((M, d.N), dtype=torch.float32, device=x.device)
-    flags = (W12_GEMM_Q8VIEW if q8view else 0) | (W12_GEMM_INPUT_READY if input_ready else 0)
+        y = torch.empty((M, cols), dtype=dt, device=x.device)
+    elif y.dtype != dt or not y.is_cuda or y.numel() < M * cols:
+        raise TypeError(f"y must be a CUDA {dt} tensor of at least {M} x {cols} elements")
+    flags = ((W12_GEMM_Q8VIEW if q8view else 0) | (W12_GEMM_INPUT_READY if input_ready else 0)
+             | (W12_GEMM_OUT_BF16 if out_bf16 else 0) | (W12_GEMM_SILU_MUL if silu_mul else 0))
     _check(_lib.w12_gemm_ex(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
                             flags, _stream_ptr(stream)), "w12_gemm_ex")
     return y

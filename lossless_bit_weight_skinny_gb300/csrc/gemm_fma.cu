@@ -605,24 +605,42 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 const bool writer = (V >= 32) || ((lane & ((32 >> LOGV) - 1)) == 0);
                 const bool direct = (c_first == c_last);
                 const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
+                float tot[VPL];
 #pragma unroll
                 for (int q = 0; q < VPL; ++q) {
                     const int idx = (V >= 32) ? lane * VPL + q : (lane >> (5 - LOGV));
                     const int r = idx / MT, m = idx % MT;
                     // the placeholder products out first, then the exact ones in
-                    float total = v[q];
+                    tot[q] = v[q];
                     if (!Q8) {
                         const int i = (wrow + r) * MT + m;
                         if constexpr (NE == 1)
-                            total = (total + cneg0[i]) + cpos0[i];
+                            tot[q] = (tot[q] + cneg0[i]) + cpos0[i];
                         else
-                            total = (total + (cneg0[i] + cneg1[i])) + (cpos0[i] + cpos1[i]);
+                            tot[q] = (tot[q] + (cneg0[i] + cneg1[i])) + (cpos0[i] + cpos1[i]);
                     }
+                }
+                // under kOutSiluMul, the value of row r + 1 (value index idx + MT):
+                // another lane's (same q) or, with several values a lane, this one's
+                constexpr int PAIR_IN_LANE = (V >= 32 && VPL % (2 * MT) == 0) ? 1 : 0;
+                constexpr int PAIR_DL = V < 32 ? (MT << (5 - LOGV)) : (PAIR_IN_LANE ? 0 : MT / VPL);
+                static_assert(PAIR_IN_LANE || (V < 32) || (MT % VPL == 0), "gate/up pairing layout");
+                const bool pair = direct && (a.out_mode & kOutSiluMul);
+#pragma unroll
+                for (int q = 0; q < VPL; ++q) {
+                    const int idx = (V >= 32) ? lane * VPL + q : (lane >> (5 - LOGV));
+                    const int r = idx / MT, m = idx % MT;
+                    const float total = tot[q];
+                    float next = 0.f;
+                    if constexpr (PAIR_IN_LANE)
+                        next = tot[(q + MT) % VPL];
+                    else if (pair)
+                        next = __shfl_down_sync(0xffffffffu, total, PAIR_DL);
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
                         if (direct) {
                             if (n < a.N)
-                                a.y[static_cast<size_t>(m) * a.N + n] = total;
+                                emit_y(a, m, n, total, next);
                         } else {
                             a.partials[(static_cast<size_t>(slot) * a.M + m) * RBLK + wrow + r] = total;
                         }
@@ -643,7 +661,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                         *seg_last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1 : 0;
                     named_bar_sync(1, CW * 32);
                     if (*seg_last)
-                        sk_reduce_block(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
+                        sk_reduce_block<true>(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
                 }
             }
             // next iteration: (row block, k step) and ring slot

@@ -180,7 +180,9 @@ struct EscPatcher {
 };
 
 // 19 warps: 5 per SM sub-partition, whose 16K registers allow 102 per thread
-template <int MT, bool Q8>
+// EPI: the output goes through the output mode (BF16, SiLU*mul); the default
+// FP32 store is a kernel of its own, whose registers that code leaves alone.
+template <int MT, bool Q8, bool EPI>
 __global__ void __maxnreg__(96)
     gemm_tc_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
                    const __grid_constant__ CUtensorMap tm_b,
@@ -630,13 +632,20 @@ __global__ void __maxnreg__(96)
                 const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
                 const int n = row0 + row;
                 if (used) {
+                    const bool pair = EPI && direct && (a.out_mode & kOutSiluMul);
 #pragma unroll
                     for (int j = 0; j < PART; ++j) {
                         const int m = c * PART + j;
+                        // row + 1 (the up row of an even gate row) is lane + 1
+                        const float next = pair ? __shfl_down_sync(0xffffffffu, out[j], 1) : 0.f;
                         if (m < a.M) {
                             if (direct) {
-                                if (n < a.N)
-                                    a.y[static_cast<size_t>(m) * a.N + n] = out[j];
+                                if (n < a.N) {
+                                    if constexpr (EPI)
+                                        emit_y(a, m, n, out[j], next);
+                                    else
+                                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + n] = out[j];
+                                }
                             } else {
                                 a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = out[j];
                             }
@@ -652,7 +661,7 @@ __global__ void __maxnreg__(96)
                         *seg_last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1 : 0;
                     named_bar_sync(1, kDecodeWarps * 32);
                     if (*seg_last)
-                        sk_reduce_block(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);
+                        sk_reduce_block<EPI>(a, rb, 128, grid, c_first, c_last, threadIdx.x, kDecodeWarps * 32);
                 }
             }
             if (++ks == nk) {
@@ -677,12 +686,12 @@ __global__ void __maxnreg__(96)
     }
 }
 
-template <int MT, bool Q8>
+template <int MT, bool Q8, bool EPI>
 cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
                        const CUtensorMap *tm_x, int grid, cudaStream_t st)
 {
     using L = TcSmem<MT, Q8>;
-    auto kern = gemm_tc_kernel<MT, Q8>;
+    auto kern = gemm_tc_kernel<MT, Q8, EPI>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -704,17 +713,25 @@ int tc_smem_bytes(int mt, bool q8)
     }
 }
 
+template <int MT>
+cudaError_t launch_mt(bool q8, const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
+                      const CUtensorMap *tm_x, int grid, cudaStream_t st)
+{
+    if (a.out_mode)
+        return q8 ? launch_one<MT, true, true>(a, tm_ae, tm_b, tm_x, grid, st)
+                  : launch_one<MT, false, true>(a, tm_ae, tm_b, tm_x, grid, st);
+    return q8 ? launch_one<MT, true, false>(a, tm_ae, tm_b, tm_x, grid, st)
+              : launch_one<MT, false, false>(a, tm_ae, tm_b, tm_x, grid, st);
+}
+
 cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                            cudaStream_t st)
 {
     switch (mt) {
-    case 16: return q8 ? launch_one<16, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                       : launch_one<16, false>(a, tm_ae, tm_b, tm_x, grid, st);
-    case 32: return q8 ? launch_one<32, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                       : launch_one<32, false>(a, tm_ae, tm_b, tm_x, grid, st);
-    case 64: return q8 ? launch_one<64, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                       : launch_one<64, false>(a, tm_ae, tm_b, tm_x, grid, st);
+    case 16: return launch_mt<16>(q8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 32: return launch_mt<32>(q8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 64: return launch_mt<64>(q8, a, tm_ae, tm_b, tm_x, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -21,7 +22,7 @@ struct GemmArgs {
     const uint32_t *tile_ptr;      // [T + 1]
     const uint32_t *esc;           // escape entries
     const uint16_t *gptr;          // [T][16]: entries of tile t in rows < 8g
-    float *y;                      // [M][N]
+    void *y;                       // [M][ldy]: FP32, or BF16 under kOutBF16
     float *partials;               // [2 * grid][M][rows_blk] split-K partial sums
     unsigned long long *counters;  // [n_rowblk] arrivals (zero between launches)
     int *status;                   // device status word of the handle
@@ -33,7 +34,38 @@ struct GemmArgs {
     uint64_t limit_ns;             // bounded-wait limit
     int inject_stall;              // test hook: wait on a barrier nobody arrives on
     int x_ready;                   // x was complete before the previous launch: load it at once
+    int out_mode;                  // kOutBF16 | kOutSiluMul
+    int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
 };
+
+// Output modes.  kOutBF16: y holds BF16, each FP32 result rounded to the
+// nearest BF16 (ties to even).  kOutSiluMul: the matrix's rows come in
+// (gate, up) pairs -- row 2i is gate row i, row 2i+1 up row i -- and y[m][i]
+// = silu(y2i) * y2i+1 with silu(g) = g / (1 + e^-g), the gated-MLP product
+// of a dense layer, so that y[M][N/2] is the input of the down projection.
+constexpr int kOutBF16 = 1;
+constexpr int kOutSiluMul = 2;
+
+__device__ __forceinline__ void put_y(const GemmArgs &a, int m, int col, float v)
+{
+    const size_t i = static_cast<size_t>(m) * a.ldy + col;
+    if (a.out_mode & kOutBF16)
+        static_cast<__nv_bfloat16 *>(a.y)[i] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(a.y)[i] = v;
+}
+
+// The final value v of y[m][n] (n < N); `next` is the final value of row n + 1
+// (read only under kOutSiluMul, where N is even and a gate row n is even).
+__device__ __forceinline__ void emit_y(const GemmArgs &a, int m, int n, float v, float next)
+{
+    if (a.out_mode & kOutSiluMul) {
+        if ((n & 1) == 0)
+            put_y(a, m, n >> 1, v / (1.0f + expf(-v)) * next);
+    } else {
+        put_y(a, m, n, v);
+    }
+}
 
 // One BF16x2 pair (weights 2i, 2i+1 of a group of 8) from the group's AE word
 // holding those two bytes and its B word (SpecPilot, Figure 5(a) caption):
@@ -135,7 +167,9 @@ __device__ __forceinline__ void report(int *status, int code)
 // contributors c_first + j, c_first + j + P, ... in order, with independent
 // 16-byte loads, and the P lanes then combine by a fixed butterfly.  The order
 // is fixed, so results are bitwise reproducible, and many contributors cost
-// one round of loads instead of one per contributor.
+// one round of loads instead of one per contributor.  EPI: the results go
+// through the output mode (emit_y); otherwise y is FP32 [M][N].
+template <bool EPI>
 __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int rows_blk, int grid,
                                                 int c_first, int c_last, int tid, int nthreads)
 {
@@ -186,12 +220,16 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
         }
         if (g < groups && j == 0) {
             const int m = (4 * g) / rows_blk, r = (4 * g) % rows_blk;
-            float *yp = a.y + static_cast<size_t>(m) * a.N + row0 + r;
             const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (row0 + r + q < a.N)
-                    yp[q] = v4[q];
+            for (int q = 0; q < 4; ++q) {
+                if (row0 + r + q < a.N) {
+                    if constexpr (EPI)
+                        emit_y(a, m, row0 + r + q, v4[q], v4[(q + 1) & 3]);
+                    else
+                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + row0 + r + q] = v4[q];
+                }
+            }
         }
     }
 }

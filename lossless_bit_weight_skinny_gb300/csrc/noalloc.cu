@@ -146,6 +146,7 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     a.esc = w->esc;
     a.gptr = w->gptr;
     a.y = y;
+    a.ldy = N;
     a.status = w->status;
     a.M = M;
     a.N = N;

@@ -131,13 +131,17 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, int K,
-                     cudaStream_t st, bool q8, bool x_ready = false)
+w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
+                     cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
 {
     if (!w || M < 0)
         return W12_ERR_INVALID_ARG;
     if (N != w->N || K != w->K)
         return W12_ERR_SHAPE;
+    if ((out_mode & kOutSiluMul) && (N & 1))
+        return W12_ERR_SHAPE;
+    const int ldy = (out_mode & kOutSiluMul) ? N / 2 : N;
+    const size_t ybytes = ((out_mode & kOutBF16) ? 2 : 4) * static_cast<size_t>(M) * ldy;
     if (M > 64)
         return W12_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
@@ -152,7 +156,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     if (cur != w->device)
         return W12_ERR_INVALID_ARG;
     if (K == 0)
-        return cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st) == cudaSuccess
+        return cudaMemsetAsync(y, 0, ybytes, st) == cudaSuccess
                    ? W12_OK
                    : W12_ERR_CUDA;
     if (!w->gemm_ok)
@@ -171,6 +175,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, float *y, int M, int N, in
     a.esc = w->esc;
     a.gptr = w->gptr;
     a.y = y;
+    a.out_mode = out_mode;
+    a.ldy = ldy;
     a.status = w->status;
     a.M = M;
     a.N = N;
@@ -371,13 +377,15 @@ w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M
     return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
-w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int N, int K,
                        unsigned flags, w12_stream_t stream)
 {
-    if (flags & ~static_cast<unsigned>(W12_GEMM_Q8VIEW | W12_GEMM_INPUT_READY))
+    if (flags & ~static_cast<unsigned>(W12_GEMM_Q8VIEW | W12_GEMM_INPUT_READY | W12_GEMM_OUT_BF16 |
+                                       W12_GEMM_SILU_MUL))
         return W12_ERR_INVALID_ARG;
+    const int out_mode = ((flags & W12_GEMM_OUT_BF16) ? kOutBF16 : 0) | ((flags & W12_GEMM_SILU_MUL) ? kOutSiluMul : 0);
     return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream),
-                     (flags & W12_GEMM_Q8VIEW) != 0, (flags & W12_GEMM_INPUT_READY) != 0);
+                     (flags & W12_GEMM_Q8VIEW) != 0, (flags & W12_GEMM_INPUT_READY) != 0, out_mode);
 }
 
 w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, float *y_dev,

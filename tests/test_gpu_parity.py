@@ -356,4 +356,4 @@ def test_input_ready_chain(w12):
     d, x, ref = cases[0]
     P = __import__("ctypes").c_void_p
     assert w12.lib().w12_gemm_ex(P(x.data_ptr()), d.ptr, P(ys[0].data_ptr()), x.shape[0], d.N, x.shape[1],
-                                 8, P(stream.cuda_stream)) == 1
+                                 16, P(stream.cuda_stream)) == 1
