@@ -346,9 +346,11 @@ def run_w12(args):
                 "no_overlap": round(1e3 * time_graph(M, xs, ys, "none", short), 2),
                 "independent_inputs": round(1e3 * time_graph(M, xs, ys, "independent", short), 2)}
 
-    # the same layer at M = 32 and M = 64 (tensor-core path), shorter runs
+    # the same layer at M = 32, 64, 128 (tensor-core path, one launch per
+    # projection) and 256 (two launches of 128 rows), shorter runs; GB/s counts
+    # the W12 bytes once
     by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
-    for Mx in (32, 64):
+    for Mx in (32, 64, 128, 256):
         xm = acts(Mx, 9)
         ym = {n: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
         msm = time_graph(Mx, xm, ym, "layer", short)
@@ -462,7 +464,8 @@ def run_w12(args):
         dlayers = [[(name, WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi).view(torch.bfloat16))
                     for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS)] for li in range(len(layers))]
         dense = {"us_per_layer": {}, "w12_speedup": {}}
-        for Mx, w12_us in ((1, modes_us["layer"]), (32, by_m["32"]["us_per_layer"])):
+        for Mx, w12_us in ((1, modes_us["layer"]), (32, by_m["32"]["us_per_layer"]),
+                           (128, by_m["128"]["us_per_layer"])):
             xdn = {g: v for g, v in acts(Mx, 9 if Mx > 1 else 7).items()}
 
             def stepd(i):

@@ -1,6 +1,6 @@
 /*
  * w12.h -- C ABI of the W12 library: lossless 12-bit storage of BF16 weights
- * and the skinny-M GEMM (1..64 activation rows) that decodes it on the fly on
+ * and the skinny-M GEMM (1..256 activation rows) that decodes it on the fly on
  * one GB300 GPU (sm_103a).
  *
  * Sources (pages about "SpecPilot: Autonomous Algorithm Discovery and Systems
@@ -51,7 +51,7 @@ typedef enum {
     W12_ERR_INVALID_ARG = 1, /* NULL pointer or negative size               */
     W12_ERR_SHAPE = 2,       /* N/K disagree with the encoded matrix         */
     W12_ERR_ALIGNMENT = 3,   /* a device buffer is not 16-byte aligned       */
-    W12_ERR_UNSUPPORTED = 4, /* M outside 1..64, K % 32 != 0 for the GEMM    */
+    W12_ERR_UNSUPPORTED = 4, /* M outside 0..256, K % 32 != 0 for the GEMM   */
     W12_ERR_OOM = 5,         /* host or device allocation failed             */
     W12_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed            */
     W12_ERR_CORRUPT = 7,     /* an encoded matrix breaks a format invariant  */
@@ -154,10 +154,12 @@ w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device
 /*
  * y[M][N] = x[M][K] . W^T with W decoded to exact BF16 on the fly [F5a, F5b]
  * and FP32 accumulation.  x: device BF16 [M][K], 16-byte aligned; y: device
- * FP32 [M][N], 16-byte aligned; both caller-owned.  1 <= M <= 64 (M = 0 is a
- * no-op), N and K must equal the handle's; K % 32 == 0 (else UNSUPPORTED).
+ * FP32 [M][N], 16-byte aligned; both caller-owned.  1 <= M <= 256 (M = 0 is
+ * a no-op), N and K must equal the handle's; K % 32 == 0 (else UNSUPPORTED).
  * Kernel choice is a function of M only: M <= 2 CUDA-core FMAs with warp
- * reductions, 3..64 tcgen05 tensor cores with TMEM accumulators.  Uses a
+ * reductions, 3..128 tcgen05 tensor cores with TMEM accumulators (one
+ * launch; every weight is read once), 129..256 two launches of up to 128
+ * activation rows each (the weights are read twice).  Uses a
  * library-owned workspace cached per (device, stream); the first call on a
  * stream allocates it (stream-ordered), so make that first call outside any
  * stream capture.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM,
@@ -232,8 +234,9 @@ w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, 
  * convenience.)  Same arguments, result and errors as w12_gemm, but the
  * split-K scratch comes from one fixed 16 MiB array in device memory that
  * every GPU loading this library holds until exit; a call needing more
- * (over 8192 row blocks, or a GPU too large for 2 * SMs * M * 128 partial
- * sums) fails with W12_ERR_UNSUPPORTED.  All calls on a device share the
+ * (over 8192 row blocks, or more than 2 * CTAs * M * 128 FP32 partial sums,
+ * M counted per launch of at most 128 rows -- on a 152-SM GB300 that is M
+ * above about 107) fails with W12_ERR_UNSUPPORTED.  All calls on a device share the
  * array, so calls whose kernels overlap on the GPU (other streams, other
  * threads) race: serialise them.  The first call on each device looks up the
  * array, clears its counters and synchronises the device; make it before any

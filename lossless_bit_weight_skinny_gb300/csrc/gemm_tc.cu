@@ -42,8 +42,6 @@ constexpr int kWarpM = kDecodeWarps + 2; // MMA issuer, tensor-memory owner
 constexpr int kWarpE = kDecodeWarps + 3; // escape warp: sorts each unit's escapes per decode warp
 constexpr int kThreads = (kDecodeWarps + 4) * 32;
 constexpr int kPCap = 24;                // escapes per decode warp and unit kept in its list
-constexpr int kNA = 3;                   // A buffers in tensor memory, 128 columns each
-constexpr uint32_t kDCol = kNA * 128;    // two accumulator buffers of 64 columns
 static_assert(kTcKStep == 256 && kTcRows == 128, "one unit = one escape tile");
 
 constexpr int a1024(int v) { return (v + 1023) & ~1023; }
@@ -65,27 +63,39 @@ struct TcSmem {
     static constexpr int PL_LO = 64;
     static constexpr int PL_LIST = 80;
     static constexpr int PL = Q8 ? 0 : PL_LIST + 4 * kPCap * kDecodeWarps;
-    // activation stage: four 64-column sub-tiles of MT rows, 128-byte swizzle
+    // tensor memory (512 columns): NA decoded A tiles of 128 columns, then two
+    // FP32 accumulator buffers of DW columns (MT <= 64: 3 x 128 + 2 x 64;
+    // MT = 128: 2 x 128 + 2 x 128)
+    static constexpr int NA = MT == 128 ? 2 : 3;
+    static constexpr uint32_t DCOL = NA * 128;
+    static constexpr uint32_t DW = MT <= 64 ? 64 : 128;
+    // activations: a unit needs four 64-column sub-tiles of MT rows (128-byte
+    // swizzle); a ring slot holds SPS of them -- the whole unit's (SPS = 4)
+    // up to 64 rows, one sub-tile (SPS = 1) at 128 rows, where a unit's 64 KB
+    // would leave too little room for the weights
     static constexpr int XSUB = MT * 128;
-    static constexpr int XSTAGE = 4 * XSUB;
-    static constexpr int XST = (MT <= 32) ? 3 : 2; // activation slots
+    static constexpr int SPS = MT == 128 ? 1 : 4;
+    static constexpr int SPU = 4 / SPS;       // slots per unit
+    static constexpr int XSLOT = SPS * XSUB;
+    static constexpr int XST = MT <= 32 ? 3 : MT == 64 ? 2 : W12_TC_XST128; // activation slots
     // per decode warp: one row of 32 BF16 pairs, for patching escapes
     static constexpr int SCR_PITCH = 144;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * SCR_PITCH;
     static constexpr int BUDGET = 227 * 1024 - 2048;
-    static constexpr int WST_RAW = (BUDGET - XST * XSTAGE - SCR) / (WSTAGE + PL);
+    static constexpr int WST_RAW = (BUDGET - XST * XSLOT - SCR) / (WSTAGE + PL);
     static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight slots
     static constexpr int OFF_X = WST * WSTAGE;
-    static constexpr int OFF_SCR = OFF_X + XST * XSTAGE;
+    static constexpr int OFF_SCR = OFF_X + XST * XSLOT;
     static constexpr int OFF_PL = OFF_SCR + SCR;
     static constexpr int BARS = (OFF_PL + WST * PL + 15) & ~15;
-    // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [kNA];
+    // w_full, w_empty [WST]; x_full, x_empty [XST]; a_full, a_empty [NA];
     // acc_full, acc_empty [2]; final, stall; pl_full, pl_empty [WST]
-    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * kNA + 4 + 2 + 2 * WST;
+    static constexpr int NBARS = 2 * WST + 2 * XST + 2 * NA + 4 + 2 + 2 * WST;
     static constexpr int TOTAL = BARS + 8 * NBARS + 32 + 1024; // + slack to align the base
     static constexpr int W_TX = AE + B;
-    static_assert(kDCol + 2 * 64 <= 512, "tensor memory budget");
-    static_assert(WST >= 3, "weight ring too shallow");
+    static_assert(DCOL + 2 * DW <= 512 && DW >= MT, "tensor memory budget");
+    static_assert(WST >= 3 || (MT == 128 && WST >= 2), "weight ring too shallow");
+    static_assert(XST >= SPU, "activation ring shallower than a unit");
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
@@ -189,7 +199,8 @@ __global__ void __maxnreg__(96)
                    const __grid_constant__ CUtensorMap tm_x)
 {
     using L = TcSmem<MT, Q8>;
-    constexpr int WST = L::WST, XST = L::XST;
+    constexpr int WST = L::WST, XST = L::XST, kNA = L::NA;
+    constexpr uint32_t kDCol = L::DCOL;
     constexpr uint32_t IDESC = idesc_bf16_f32(128, MT);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -306,26 +317,32 @@ __global__ void __maxnreg__(96)
             // kernel started (writes wait for it in any case: see the epilogue)
             if (!a.x_ready)
                 pdl_wait_prior_grid();
-            int issued = 0;
+            int issued = 0; // slot loads started
             int ks = it0 % nk, s = 0;
             uint32_t ph = 0;
-            for (int it = 0; it < n_it; ++it) {
-                if (!wait_or_abort(x_empty0 + 8 * s, ph ^ 1, a, abort_flag))
-                    break;
+            bool ok = true;
+            for (int it = 0; it < n_it && ok; ++it) {
                 const int k0 = ks * 256;
-                uint8_t *xs = smem + L::OFF_X + s * L::XSTAGE;
-                const uint32_t fb = x_full0 + 8 * s;
-                mbar_arrive_expect_tx(fb, L::XSTAGE);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    tma_load_2d(smem_u32(xs + j * L::XSUB), &tm_x, k0 + 64 * j, 0, fb);
-                issued = it + 1;
+                for (int h = 0; h < L::SPU; ++h) {
+                    if (!wait_or_abort(x_empty0 + 8 * s, ph ^ 1, a, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *xs = smem + L::OFF_X + s * L::XSLOT;
+                    const uint32_t fb = x_full0 + 8 * s;
+                    mbar_arrive_expect_tx(fb, L::XSLOT);
+#pragma unroll
+                    for (int j = 0; j < L::SPS; ++j)
+                        tma_load_2d(smem_u32(xs + j * L::XSUB), &tm_x, k0 + 64 * (h * L::SPS + j), 0, fb);
+                    ++issued;
+                    if (++s == XST) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
                 if (++ks == nk)
                     ks = 0;
-                if (++s == XST) {
-                    s = 0;
-                    ph ^= 1;
-                }
             }
             for (int it = issued - 1; it >= 0 && it >= issued - XST; --it)
                 mbar_wait(x_full0 + 8 * (it % XST), (it / XST) & 1, 1000000000ull);
@@ -334,13 +351,11 @@ __global__ void __maxnreg__(96)
     } else if (warp == kWarpM) {
         // ------------------------------ MMA issuer -----------------------------
         if (lane == 0) {
-            // shared-memory descriptor of each activation slot's first sub-tile;
-            // the 16 K-steps of a unit add a fixed offset (address field in
-            // 16-byte units: +2 per 16 columns, +XSUB/16 per 64-column sub-tile)
-            uint64_t xdesc[XST];
-#pragma unroll
-            for (int j = 0; j < XST; ++j)
-                xdesc[j] = smem_desc_sw128(smem_u32(smem + L::OFF_X + j * L::XSTAGE), 1024);
+            // shared-memory descriptor of the first activation slot; slot sx
+            // adds sx * XSLOT / 16, and within a slot the K-steps of 16 columns
+            // add a fixed offset (address field in 16-byte units: +2 per 16
+            // columns, +XSUB/16 per 64-column sub-tile)
+            const uint64_t xdesc0 = smem_desc_sw128(smem_u32(smem + L::OFF_X), 1024);
             int seg = 0;
             int ks = it0 % nk, sx = 0, b = 0;
             uint32_t phx = 0, pha = 0;
@@ -353,35 +368,38 @@ __global__ void __maxnreg__(96)
                 if (seg_start && seg >= 2)
                     ok = wait_or_abort(acc_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
                 ok = wait_or_abort(a_full0 + 8 * b, pha, a, abort_flag) && ok;
-                ok = wait_or_abort(x_full0 + 8 * sx, phx, a, abort_flag) && ok;
-                tc_fence_after();
-                if (ok) {
-                    uint64_t bdesc = xdesc[0];
+                const uint32_t d = tmem + kDCol + L::DW * db;
+                const uint32_t a0 = tmem + b * 128;
 #pragma unroll
-                    for (int j = 1; j < XST; ++j)
-                        if (sx == j)
-                            bdesc = xdesc[j];
-                    const uint32_t d = tmem + kDCol + 64 * db;
-                    const uint32_t a0 = tmem + b * 128;
-                    tc_mma_ts(d, a0, bdesc, IDESC, seg_start ? 0u : 1u);
+                for (int h = 0; h < L::SPU; ++h) {
+                    const bool okx = wait_or_abort(x_full0 + 8 * sx, phx, a, abort_flag) && ok;
+                    tc_fence_after();
+                    if (okx) {
+                        const uint64_t bdesc = xdesc0 + static_cast<uint64_t>(sx * (L::XSLOT >> 4));
 #pragma unroll
-                    for (int j = 1; j < 16; ++j)
-                        tc_mma_ts_acc(d, a0 + j * 8,
-                                      bdesc + static_cast<uint64_t>((j >> 2) * (L::XSUB >> 4) + (j & 3) * 2), IDESC);
+                        for (int jj = 0; jj < 4 * L::SPS; ++jj) {
+                            const int j = h * 4 * L::SPS + jj; // K-step of 16 columns in the unit
+                            const uint64_t bj = bdesc + static_cast<uint64_t>((jj >> 2) * (L::XSUB >> 4) + (jj & 3) * 2);
+                            if (j == 0)
+                                tc_mma_ts(d, a0, bj, IDESC, seg_start ? 0u : 1u);
+                            else
+                                tc_mma_ts_acc(d, a0 + j * 8, bj, IDESC);
+                        }
+                    }
+                    // each commit arrives once every MMA issued so far has completed
+                    tc_commit(x_empty0 + 8 * sx);
+                    if (++sx == XST) {
+                        sx = 0;
+                        phx ^= 1;
+                    }
                 }
-                // each commit arrives once every MMA issued so far has completed
                 tc_commit(a_empty0 + 8 * b);
-                tc_commit(x_empty0 + 8 * sx);
                 if (seg_end) {
                     tc_commit(acc_full0 + 8 * db);
                     ++seg;
                 }
                 if (++ks == nk)
                     ks = 0;
-                if (++sx == XST) {
-                    sx = 0;
-                    phx ^= 1;
-                }
                 if (++b == kNA) {
                     b = 0;
                     pha ^= 1;
@@ -592,32 +610,46 @@ __global__ void __maxnreg__(96)
                 wait_or_abort(acc_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
                 __syncwarp();
                 tc_fence_after();
-                constexpr int PART = MT / 4; // accumulator columns read by this warp
-                float out[PART];
+                constexpr int PART = MT / 4;              // accumulator columns read by this warp
+                constexpr int CH = PART < 16 ? PART : 16; // read and stored in chunks of CH
                 const bool used = c * PART < a.M;
+                const int c_first = sk_owner(rb * nk, grid, a.total_iters);
+                const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
+                const bool direct = (c_first == c_last);
+                const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
+                const int n = row0 + row;
                 if (used) {
-                    const uint32_t dcol = tmem + t_lane + kDCol + 64 * db + c * PART;
-                    if constexpr (PART == 4) {
-                        uint32_t d[4];
-                        tmem_ld4(dcol, d);
+                    const uint32_t dcol = tmem + t_lane + kDCol + L::DW * db + c * PART;
+                    const bool pair = EPI && direct && (a.out_mode & kOutSiluMul);
+#pragma unroll
+                    for (int h = 0; h < PART / CH; ++h) {
+                        uint32_t d[CH];
+                        if constexpr (CH == 4)
+                            tmem_ld4(dcol, d);
+                        else if constexpr (CH == 8)
+                            tmem_ld8(dcol, d);
+                        else
+                            tmem_ld16(dcol + 16 * h, d);
                         tc_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            out[j] = __uint_as_float(d[j]);
-                    } else if constexpr (PART == 8) {
-                        uint32_t d[8];
-                        tmem_ld8(dcol, d);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            out[j] = __uint_as_float(d[j]);
-                    } else {
-                        uint32_t d[16];
-                        tmem_ld16(dcol, d);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            out[j] = __uint_as_float(d[j]);
+                        for (int j = 0; j < CH; ++j) {
+                            const float v = __uint_as_float(d[j]);
+                            const int m = c * PART + h * CH + j;
+                            // row + 1 (the up row of an even gate row) is lane + 1
+                            const float next = pair ? __shfl_down_sync(0xffffffffu, v, 1) : 0.f;
+                            if (m < a.M) {
+                                if (direct) {
+                                    if (n < a.N) {
+                                        if constexpr (EPI)
+                                            emit_y(a, m, n, v, next);
+                                        else
+                                            static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + n] = v;
+                                    }
+                                } else {
+                                    a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = v;
+                                }
+                            }
+                        }
                     }
                 }
                 tc_fence_before();
@@ -626,32 +658,6 @@ __global__ void __maxnreg__(96)
                     mbar_arrive(acc_empty0 + 8 * db);
                 ++seg;
 
-                const int c_first = sk_owner(rb * nk, grid, a.total_iters);
-                const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
-                const bool direct = (c_first == c_last);
-                const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
-                const int n = row0 + row;
-                if (used) {
-                    const bool pair = EPI && direct && (a.out_mode & kOutSiluMul);
-#pragma unroll
-                    for (int j = 0; j < PART; ++j) {
-                        const int m = c * PART + j;
-                        // row + 1 (the up row of an even gate row) is lane + 1
-                        const float next = pair ? __shfl_down_sync(0xffffffffu, out[j], 1) : 0.f;
-                        if (m < a.M) {
-                            if (direct) {
-                                if (n < a.N) {
-                                    if constexpr (EPI)
-                                        emit_y(a, m, n, out[j], next);
-                                    else
-                                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + n] = out[j];
-                                }
-                            } else {
-                                a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = out[j];
-                            }
-                        }
-                    }
-                }
                 if (!direct) {
                     // the CTA barrier orders every thread's partial stores before
                     // thread 0's release-acquire arrival (cumulativity), and that
@@ -709,7 +715,8 @@ int tc_smem_bytes(int mt, bool q8)
     switch (mt) {
     case 16: return q8 ? TcSmem<16, true>::TOTAL : TcSmem<16, false>::TOTAL;
     case 32: return q8 ? TcSmem<32, true>::TOTAL : TcSmem<32, false>::TOTAL;
-    default: return q8 ? TcSmem<64, true>::TOTAL : TcSmem<64, false>::TOTAL;
+    case 64: return q8 ? TcSmem<64, true>::TOTAL : TcSmem<64, false>::TOTAL;
+    default: return q8 ? TcSmem<128, true>::TOTAL : TcSmem<128, false>::TOTAL;
     }
 }
 
@@ -732,6 +739,7 @@ cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap
     case 16: return launch_mt<16>(q8, a, tm_ae, tm_b, tm_x, grid, st);
     case 32: return launch_mt<32>(q8, a, tm_ae, tm_b, tm_x, grid, st);
     case 64: return launch_mt<64>(q8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 128: return launch_mt<128>(q8, a, tm_ae, tm_b, tm_x, grid, st);
     }
     return cudaErrorInvalidValue;
 }

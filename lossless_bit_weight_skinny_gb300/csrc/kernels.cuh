@@ -275,6 +275,10 @@ static_assert(W12_TC_MIN_M >= 1 && W12_TC_MIN_M <= 5, "the CUDA-core kernel cove
 constexpr int kFmaKStep = 256;
 constexpr int kTcKStep = 256;
 constexpr int kTcRows = 128;
+// activation ring slots (one 64-column sub-tile each) of the 128-row kernel
+#ifndef W12_TC_XST128
+#define W12_TC_XST128 4
+#endif
 
 // Grid of one GEMM launch (host side).  The units (row block, k step) are
 // split evenly over the CTAs, one CTA per SM at most; a CTA's time is about

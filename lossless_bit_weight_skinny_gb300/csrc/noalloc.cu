@@ -104,16 +104,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 } // namespace
 
-extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, float *y, int M, int N,
-                                       int K, w12_stream_t stream)
+static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
+                               cudaStream_t st, bool x_ready)
 {
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (!w || M < 0)
-        return W12_ERR_INVALID_ARG;
-    if (N != w->N || K != w->K)
-        return W12_ERR_SHAPE;
-    if (M > 64)
-        return W12_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return W12_OK;
     if (!x_bf16 || !y)
@@ -133,7 +126,7 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
         return W12_ERR_UNSUPPORTED;
 
     const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     int sms = 0;
@@ -165,7 +158,7 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     a.total_iters = static_cast<int>(iters);
     a.limit_ns = 200ull * 1000 * 1000;
     a.inject_stall = 0;
-    a.x_ready = 0;
+    a.x_ready = x_ready ? 1 : 0;
 
     unsigned char *scratch = nullptr;
     const w12_status s = noalloc_setup(dev, &scratch);
@@ -186,4 +179,26 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
     const cudaError_t e = tc ? launch_gemm_tc(mt, false, a, pae, pb, &tmx, grid, st)
                              : launch_gemm_fma(mt, false, a, pae, pb, &tmx, grid, st);
     return e == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, float *y, int M, int N,
+                                       int K, w12_stream_t stream)
+{
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!w || M < 0)
+        return W12_ERR_INVALID_ARG;
+    if (N != w->N || K != w->K)
+        return W12_ERR_SHAPE;
+    if (M > 256)
+        return W12_ERR_UNSUPPORTED;
+    if (M <= 128)
+        return noalloc_impl(x_bf16, w, y, M, N, K, st, false);
+    // 128 activation rows per launch, as w12_gemm
+    if (!x_bf16 || !y)
+        return W12_ERR_INVALID_ARG;
+    const w12_status s1 = noalloc_impl(x_bf16, w, y, 128, N, K, st, false);
+    if (s1 != W12_OK)
+        return s1;
+    return noalloc_impl(static_cast<const uint16_t *>(x_bf16) + static_cast<size_t>(128) * K, w,
+                        y + static_cast<size_t>(128) * N, M - 128, N, K, st, true);
 }

@@ -108,9 +108,9 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
             return W12_ERR_UNSUPPORTED; // grow outside capture: make one call first
-        // first use: room for the largest call (M = 64, one CTA per SM), so a
+        // first use: room for the largest call (M = 128, one CTA per SM), so a
         // workspace never moves under a captured CUDA graph
-        const size_t most = kCounterBytes + sizeof(float) * 2 * static_cast<size_t>(sm_count(dev)) * 64 * 128;
+        const size_t most = kCounterBytes + sizeof(float) * 2 * static_cast<size_t>(sm_count(dev)) * 128 * 128;
         const size_t grow = need < most ? most : need;
         if (w.ptr)
             cudaFreeAsync(w.ptr, st);
@@ -131,6 +131,8 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+constexpr int kMaxM = 256;
+
 w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
                      cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
 {
@@ -142,10 +144,23 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
         return W12_ERR_SHAPE;
     const int ldy = (out_mode & kOutSiluMul) ? N / 2 : N;
     const size_t ybytes = ((out_mode & kOutBF16) ? 2 : 4) * static_cast<size_t>(M) * ldy;
-    if (M > 64)
+    if (M > kMaxM)
         return W12_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return W12_OK;
+    if (M > 128) {
+        // 128 activation rows per launch: the first 128, then the rest (whose
+        // x was complete before the first launch started)
+        if (!x || !y)
+            return W12_ERR_INVALID_ARG;
+        const size_t esz = (out_mode & kOutBF16) ? 2 : 4;
+        w12_status s1 = gemm_impl(x, w, y, 128, N, K, st, q8, x_ready, out_mode);
+        if (s1 != W12_OK)
+            return s1;
+        return gemm_impl(static_cast<const uint16_t *>(x) + static_cast<size_t>(128) * K, w,
+                         static_cast<char *>(y) + esz * 128 * static_cast<size_t>(ldy), M - 128, N, K, st, q8,
+                         true, out_mode);
+    }
     if (!x || !y)
         return W12_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y))
@@ -166,7 +181,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     // kernel for M <= 2; from 3 rows on, the tensor-core kernel (M padded to
     // 16, 32 or 64) is faster than four FMAs per weight.
     const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     GemmArgs a{};

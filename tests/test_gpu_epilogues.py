@@ -104,7 +104,7 @@ def _check_silu(got, ref, tol, what, bf16=False):
     assert not bad.any(), f"{what}: {bad.sum()} outside the bound; worst {(err / lim)[fin].max()}"
 
 
-@pytest.mark.parametrize("M", (1, 2, 3, 16, 33, 64))
+@pytest.mark.parametrize("M", (1, 2, 3, 16, 33, 64, 128, 200))
 @pytest.mark.parametrize("name", list(CASES.keys()))
 def test_bf16_output(w12, name, M):
     import torch
@@ -123,7 +123,7 @@ def test_bf16_output(w12, name, M):
 
 
 @pytest.mark.parametrize("bf16", (False, True))
-@pytest.mark.parametrize("M", (1, 2, 3, 16, 33, 64))
+@pytest.mark.parametrize("M", (1, 2, 3, 16, 33, 64, 96, 256))
 @pytest.mark.parametrize("name", list(CASES.keys()))
 def test_silu_mul(w12, name, M, bf16):
     import torch
@@ -165,7 +165,7 @@ def gate_up_full(w12):
     return W, d
 
 
-@pytest.mark.parametrize("M", (1, 2, 32, 64))
+@pytest.mark.parametrize("M", (1, 2, 32, 64, 128))
 def test_gate_up_full_size_sampled(w12, gate_up_full, M):
     W, d = gate_up_full
     rng = np.random.Generator(np.random.PCG64(M))

@@ -111,7 +111,7 @@ SHAPES = {
     "heavy_640x1024": lambda: WL.heavy_weights(640, 1024, seed=9),
     "rows_200x4096": lambda: WL.projection_weights(200, 4096, seed=10),
 }
-MS = (1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64)
+MS = (1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65, 96, 127, 128, 129, 200, 256)
 _cache = {}
 
 
@@ -132,7 +132,7 @@ def test_gemm_parity(w12, name, M):
     _check(_gemm(w12, d, x), x, Wdec, what=f"{name} M={M}")
 
 
-@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64))
+@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64, 128, 256))
 @pytest.mark.parametrize("name", list(SHAPES.keys()))
 def test_q8view_parity(w12, name, M):
     W, Wdec, Wq, d = _prepared(w12, name)
@@ -140,7 +140,7 @@ def test_q8view_parity(w12, name, M):
     _check(_gemm(w12, d, x, q8=True), x, Wq, what=f"q8 {name} M={M}")
 
 
-@pytest.mark.parametrize("M", (1, 4, 8, 16, 64))
+@pytest.mark.parametrize("M", (1, 4, 8, 16, 64, 128, 200))
 def test_deterministic(w12, M):
     W, Wdec, Wq, d = _prepared(w12, "heavy_640x1024")
     x = WL.activations(M, W.shape[1], seed=3000 + M)
@@ -159,7 +159,7 @@ def _one_hot_matrix():
     return W
 
 
-@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64))
+@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64, 128, 256))
 def test_one_hot_exact(w12, M):
     W = _one_hot_matrix()
     K = W.shape[1]
@@ -221,7 +221,7 @@ def test_projection_shapes_m1(w12, full_shapes, shape):
     assert np.array_equal(got, W)
 
 
-@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64))
+@pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64, 128, 256))
 @pytest.mark.parametrize("shape", [(17408, 5120), (5120, 17408)], ids=lambda s: f"{s[0]}x{s[1]}")
 def test_m_sweep(w12, full_shapes, shape, M):
     W, blob, d = full_shapes[shape]
@@ -261,12 +261,12 @@ def test_edges_and_errors(w12):
     lib = w12.lib()
     import ctypes
 
-    y = torch.empty((65, 256), dtype=torch.float32, device="cuda")
+    y = torch.empty((257, 256), dtype=torch.float32, device="cuda")
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     P = ctypes.c_void_p
     assert lib.w12_gemm(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 0, 256, 512, s) == 0
     assert lib.w12_gemm(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 4, 255, 512, s) == 2
-    assert lib.w12_gemm(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 65, 256, 512, s) == 4
+    assert lib.w12_gemm(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 257, 256, 512, s) == 4
     assert lib.w12_gemm(P(x.data_ptr() + 2), d.ptr, P(y.data_ptr()), 4, 256, 512, s) == 3
     assert lib.w12_gemm(None, d.ptr, P(y.data_ptr()), 4, 256, 512, s) == 1
     # K not a multiple of 32: the GEMM refuses, decode still works

@@ -36,8 +36,8 @@ def w12():
 
 
 CASES = [
-    ("kv_1024x5120", lambda: WL.projection_weights(1024, 5120, seed=2), (1, 2, 5, 16, 64)),
-    ("heavy_640x1024", lambda: WL.heavy_weights(640, 1024, seed=9), (1, 8, 16, 33, 64)),
+    ("kv_1024x5120", lambda: WL.projection_weights(1024, 5120, seed=2), (1, 2, 5, 16, 64, 100)),
+    ("heavy_640x1024", lambda: WL.heavy_weights(640, 1024, seed=9), (1, 8, 16, 33, 64, 128, 200)),
     ("ragged_300x800", lambda: WL.projection_weights(300, 800, seed=7, outlier_frac=2e-3), (3, 17)),
 ]
 
@@ -68,7 +68,7 @@ def test_noalloc_matches_gemm(w12, name, make, ms):
             got = y.cpu().numpy().astype(np.float64)
             assert np.all(np.abs(got - want) <= bound), f"{name} M={M} call {call}"
     # sizes past the supported range are refused, not run
-    x = torch.zeros((65, K), dtype=torch.bfloat16, device="cuda")
-    y = torch.empty((65, N), dtype=torch.float32, device="cuda")
-    assert lib.w12_gemm_noalloc(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 65, N, K,
+    x = torch.zeros((257, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((257, N), dtype=torch.float32, device="cuda")
+    assert lib.w12_gemm_noalloc(P(x.data_ptr()), d.ptr, P(y.data_ptr()), 257, N, K,
                                 P(stream.cuda_stream)) == 4
