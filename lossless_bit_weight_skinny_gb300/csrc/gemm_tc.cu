@@ -658,7 +658,7 @@ __global__ void __maxnreg__(96)
                     mbar_arrive(acc_empty0 + 8 * db);
                 ++seg;
 
-                if (!direct) {
+                if (!direct && !a.defer) {
                     // the CTA barrier orders every thread's partial stores before
                     // thread 0's release-acquire arrival (cumulativity), and that
                     // arrival before everyone's reads of the other partials

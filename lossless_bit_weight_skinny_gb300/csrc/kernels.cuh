@@ -36,6 +36,7 @@ struct GemmArgs {
     int x_ready;                   // x was complete before the previous launch: load it at once
     int out_mode;                  // kOutBF16 | kOutSiluMul
     int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
+    int defer;                     // split row blocks: leave the partials to sk_reduce_kernel
 };
 
 // Output modes.  kOutBF16: y holds BF16, each FP32 result rounded to the
@@ -103,20 +104,20 @@ __device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint3
 }
 
 // First iteration of CTA c when `iters` iterations are split over `grid` CTAs.
-__device__ __forceinline__ int sk_begin(int c, int grid, int iters)
+__host__ __device__ __forceinline__ int sk_begin(int c, int grid, int iters)
 {
     return static_cast<int>((static_cast<long long>(c) * iters) / grid);
 }
 
 // The CTA that owns iteration i.
-__device__ __forceinline__ int sk_owner(int i, int grid, int iters)
+__host__ __device__ __forceinline__ int sk_owner(int i, int grid, int iters)
 {
     return static_cast<int>((static_cast<long long>(i + 1) * grid + iters - 1) / iters) - 1;
 }
 
 // Partial slot of contributor c for row block rb (a CTA contributes to at most
 // two row blocks partially: the one it starts in and the one it ends in).
-__device__ __forceinline__ int sk_slot(int c, int rb, int grid, int iters, int n_kstep)
+__host__ __device__ __forceinline__ int sk_slot(int c, int rb, int grid, int iters, int n_kstep)
 {
     const int first_rb = sk_begin(c, grid, iters) / n_kstep;
     return 2 * c + (rb == first_rb ? 0 : 1);
@@ -169,12 +170,23 @@ __device__ __forceinline__ void report(int *status, int code)
 // is fixed, so results are bitwise reproducible, and many contributors cost
 // one round of loads instead of one per contributor.  EPI: the results go
 // through the output mode (emit_y); otherwise y is FP32 [M][N].
-template <bool EPI>
-__device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int rows_blk, int grid,
-                                                int c_first, int c_last, int tid, int nthreads)
+#ifndef W12_SK_UNROLL
+#define W12_SK_UNROLL 4 // partial loads in flight per lane
+#endif
+#ifndef W12_SK_NOINLINE
+#define W12_SK_NOINLINE 0
+#endif
+#if W12_SK_NOINLINE
+#define W12_SK_INL static __noinline__
+#else
+#define W12_SK_INL __forceinline__
+#endif
+template <bool EPI, int U = W12_SK_UNROLL>
+__device__ W12_SK_INL void sk_reduce_range(const GemmArgs &a, int rb, int rows_blk, int grid, int c_first,
+                                           int c_last, int tid, int nthreads, int g_lo, int g_hi)
 {
     const int row0 = rb * rows_blk;
-    const int groups = a.M * rows_blk / 4; // float4 groups per partial
+    const int groups = g_hi; // float4 groups [g_lo, g_hi) of the partial
     const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
     const float4 *base = reinterpret_cast<const float4 *>(a.partials);
     const int n_contrib = c_last - c_first + 1;
@@ -182,19 +194,19 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
     // row block, so their slot is 2c
     const int slot_first = sk_slot(c_first, rb, grid, a.total_iters, a.n_kstep);
     int P = 1;
-    while (P < 32 && P < n_contrib && 2 * P * groups <= nthreads)
+    while (P < 32 && P < n_contrib && 2 * P * (g_hi - g_lo) <= nthreads)
         P *= 2;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
     const int gpw = 32 / P; // groups per warp and pass
     const int j = lane % P;
-    for (int gbase = warp * gpw; gbase < groups; gbase += nwarps * gpw) {
+    for (int gbase = g_lo + warp * gpw; gbase < groups; gbase += nwarps * gpw) {
         const int g = gbase + lane / P;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (g < groups) {
-            for (int c0 = c_first + j; c0 <= c_last; c0 += 4 * P) {
-                float4 v[4];
+            for (int c0 = c_first + j; c0 <= c_last; c0 += U * P) {
+                float4 v[U];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < U; ++u) {
                     const int c = c0 + u * P;
                     if (c <= c_last) {
                         const int slot = (c == c_first) ? slot_first : 2 * c;
@@ -202,7 +214,7 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < U; ++u) {
                     if (c0 + u * P <= c_last) {
                         acc.x += v[u].x;
                         acc.y += v[u].y;
@@ -234,6 +246,14 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
     }
 }
 
+// The whole row block: every float4 group of its M x rows_blk partial.
+template <bool EPI>
+__device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int rows_blk, int grid, int c_first,
+                                                int c_last, int tid, int nthreads)
+{
+    sk_reduce_range<EPI>(a, rb, rows_blk, grid, c_first, c_last, tid, nthreads, 0, a.M * rows_blk / 4);
+}
+
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream is finishing; it calls
 // pdl_wait_prior_grid() before touching anything that kernel may write.
@@ -258,6 +278,10 @@ cudaError_t launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t 
 cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
                             const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                             cudaStream_t st);
+// Split-K fix-up as a kernel of its own (reduce.cu), chained after a
+// tensor-core GEMM launched with a.defer set; nothing is launched when no row
+// block is split.  *launched tells whether it was.
+cudaError_t launch_sk_reduce(const GemmArgs &a, int gemm_grid, int rows_blk, cudaStream_t st, bool *launched);
 cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                            cudaStream_t st);
@@ -290,6 +314,29 @@ constexpr int kTcRows = 128;
 #ifndef W12_GRID_ALIGNED
 #define W12_GRID_ALIGNED 1
 #endif
+// Smallest unit count per CTA of the tensor-core kernel: a 128 x 256 unit
+// reads 48 KB of W12 and a CTA's partial of a row block is M x 512 bytes, so
+// for large M fewer CTAs each stream several units per partial they write.
+//
+// Above W12_TC_DEFER_M rows, the tensor-core GEMM leaves split row blocks to
+// the separate fix-up kernel (reduce.cu), which reads the partials with many
+// CTAs; then the partials cost little and the unit floor is lower.  Measured
+// on GB300: at M = 128 a 1024 x 5120 GEMM takes 10.3 us that way against 23.2
+// us with the in-kernel fix-up; at M <= 32 the second launch costs 2-3 us
+// more than it saves.
+#ifndef W12_TC_DEFER_M
+#define W12_TC_DEFER_M 64
+#endif
+#ifndef W12_TC_PART_RATIO
+#define W12_TC_PART_RATIO 24
+#endif
+inline bool tc_defer(int M) { return M > W12_TC_DEFER_M; }
+inline int64_t tc_min_iters(int M)
+{
+    const int64_t ratio = tc_defer(M) ? 64 : W12_TC_PART_RATIO;
+    return std::max<int64_t>(1, (static_cast<int64_t>(M) + ratio - 1) / ratio);
+}
+
 inline int choose_grid(int64_t n_rowblk, int64_t n_kstep, int sms, int64_t min_iters)
 {
     const int64_t iters = n_rowblk * n_kstep;

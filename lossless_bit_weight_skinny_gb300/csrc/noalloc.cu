@@ -148,7 +148,7 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     a.n_rowblk = static_cast<int>(ceil_div(N, rows_blk));
     a.n_kstep = static_cast<int>(ceil_div(K, kstep));
     const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
-    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : W12_FMA_MIN_ITERS;
+    const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
     const int grid = choose_grid(a.n_rowblk, a.n_kstep, sms * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     // the fixed array must hold the counters and the partial sums of this call
@@ -159,6 +159,7 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     a.limit_ns = 200ull * 1000 * 1000;
     a.inject_stall = 0;
     a.x_ready = x_ready ? 1 : 0;
+    a.defer = tc && tc_defer(M);
 
     unsigned char *scratch = nullptr;
     const w12_status s = noalloc_setup(dev, &scratch);
@@ -176,8 +177,11 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     const w12_tmap &tb = tc ? w->tm_b_tc : (rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
     const CUtensorMap *pae = reinterpret_cast<const CUtensorMap *>(&tae);
     const CUtensorMap *pb = reinterpret_cast<const CUtensorMap *>(&tb);
-    const cudaError_t e = tc ? launch_gemm_tc(mt, false, a, pae, pb, &tmx, grid, st)
-                             : launch_gemm_fma(mt, false, a, pae, pb, &tmx, grid, st);
+    cudaError_t e = tc ? launch_gemm_tc(mt, false, a, pae, pb, &tmx, grid, st)
+                       : launch_gemm_fma(mt, false, a, pae, pb, &tmx, grid, st);
+    bool red = false;
+    if (e == cudaSuccess && a.defer)
+        e = launch_sk_reduce(a, grid, rows_blk, st, &red);
     return e == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 

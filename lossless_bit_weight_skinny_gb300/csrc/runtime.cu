@@ -206,10 +206,11 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     a.limit_ns = g_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
     a.x_ready = x_ready ? 1 : 0;
+    a.defer = tc && tc_defer(M);
     // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
     // streams several times the weight bytes of the partial sums it writes
     // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
-    const int64_t min_iters = tc ? std::max<int64_t>(1, (static_cast<int64_t>(M) + 23) / 24) : W12_FMA_MIN_ITERS;
+    const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
     const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur) * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
@@ -227,9 +228,12 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
         return W12_ERR_CUDA;
     }
     cudaError_t e;
-    if (tc)
+    if (tc) {
         e = launch_gemm_tc(mt, q8, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
-    else if (rows_blk == 128)
+        bool red = false;
+        if (e == cudaSuccess && a.defer)
+            e = launch_sk_reduce(a, grid, rows_blk, st, &red);
+    } else if (rows_blk == 128)
         e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma128), tmap_of(w->tm_b_fma128), &tmx, grid, st);
     else
         e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma64), tmap_of(w->tm_b_fma64), &tmx, grid, st);

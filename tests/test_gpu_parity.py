@@ -301,7 +301,7 @@ def test_gemm_host_entry(w12):
         _check(yh.numpy().astype(np.float64), x, Wdec, what=f"host entry M={M}")
 
 
-@pytest.mark.parametrize("M", (1, 16))
+@pytest.mark.parametrize("M", (1, 16, 128))
 def test_timeout_reports_and_recovers(w12, M):
     """A wait that nothing satisfies ends in W12_ERR_TIMEOUT, not a hang, and
     the next call on the same handle and workspace is correct again."""
