@@ -738,9 +738,10 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_case(case):
-    """A small profiling case: one 17408x5120 W12 matrix (134 MB, larger than
-    L2) and three launches of one kernel (for ncu captures)."""
+def run_case(cases):
+    """Small profiling cases: one 17408x5120 W12 matrix (134 MB, larger than
+    L2) and three launches of each named case's kernel, in order (for ncu
+    captures); `cases` is a comma-separated list."""
     import torch
 
     import __graft_entry__
@@ -751,14 +752,16 @@ def run_case(case):
     N, K = 17408, 5120
     wb = WL.projection_weights_torch(N, K, seed=5)
     d = w12.w12_upload(w12.w12_encode(wb.cpu().numpy().view(np.uint16)))
-    M = {"fma": 1, "fma2": 2, "fma4": 4, "tc16": 16, "tc32": 32, "tc": 64, "q8": 64, "q8m1": 1}[case]
-    x = torch.from_numpy(WL.activations(M, K, seed=1).view(np.int16)).cuda().view(torch.bfloat16)
-    fn = w12.w12_gemm_q8view if case.startswith("q8") else w12.w12_gemm
-    for _ in range(3):
-        y = fn(x, d)
-    torch.cuda.synchronize()
-    assert w12.w12_dev_status(d) == 0
-    print(case, "ok", float(y.abs().sum()))
+    rows = {"fma": 1, "fma2": 2, "fma4": 4, "tc16": 16, "tc32": 32, "tc": 64, "tc128": 128, "q8": 64, "q8m1": 1}
+    for case in cases.split(","):
+        M = rows[case]
+        x = torch.from_numpy(WL.activations(M, K, seed=1).view(np.int16)).cuda().view(torch.bfloat16)
+        fn = w12.w12_gemm_q8view if case.startswith("q8") else w12.w12_gemm
+        for _ in range(3):
+            y = fn(x, d)
+        torch.cuda.synchronize()
+        assert w12.w12_dev_status(d) == 0
+        print(case, "ok", float(y.abs().sum()))
 
 
 def main():
@@ -772,7 +775,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense BF16 (cuBLAS) comparison")
-    ap.add_argument("--case", default=None, help="profiling case: fma, fma2, fma4, tc16, tc32, tc, q8, q8m1")
+    ap.add_argument("--case", default=None,
+                    help="profiling cases, comma-separated: fma, fma2, fma4, tc16, tc32, tc (M=64), tc128, q8, q8m1")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
