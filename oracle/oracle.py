@@ -53,6 +53,12 @@ def _declare(lib):
     lib.orc_encoded_size.restype = _I64
     lib.orc_encode.argtypes = [_P, _I64, _I64, _P, _I64]
     lib.orc_encode.restype = _I64
+    lib.orc_encoded_size_count_max.argtypes = [_P, _I64, _I64]
+    lib.orc_encoded_size_count_max.restype = _I64
+    lib.orc_encode_count_max.argtypes = [_P, _I64, _I64, _P, _I64]
+    lib.orc_encode_count_max.restype = _I64
+    lib.orc_row_ebase_count_max.argtypes = [_P, _I64]
+    lib.orc_row_ebase_count_max.restype = ctypes.c_int
     lib.orc_blob_header.argtypes = [_P, _I64, _P]
     lib.orc_blob_header.restype = ctypes.c_int
     lib.orc_decode.argtypes = [_P, _I64, _P]
@@ -104,14 +110,17 @@ def _u16(a) -> np.ndarray:
     return a
 
 
-def encode(w_bits: np.ndarray, lib=None) -> bytes:
-    """W[N][K] (uint16 BF16 bits) -> W12 blob bytes."""
+def encode(w_bits: np.ndarray, lib=None, count_max: bool = False) -> bytes:
+    """W[N][K] (uint16 BF16 bits) -> W12 blob bytes; count_max selects the
+    count-maximising window (R13) instead of the max-anchored one (R1)."""
     lib = lib or _get()
     w = _u16(w_bits)
     N, K = w.shape
-    size = lib.orc_encoded_size(_ptr(w), N, K)
+    size_fn = lib.orc_encoded_size_count_max if count_max else lib.orc_encoded_size
+    enc_fn = lib.orc_encode_count_max if count_max else lib.orc_encode
+    size = size_fn(_ptr(w), N, K)
     out = np.zeros(max(size, 1), dtype=np.uint8)
-    n = lib.orc_encode(_ptr(w), N, K, _ptr(out), size)
+    n = enc_fn(_ptr(w), N, K, _ptr(out), size)
     if n != size:
         raise RuntimeError("oracle encode failed")
     return out[:size].tobytes()
@@ -192,10 +201,11 @@ def abs_gemm(x_bits: np.ndarray, w_bits: np.ndarray, lib=None) -> np.ndarray:
     return s
 
 
-def row_ebase(row_bits: np.ndarray, lib=None) -> int:
+def row_ebase(row_bits: np.ndarray, lib=None, count_max: bool = False) -> int:
     lib = lib or _get()
     r = _u16(row_bits).reshape(-1)
-    return int(lib.orc_row_ebase(_ptr(r), r.size))
+    fn = lib.orc_row_ebase_count_max if count_max else lib.orc_row_ebase
+    return int(fn(_ptr(r), r.size))
 
 
 def num_tiles(N: int, K: int, lib=None) -> int:

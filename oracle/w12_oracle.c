@@ -52,6 +52,16 @@
  *   R12 gated MLP: with the gate and up rows interleaved (row 2i = gate row i,
  *      row 2i+1 = up row i), h[m][i] = silu(y[m][2i]) * y[m][2i+1], where
  *      silu(g) = g / (1 + exp(-g)).
+ *
+ * Encoder option (the pages fix the max-anchored window, R1; this variant
+ * trades the top outliers of heavy-tailed rows for fewer escapes):
+ *   R13 count-maximising window: a row's window base is the b in [1, b1]
+ *      (b1 = the R1 base) whose 16 binades [b, b+15] hold the most finite
+ *      normal weights of the row, the largest such b on ties; weights above
+ *      the window then escape too, and their slot holds the saturated
+ *      placeholder A = s<<3 | 7, E = 15, B = 15 -- the window's largest
+ *      magnitude with the weight's sign -- so that the 8-bit view reads them
+ *      as the nearest value it can hold.  Decoding is unchanged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -138,6 +148,42 @@ int orc_row_ebase(const uint16_t *row, int64_t K)
     return emax - 15;
 }
 
+/* R13: the count-maximising window base of one row. */
+int orc_row_ebase_count_max(const uint16_t *row, int64_t K)
+{
+    int64_t count[256];
+    int64_t best = -1, c;
+    int b, e, best_b = 1, b1 = orc_row_ebase(row, K);
+    int64_t k;
+    for (e = 0; e < 256; e++)
+        count[e] = 0;
+    for (k = 0; k < K; k++)
+        if (is_finite_normal(row[k]))
+            count[bf16_exp(row[k])]++;
+    for (b = 1; b <= b1; b++) {
+        c = 0;
+        for (e = b; e <= b + 15; e++)
+            c += count[e];
+        if (c >= best) { /* ">=": the largest base among equal counts */
+            best = c;
+            best_b = b;
+        }
+    }
+    return best_b;
+}
+
+/* Window base of a row under the chosen rule (0: R1, 1: R13). */
+static int row_base(const uint16_t *row, int64_t K, int count_max)
+{
+    return count_max ? orc_row_ebase_count_max(row, K) : orc_row_ebase(row, K);
+}
+
+/* R13: a finite normal weight above the window (never under R1). */
+static int above_window(uint16_t b, int ebase)
+{
+    return is_finite_normal(b) && bf16_exp(b) > ebase + 15;
+}
+
 /* R1 + R3: does weight `b` of a row with window base `ebase` fit the window? */
 static int in_window(uint16_t b, int ebase)
 {
@@ -150,6 +196,8 @@ static int field_A(uint16_t b, int ebase)
 {
     if (in_window(b, ebase))
         return (bf16_sign(b) << 3) | (bf16_mant(b) >> 4);
+    if (above_window(b, ebase))
+        return (bf16_sign(b) << 3) | 7; /* R13 saturated placeholder */
     return bf16_sign(b) << 3; /* R4 placeholder */
 }
 
@@ -157,6 +205,8 @@ static int field_E(uint16_t b, int ebase)
 {
     if (in_window(b, ebase))
         return bf16_exp(b) - ebase;
+    if (above_window(b, ebase))
+        return 15;
     return 0;
 }
 
@@ -164,6 +214,8 @@ static int field_B(uint16_t b, int ebase)
 {
     if (in_window(b, ebase))
         return bf16_mant(b) & 0xF;
+    if (above_window(b, ebase))
+        return 15;
     return 0;
 }
 
@@ -175,11 +227,11 @@ static int b_slot_of(int k8)
     return 4 + (k8 - 1) / 2;   /* odds in slots 4..7 */
 }
 
-static int64_t count_escapes(const uint16_t *w, int64_t N, int64_t K)
+static int64_t count_escapes(const uint16_t *w, int64_t N, int64_t K, int count_max)
 {
     int64_t n, k, count = 0;
     for (n = 0; n < N; n++) {
-        int ebase = orc_row_ebase(w + n * K, K);
+        int ebase = row_base(w + n * K, K, count_max);
         for (k = 0; k < K; k++)
             if (!in_window(w[n * K + k], ebase))
                 count++;
@@ -187,19 +239,32 @@ static int64_t count_escapes(const uint16_t *w, int64_t N, int64_t K)
     return count;
 }
 
-/* Size in bytes of the blob that orc_encode writes for this matrix. */
-int64_t orc_encoded_size(const uint16_t *w, int64_t N, int64_t K)
+static int64_t encoded_size(const uint16_t *w, int64_t N, int64_t K, int count_max)
 {
     int64_t T = orc_num_tiles(N, K);
     return ORC_HEADER_BYTES + N + N * K + N * orc_b_row_bytes(K) + 4 * (T + 1) +
-           4 * count_escapes(w, N, K);
+           4 * count_escapes(w, N, K, count_max);
+}
+
+/* Size in bytes of the blob that orc_encode writes for this matrix. */
+int64_t orc_encoded_size(const uint16_t *w, int64_t N, int64_t K)
+{
+    return encoded_size(w, N, K, 0);
+}
+
+/* The same for orc_encode_count_max. */
+int64_t orc_encoded_size_count_max(const uint16_t *w, int64_t N, int64_t K)
+{
+    return encoded_size(w, N, K, 1);
 }
 
 /*
- * Encode W[N][K] (BF16 bit patterns, row-major) into a W12 blob (R8).
- * Returns the blob length, or -1 if `cap` is too small / arguments are bad.
+ * Encode W[N][K] (BF16 bit patterns, row-major) into a W12 blob (R8), with
+ * the R1 window (count_max = 0) or the R13 one.  Returns the blob length, or
+ * -1 if `cap` is too small / arguments are bad.
  */
-int64_t orc_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap)
+static int64_t encode_with(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap,
+                           int count_max)
 {
     int64_t T, tiles_c, n_esc, len, n, k, t;
     int64_t off_ebase, off_ae, off_b, off_ptr, off_esc, brow;
@@ -207,12 +272,12 @@ int64_t orc_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64
 
     if (N < 0 || K < 0)
         return -1;
-    len = orc_encoded_size(w, N, K);
+    len = encoded_size(w, N, K, count_max);
     if (len > cap)
         return -1;
     T = orc_num_tiles(N, K);
     tiles_c = (K + ORC_TILE_COLS - 1) / ORC_TILE_COLS;
-    n_esc = count_escapes(w, N, K);
+    n_esc = count_escapes(w, N, K, count_max);
     brow = orc_b_row_bytes(K);
 
     off_ebase = ORC_HEADER_BYTES;
@@ -235,7 +300,7 @@ int64_t orc_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64
 
     /* per-channel window base (R1) */
     for (n = 0; n < N; n++) {
-        ebase[n] = orc_row_ebase(w + n * K, K);
+        ebase[n] = row_base(w + n * K, K, count_max);
         blob[off_ebase + n] = (uint8_t)ebase[n];
     }
 
@@ -278,6 +343,17 @@ int64_t orc_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64
     }
     free(ebase);
     return len;
+}
+
+int64_t orc_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap)
+{
+    return encode_with(w, N, K, blob, cap, 0);
+}
+
+/* R13: the same blob layout with the count-maximising window. */
+int64_t orc_encode_count_max(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap)
+{
+    return encode_with(w, N, K, blob, cap, 1);
 }
 
 /* Read the header: out[0..3] = N, K, n_esc, T.  Returns 0, or -1 if malformed. */

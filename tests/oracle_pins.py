@@ -265,6 +265,99 @@ def pin_gemm_exact_integers(lib=None):
         assert y[1, n] == float(sum(-v[k] if k % 2 == 0 else v[k] for k in range(K)))
 
 
+# ---- count-maximising window (encoder option) ------------------------------------
+
+def _brute_count_max_base(row):
+    """The rule written out directly: every base b from 1 up to the
+    max-anchored one, counting the row's finite normal weights whose exponent
+    lies in [b, b + 15]; the largest b with the most."""
+    e = [(int(v) >> 7) & 0xFF for v in row]
+    normal = [x for x in e if 1 <= x <= 254]
+    b1 = max(max(normal, default=0), 16) - 15
+    best, best_b = -1, 1
+    for b in range(1, b1 + 1):
+        c = sum(1 for x in normal if b <= x <= b + 15)
+        if c >= best:
+            best, best_b = c, b
+    return best_b
+
+
+def pin_count_max_window(lib=None):
+    """Window bases against the brute-force rule on constructed and random
+    rows, and the escape count never above the max-anchored one."""
+    rng = np.random.Generator(np.random.PCG64(93))
+    rows = [
+        np.zeros(64, dtype=np.uint16),                      # no normal weight: b = 1
+        np.array([0x7F80, 0x3F80, 0x0001] * 8, dtype=np.uint16),
+        np.array([0x7F7F] + [0x3F80] * 40, dtype=np.uint16),  # one huge outlier: the window drops
+        np.array([0x7F7F] * 40 + [0x3F80] * 40, dtype=np.uint16),  # a tie: the higher window
+        np.array([(e << 7) for e in range(1, 255)], dtype=np.uint16),  # one of every exponent
+        np.array([(e << 7) | 0x8000 for e in range(100, 140)] * 3 + [200 << 7], dtype=np.uint16),
+    ]
+    for i in range(40):
+        centre = int(rng.integers(20, 230))
+        e = np.clip(rng.normal(centre, rng.uniform(2, 20), size=97).round(), 0, 255).astype(np.uint16)
+        rows.append(((rng.integers(0, 2, 97).astype(np.uint16) << 15) | (e << 7)
+                     | rng.integers(0, 128, 97).astype(np.uint16)).astype(np.uint16))
+    for r in rows:
+        got = O.row_ebase(r, lib=lib, count_max=True)
+        assert got == _brute_count_max_base(r), (got, _brute_count_max_base(r), r[:8])
+    # the outlier row keeps 1.0 (exponent 127) in its window and lets 2^127 escape
+    b = O.row_ebase(rows[2], lib=lib, count_max=True)
+    assert b <= 127 <= b + 15 and b + 15 < 254
+    W = WL.heavy_weights(64, 1024, seed=94)
+    for n in range(64):
+        bm = O.row_ebase(W[n], lib=lib)
+        bc = O.row_ebase(W[n], lib=lib, count_max=True)
+        e = (W[n].astype(np.int32) >> 7) & 0xFF
+        normal = (e >= 1) & (e <= 254)
+        assert np.sum(normal & (e >= bc) & (e <= bc + 15)) >= np.sum(normal & (e >= bm) & (e <= bm + 15))
+
+
+def pin_count_max_encoding(lib=None):
+    """Blobs with the count-maximising window: lossless; weights above the
+    window escape with the saturated placeholder (A = s<<3|7, E = 15, B = 15),
+    which the 8-bit view reads as +-1.875 * 2^(ebase+15-127); weights below it
+    keep the ordinary placeholder; fewer escapes on heavy tails."""
+    W = WL.projection_weights(96, 520, seed=95, outlier_frac=5e-3)
+    W[3, 7] = 0x7F7F   # huge, positive
+    W[4, 9] = 0xFF00   # huge, negative
+    W[5, :] = 0x3F80   # a flat row: every weight in one binade
+    blob = O.encode(W, lib=lib, count_max=True)
+    N, K, n_esc, T = O.blob_header(blob, lib=lib)
+    assert np.array_equal(O.decode(blob, lib=lib), W)
+    ebase, ae, bpl, tptr, esc = _blob_arrays(blob, N, K)
+    e = (W.astype(np.int32) >> 7) & 0xFF
+    eb = ebase.astype(np.int32)[:, None]
+    normal = (e >= 1) & (e <= 254)
+    inwin = normal & (e >= eb) & (e <= eb + 15)
+    above = normal & (e > eb + 15)
+    assert above[3, 7] and above[4, 9] and above.sum() >= 2
+    s = (W.astype(np.int32) >> 15)
+    assert np.array_equal(ae[above].astype(np.int32), (s[above] << 7) | 0x7F)
+    below = ~inwin & ~above
+    assert np.array_equal(ae[below].astype(np.int32), s[below] << 7)
+    kk = np.arange(K)
+    slot = np.where(kk % 2 == 1, 4 + kk % 8 // 2, kk % 8 // 2)
+    words = bpl.reshape(N, -1).view("<u4")
+    nib = (words[:, kk // 8] >> (4 * slot)) & 0xF
+    assert np.all(nib[above] == 15) and np.all(nib[below] == 0)
+    assert n_esc == int((~inwin).sum())
+    q8 = O.decode_q8(blob, lib=lib).astype(np.int32)
+    assert np.array_equal(q8[above], (s[above] << 15) | ((eb + 15) * np.ones_like(e))[above] << 7 | 0x70)
+    # max-anchored blobs of the same matrix have no weight above the window
+    blob1 = O.encode(W, lib=lib)
+    e1 = O.blob_header(blob1, lib=lib)[2]
+    assert n_esc <= e1
+    H = WL.heavy_weights(128, 2048, seed=96)
+    f_max = O.blob_header(O.encode(H, lib=lib), lib=lib)[2] / H.size
+    f_cnt = O.blob_header(O.encode(H, lib=lib, count_max=True), lib=lib)[2] / H.size
+    assert f_cnt < 0.4 * f_max, (f_cnt, f_max)
+    pats = np.random.Generator(np.random.PCG64(97)).permutation(
+        np.arange(65536, dtype=np.uint32)).astype(np.uint16).reshape(8, 8192)
+    assert np.array_equal(O.decode(O.encode(pats, lib=lib, count_max=True), lib=lib), pats)
+
+
 # ---- epilogues: BF16 output and the gated-MLP product ----------------------------
 
 def _f32(bits):
@@ -407,4 +500,6 @@ FAST_PINS = (
     pin_gemm_exact_integers,
     pin_round_bf16,
     pin_silu_mul,
+    pin_count_max_window,
+    pin_count_max_encoding,
 )

@@ -51,6 +51,17 @@ MUTANTS = [
      "h[m * (N / 2) + i] = u / (1.0 + exp(-u)) * g;"),
     ("silu_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
     ("silu_pairs_shifted", "u = y[m * N + 2 * i + 1];", "u = y[m * N + (2 * i + 3) % N];"),
+    ("count_max_ties_low", "if (c >= best) {", "if (c > best) {"),
+    ("count_max_window_15_binades", "for (e = b; e <= b + 15; e++)\n            c += count[e];",
+     "for (e = b; e <= b + 14; e++)\n            c += count[e];"),
+    ("count_max_search_short", "for (b = 1; b <= b1; b++) {", "for (b = 1; b < b1; b++) {"),
+    ("saturated_A_missing", "return (bf16_sign(b) << 3) | 7; /* R13 saturated placeholder */",
+     "return bf16_sign(b) << 3;"),
+    ("saturated_E_zero", "    if (above_window(b, ebase))\n        return 15;\n    return 0;\n}\n\nstatic int field_B",
+     "    if (above_window(b, ebase))\n        return 0;\n    return 0;\n}\n\nstatic int field_B"),
+    ("saturated_B_zero", "        return 15;\n    return 0;\n}\n\n/* R6", "        return 0;\n    return 0;\n}\n\n/* R6"),
+    ("above_one_binade_late", "return is_finite_normal(b) && bf16_exp(b) > ebase + 15;",
+     "return is_finite_normal(b) && bf16_exp(b) > ebase + 16;"),
 ]
 
 
