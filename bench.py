@@ -360,15 +360,21 @@ def run_w12(args):
     # Two-level-verification pair on a 17408x5120 matrix: the Q pass over the
     # 8-bit view at M = 64 (draft-tree nodes), then the exact pass at M = 16, for
     # the projection draw (the gate projection of the first layer) and for a
-    # heavy-tailed draw (Student-t 1.5, ~1e-2 escapes).
+    # heavy-tailed draw (Student-t 1.5, ~1e-2 escapes), the latter also with
+    # count-maximising windows (~2e-3 escapes; the top outliers escape instead).
     tlv = {}
-    hheavy = w12.w12_encode(WL.heavy_weights(17408, 5120, seed=31))
+    heavy_w = WL.heavy_weights(17408, 5120, seed=31)
+    hheavy = w12.w12_encode(heavy_w)
     wheavy = w12.w12_upload(hheavy)
+    hheavy_cm = w12.w12_encode(heavy_w, count_max=True)
+    wheavy_cm = w12.w12_upload(hheavy_cm)
+    del heavy_w
     x64 = torch.from_numpy(WL.activations(64, 5120, seed=41).view(np.int16)).cuda().view(torch.bfloat16)
     x16 = torch.from_numpy(WL.activations(16, 5120, seed=42).view(np.int16)).cuda().view(torch.bfloat16)
     y64 = torch.empty((64, 17408), dtype=torch.float32, device="cuda")
     y16 = torch.empty((16, 17408), dtype=torch.float32, device="cuda")
-    for dist_name, dm in (("projection", layers[0][4][1]), ("heavy_tail", wheavy)):
+    for dist_name, dm in (("projection", layers[0][4][1]), ("heavy_tail", wheavy),
+                          ("heavy_tail_count_max_windows", wheavy_cm)):
         def run(kind, dm=dm):
             if kind in ("q8", "pair"):
                 w12.w12_gemm_ex(x64, dm, y64, stream, q8view=True)
@@ -397,7 +403,10 @@ def run_w12(args):
         res["q8_view_GBps"] = round((17408 * 5120 + 2 * 64 * 5120 + 4 * 64 * 17408) / (res["q8_us"] * 1e3), 1)
         tlv[dist_name] = res
     tlv["escape_fraction_heavy_tail"] = round(hheavy.stats()["escape_fraction"], 5)
-    del hheavy
+    tlv["escape_fraction_heavy_tail_count_max_windows"] = round(hheavy_cm.stats()["escape_fraction"], 5)
+    del hheavy, hheavy_cm
+    wheavy.free()
+    wheavy_cm.free()
 
     # Fused projections (the same bytes, merged at encode time): q/k/v stacked
     # into one 7168x5120 matrix and gate/up interleaved by rows into one

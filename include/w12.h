@@ -87,6 +87,30 @@ const char *w12_status_string(w12_status s);
 w12_status w12_encode(const uint16_t *w_bf16, int64_t N, int64_t K, int n_threads,
                       w12_host **out);
 
+/* Flags of w12_encode_ex / w12_encode_device_ex. */
+enum {
+    W12_ENCODE_COUNT_MAX = 1 /* count-maximising windows instead of max-anchored ones */
+};
+
+/*
+ * w12_encode with flags (an unknown bit gives INVALID_ARG).
+ *
+ * W12_ENCODE_COUNT_MAX chooses each row's window as the 16 binades holding
+ * the most of its finite normal weights -- the highest such window at or
+ * below the max-anchored one -- instead of the window topped by the row's
+ * largest weight [F5a].  On heavy-tailed rows this trades a few top outliers
+ * for many fewer escapes (Student-t(1.5) weights: about 1e-2 -> 2e-3).  The
+ * weights above the window escape too; their slot holds the saturated
+ * placeholder A = s<<3 | 7, E = 15, B = 15, the window's largest magnitude
+ * with the weight's sign, which is what the Q pass reads for them.  The
+ * stored format, decoding and the exact GEMM are the same: the blob records
+ * each row's base, and w12_validate accepts both placeholders.  (The pages'
+ * encoder anchors the window at the maximum; this option is a library
+ * extension.)
+ */
+w12_status w12_encode_ex(const uint16_t *w_bf16, int64_t N, int64_t K, int n_threads, unsigned flags,
+                         w12_host **out);
+
 void w12_host_free(w12_host *h);
 
 /* Storage statistics of an encoded matrix [MF "W12 compression"]. */
@@ -140,6 +164,11 @@ void w12_dev_free(w12_dev *d);
  * INVALID_ARG, UNSUPPORTED (N or K above 2^31), OOM, CUDA.
  */
 w12_status w12_encode_device(const void *w_bf16, int64_t N, int64_t K, w12_stream_t stream, w12_dev **out);
+
+/* w12_encode_device with the flags of w12_encode_ex; the arrays are
+ * byte-identical to w12_encode_ex's with the same flags. */
+w12_status w12_encode_device_ex(const void *w_bf16, int64_t N, int64_t K, unsigned flags, w12_stream_t stream,
+                                w12_dev **out);
 
 /*
  * Copy a device handle's arrays back into a new host handle (for

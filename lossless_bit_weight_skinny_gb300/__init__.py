@@ -66,6 +66,7 @@ def _sig(name, args, res=_ST):
 
 _sig("w12_status_string", [_ST], ctypes.c_char_p)
 _sig("w12_encode", [_P, _I64, _I64, _I, ctypes.POINTER(_P)])
+_sig("w12_encode_ex", [_P, _I64, _I64, _I, ctypes.c_uint, ctypes.POINTER(_P)])
 _sig("w12_host_free", [_P], None)
 _sig("w12_host_stats", [_P, ctypes.POINTER(Stats)])
 _sig("w12_host_view", [_P] + [ctypes.POINTER(_P)] * 5)
@@ -77,6 +78,7 @@ _sig("w12_load", [ctypes.c_char_p, ctypes.POINTER(_P)])
 _sig("w12_upload", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_free", [_P], None)
 _sig("w12_encode_device", [_P, _I64, _I64, _P, ctypes.POINTER(_P)])
+_sig("w12_encode_device_ex", [_P, _I64, _I64, ctypes.c_uint, _P, ctypes.POINTER(_P)])
 _sig("w12_download", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
@@ -97,13 +99,14 @@ EXPORTED = (
     "w12_dev_free", "w12_dev_info", "w12_gemm", "w12_gemm_q8view", "w12_gemm_host",
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
-    "w12_encode_device", "w12_download",
+    "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
 )
 
 W12_GEMM_Q8VIEW = 1
 W12_GEMM_INPUT_READY = 2
 W12_GEMM_OUT_BF16 = 4
 W12_GEMM_SILU_MUL = 8
+W12_ENCODE_COUNT_MAX = 1
 
 
 class W12Error(RuntimeError):
@@ -232,11 +235,14 @@ def _stream_ptr(stream):
 
 # ---- the C ABI, one Python function per entry point -------------------------
 
-def w12_encode(w_bits, n_threads: int = 0) -> Host:
+def w12_encode(w_bits, n_threads: int = 0, count_max: bool = False) -> Host:
+    """Encode host BF16 bit patterns [N][K]; count_max selects count-maximising
+    windows (W12_ENCODE_COUNT_MAX) instead of max-anchored ones."""
     a = _u16_host(w_bits)
     N, K = a.shape
     out = _P()
-    _check(_lib.w12_encode(a.ctypes.data_as(_P), N, K, n_threads, ctypes.byref(out)), "w12_encode")
+    flags = W12_ENCODE_COUNT_MAX if count_max else 0
+    _check(_lib.w12_encode_ex(a.ctypes.data_as(_P), N, K, n_threads, flags, ctypes.byref(out)), "w12_encode")
     return Host(out.value, N, K)
 
 
@@ -265,17 +271,19 @@ def w12_upload(h: Host, stream=None) -> Dev:
     return Dev(out.value, h.N, h.K, host=h)
 
 
-def w12_encode_device(w, stream=None) -> Dev:
+def w12_encode_device(w, stream=None, count_max: bool = False) -> Dev:
     """Encode a CUDA tensor of BF16 weights [N][K] (bfloat16 or its int16 /
-    uint16 bit view) on the device; the arrays equal w12_upload(w12_encode(w))."""
+    uint16 bit view) on the device; the arrays equal
+    w12_upload(w12_encode(w, count_max=count_max))."""
     import torch
     if not (isinstance(w, torch.Tensor) and w.is_cuda and w.dim() == 2 and w.is_contiguous() and w.element_size() == 2
             and w.dtype in (torch.bfloat16, torch.int16, torch.uint16)):
         raise TypeError("w must be a contiguous CUDA [N][K] tensor of BF16 (or its 16-bit pattern)")
     N, K = w.shape
     out = _P()
-    _check(_lib.w12_encode_device(ctypes.c_void_p(w.data_ptr()), N, K, _stream_ptr(stream), ctypes.byref(out)),
-           "w12_encode_device")
+    flags = W12_ENCODE_COUNT_MAX if count_max else 0
+    _check(_lib.w12_encode_device_ex(ctypes.c_void_p(w.data_ptr()), N, K, flags, _stream_ptr(stream),
+                                     ctypes.byref(out)), "w12_encode_device")
     return Dev(out.value, N, K)
 
 

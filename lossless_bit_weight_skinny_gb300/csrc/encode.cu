@@ -7,11 +7,16 @@
 // exponent field), B = mantissa bits 3..0; zeros, subnormals, Inf, NaN and
 // anything below the window are escapes, listed per 128 x 256 tile as
 // (row % 128) << 24 | (k % 256) << 16 | bits in (row, k) order, their slot
-// holding A = s << 3, E = 0, B = 0.  The arrays come out byte-identical to the
-// host encoder's.
+// holding A = s << 3, E = 0, B = 0.  With W12_ENCODE_COUNT_MAX a row's window
+// is the one holding the most finite normal weights (the highest such base at
+// or below the max-anchored one), and weights above it escape with the
+// saturated placeholder A = s << 3 | 7, E = 15, B = 15.  The arrays come out
+// byte-identical to the host encoder's with the same flags.
 //
 // Three passes over the weights:
-//   1. window bases: one warp per row, maximum exponent field below 255;
+//   1. window bases: one warp per row, maximum exponent field below 255 (and
+//      for count-maximising windows an exponent histogram in shared memory,
+//      then the best 16-binade window sum, one candidate base per lane);
 //   2. escape counts: one CTA per tile, counts per 8-row group;
 //   3. (after an exclusive prefix of the tile counts, and the allocation of
 //      the handle, whose size depends on the total) the AE and B planes and
@@ -36,24 +41,60 @@ __device__ __forceinline__ bool is_escape(uint32_t bits, uint32_t eb)
 
 // 1. ebase[n] for every row.
 __global__ void __launch_bounds__(kEncThreads) enc_rows_kernel(const uint16_t *w, int64_t N, int64_t K,
-                                                               uint8_t *ebase)
+                                                               uint8_t *ebase, int count_max)
 {
+    __shared__ uint32_t hist_s[kEncThreads / 32][256];
     const int64_t n = static_cast<int64_t>(blockIdx.x) * (kEncThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= N)
         return;
     const uint16_t *row = w + n * K;
+    uint32_t *hist = hist_s[threadIdx.x >> 5];
+    if (count_max) {
+        for (int e = lane; e < 256; e += 32)
+            hist[e] = 0;
+        __syncwarp();
+    }
     uint32_t emax = 16; // floor: ebase >= 1 even for rows without normals
     for (int64_t k = lane; k < K; k += 32) {
         const uint32_t e = (row[k] >> 7) & 0xFFu;
         if (e != 0xFFu && e > emax)
             emax = e;
+        if (count_max && e != 0 && e != 0xFFu)
+            atomicAdd(hist + e, 1u);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
         emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    uint32_t eb = emax - 15;
+    if (count_max) {
+        __syncwarp();
+        // lane l tries bases l + 1, l + 33, ... up to the max-anchored one; the
+        // best (count, base) pair wins, higher base on equal counts
+        uint32_t best = 0, best_b = 0;
+        for (uint32_t b = lane + 1; b <= eb; b += 32) {
+            uint32_t c = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                c += hist[b + i];
+            if (best_b == 0 || c >= best) {
+                best = c;
+                best_b = b;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const uint32_t oc = __shfl_xor_sync(0xffffffffu, best, o);
+            const uint32_t ob = __shfl_xor_sync(0xffffffffu, best_b, o);
+            if (ob != 0 && (best_b == 0 || oc > best || (oc == best && ob > best_b))) {
+                best = oc;
+                best_b = ob;
+            }
+        }
+        eb = best_b;
+    }
     if (lane == 0)
-        ebase[n] = static_cast<uint8_t>(emax - 15);
+        ebase[n] = static_cast<uint8_t>(eb);
 }
 
 // Escape mask of the (up to) 8 weights of group g of row n (bit j: weight 8g+j),
@@ -242,7 +283,13 @@ __global__ void __launch_bounds__(kEncThreads) enc_fill_kernel(const uint16_t *w
             const uint32_t bits = v[j];
             const uint32_t s = bits >> 15;
             if ((m >> j) & 1u) {
-                a8[j] = static_cast<uint8_t>((s << 3) << 4); // placeholder A = s << 3, E = 0, B = 0
+                // placeholder A = s << 3, E = 0, B = 0; above the window (count-
+                // maximising windows only) the saturated A = s << 3 | 7, E = 15, B = 15
+                const uint32_t e = (bits >> 7) & 0xFFu;
+                const bool above = e != 0xFFu && e > eb + 15u;
+                a8[j] = static_cast<uint8_t>(above ? ((s << 7) | 0x7Fu) : ((s << 3) << 4));
+                if (above)
+                    bword |= 0xFu << (4 * ((j >> 1) + 4 * (j & 1)));
                 esc[pos++] = (static_cast<uint32_t>(r) << 24) | (static_cast<uint32_t>((8 * g + j) % kTileCols) << 16) | bits;
             } else {
                 const uint32_t e = (bits >> 7) & 0xFFu, mant = bits & 0x7Fu;
@@ -266,7 +313,13 @@ using namespace w12;
 extern "C" w12_status w12_encode_device(const void *w_bf16, int64_t N, int64_t K, w12_stream_t stream,
                                          w12_dev **out)
 {
-    if (!out || N < 0 || K < 0 || (N * K > 0 && !w_bf16))
+    return w12_encode_device_ex(w_bf16, N, K, 0, stream, out);
+}
+
+extern "C" w12_status w12_encode_device_ex(const void *w_bf16, int64_t N, int64_t K, unsigned flags,
+                                            w12_stream_t stream, w12_dev **out)
+{
+    if (!out || N < 0 || K < 0 || (N * K > 0 && !w_bf16) || (flags & ~static_cast<unsigned>(W12_ENCODE_COUNT_MAX)))
         return W12_ERR_INVALID_ARG;
     *out = nullptr;
     if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
@@ -290,7 +343,8 @@ extern "C" w12_status w12_encode_device(const void *w_bf16, int64_t N, int64_t K
     w12_status res = W12_OK;
     uint32_t total = 0;
     if (N > 0)
-        enc_rows_kernel<<<static_cast<unsigned>(ceil_div(N, kEncThreads / 32)), kEncThreads, 0, st>>>(w, N, K, eb_s);
+        enc_rows_kernel<<<static_cast<unsigned>(ceil_div(N, kEncThreads / 32)), kEncThreads, 0, st>>>(
+            w, N, K, eb_s, (flags & W12_ENCODE_COUNT_MAX) ? 1 : 0);
     if (T > 0) {
         enc_count_kernel<<<static_cast<unsigned>(T), kEncThreads, 0, st>>>(w, N, K, tiles_c, eb_s, cnt_s);
         enc_scan_kernel<<<1, 1024, 0, st>>>(cnt_s, T, ptr_s);

@@ -18,7 +18,8 @@
 // registers until the row block ends, then the warp reduces across lanes.
 //
 // Escapes: the main loop multiplies every slot as decoded -- an escaped slot
-// holds the placeholder +-2^(ebase-127) -- and has no branches and no escape
+// holds the placeholder +-2^(ebase-127), or the saturated one above a
+// count-maximising window -- and has no branches and no escape
 // work at all.  The escape warps (even and odd units) walk each stage's list
 // and keep, per output, the two correction sums sum(-x * placeholder) and
 // sum(x * exact value) in shared memory; the consumers add them to the output
@@ -206,7 +207,13 @@ __device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *li
         rr[u] = r;
         const uint32_t k8 = (e >> 16) & 0xFFu;
         const uint32_t eb = in[u] ? eb_s[r] : 0u;
-        const float wph = __uint_as_float(((e & 0x8000u) << 16) | (eb << 23));
+        // the slot's placeholder: +-2^(ebase-127), or, for a finite weight
+        // above the window (count-maximising windows), the saturated
+        // +-(2 - 2^-7) * 2^(ebase+15-127)
+        const uint32_t ex = (e >> 7) & 0xFFu;
+        const bool above = ex != 0xFFu && ex > eb + 15u;
+        const float wph = __uint_as_float(((e & 0x8000u) << 16) |
+                                          (above ? (((eb + 15u) << 23) | (0x7Fu << 16)) : (eb << 23)));
         const float wex = __uint_as_float((e & 0xFFFFu) << 16);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {

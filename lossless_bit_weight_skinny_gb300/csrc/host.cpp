@@ -12,6 +12,13 @@
 // in per-(128 x 256)-tile lists, each sorted; the escaped slot keeps A = s << 3,
 // E = 0, B = 0.  Lossless by construction (AI summary page, Main Findings,
 // "W12 compression").
+//
+// Encoder option W12_ENCODE_COUNT_MAX: the window of a row is instead the one
+// holding the most finite normal weights (the highest such base at or below
+// the max-anchored one); weights above it escape as well, their slot holding
+// the saturated placeholder A = s << 3 | 7, E = 15, B = 15 (the window's
+// largest magnitude with the weight's sign, what the 8-bit view then reads).
+// Decoding is the same for both.
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
@@ -37,6 +44,38 @@ int row_window_base(const uint16_t *row, int64_t K)
     return static_cast<int>(emax) - 15;
 }
 
+// Count-maximising window base: the base b <= the max-anchored one whose 16
+// binades [b, b + 15] hold the most finite normal weights of the row, the
+// highest on ties (a sliding sum over the exponent histogram).
+int row_window_base_count_max(const uint16_t *row, int64_t K)
+{
+    uint32_t cnt[256] = {};
+    uint32_t emax = 16;
+    for (int64_t k = 0; k < K; ++k) {
+        const uint32_t e = (row[k] >> 7) & 0xFFu;
+        if (e != 0 && e != 0xFFu) {
+            ++cnt[e];
+            if (e > emax)
+                emax = e;
+        }
+    }
+    const int b1 = static_cast<int>(emax) - 15;
+    uint64_t win = 0;
+    for (int e = 1; e <= 16; ++e)
+        win += cnt[e];
+    uint64_t best = win;
+    int best_b = 1;
+    for (int b = 2; b <= b1; ++b) {
+        win += cnt[b + 15];
+        win -= cnt[b - 1];
+        if (win >= best) {
+            best = win;
+            best_b = b;
+        }
+    }
+    return best_b;
+}
+
 struct BlockOut {
     // escape entries of one 128-row block, one list per column tile
     std::vector<std::vector<uint32_t>> per_tile;
@@ -44,13 +83,13 @@ struct BlockOut {
 
 // Encode rows [r0, r1) (inside one 128-row block) of W into the planes.
 void encode_block(const uint16_t *w, int64_t K, int64_t r0, int64_t r1, w12_host *h,
-                  BlockOut *out)
+                  BlockOut *out, bool count_max)
 {
     const int64_t brow = b_row_bytes(K);
     const int64_t groups = ceil_div(K, 8);
     for (int64_t n = r0; n < r1; ++n) {
         const uint16_t *row = w + n * K;
-        const int eb = row_window_base(row, K);
+        const int eb = count_max ? row_window_base_count_max(row, K) : row_window_base(row, K);
         h->ebase[n] = static_cast<uint8_t>(eb);
         uint8_t *ae_row = h->ae.data() + n * K;
         uint8_t *b_row = h->b.data() + n * brow;
@@ -69,7 +108,14 @@ void encode_block(const uint16_t *w, int64_t K, int64_t r0, int64_t r1, w12_host
                     const uint32_t slot = (j & 1) ? 4 + (j >> 1) : (j >> 1);
                     bword |= (bits & 0xFu) << (4 * slot);
                 } else {
-                    ae_row[k] = static_cast<uint8_t>(s << 7);
+                    // above the window (count-maximising windows only): the
+                    // saturated placeholder; otherwise A = s << 3, E = 0, B = 0
+                    const bool above = e != 0xFFu && e > static_cast<uint32_t>(eb) + 15u;
+                    ae_row[k] = static_cast<uint8_t>(above ? ((s << 7) | 0x7Fu) : (s << 7));
+                    if (above) {
+                        const uint32_t slot = (j & 1) ? 4 + (j >> 1) : (j >> 1);
+                        bword |= 0xFu << (4 * slot);
+                    }
                     out->per_tile[k / kTileCols].push_back(
                         (static_cast<uint32_t>(n % kTileRows) << 24) |
                         (static_cast<uint32_t>(k % kTileCols) << 16) | bits);
@@ -153,8 +199,15 @@ const char *w12_status_string(w12_status s)
 w12_status w12_encode(const uint16_t *w_bf16, int64_t N, int64_t K, int n_threads,
                       w12_host **out)
 {
-    if (!out || N < 0 || K < 0 || (!w_bf16 && N * K > 0))
+    return w12_encode_ex(w_bf16, N, K, n_threads, 0, out);
+}
+
+w12_status w12_encode_ex(const uint16_t *w_bf16, int64_t N, int64_t K, int n_threads, unsigned flags,
+                         w12_host **out)
+{
+    if (!out || N < 0 || K < 0 || (!w_bf16 && N * K > 0) || (flags & ~static_cast<unsigned>(W12_ENCODE_COUNT_MAX)))
         return W12_ERR_INVALID_ARG;
+    const bool count_max = (flags & W12_ENCODE_COUNT_MAX) != 0;
     *out = nullptr;
     w12_host *h = new (std::nothrow) w12_host;
     if (!h)
@@ -186,7 +239,7 @@ w12_status w12_encode(const uint16_t *w_bf16, int64_t N, int64_t K, int n_thread
             if (blk >= blocks)
                 break;
             const int64_t r0 = blk * kTileRows;
-            encode_block(w_bf16, K, r0, std::min<int64_t>(N, r0 + kTileRows), h, &outs[blk]);
+            encode_block(w_bf16, K, r0, std::min<int64_t>(N, r0 + kTileRows), h, &outs[blk], count_max);
         }
     };
     try {
@@ -300,13 +353,16 @@ w12_status w12_validate(const w12_host *h)
             const int eb = h->ebase[n];
             if (ex != 0 && ex != 0xFF && static_cast<int>(ex) >= eb && static_cast<int>(ex) <= eb + 15)
                 return W12_ERR_CORRUPT; // an in-window weight must not escape
-            if (h->ae[n * K + k] != ((bits >> 15) << 7))
-                return W12_ERR_CORRUPT; // placeholder A = s<<3, E = 0
+            // placeholder: A = s<<3, E = 0, B = 0; above the window (a
+            // count-maximising window) A = s<<3 | 7, E = 15, B = 15
+            const bool above = ex != 0xFF && static_cast<int>(ex) > eb + 15;
+            if (h->ae[n * K + k] != (((bits >> 15) << 7) | (above ? 0x7Fu : 0u)))
+                return W12_ERR_CORRUPT;
             const int64_t j = k % 8;
             const int slot = (j & 1) ? 4 + static_cast<int>(j >> 1) : static_cast<int>(j >> 1);
             const uint32_t word = rd32(&h->b[n * brow + 4 * (k / 8)]);
-            if ((word >> (4 * slot)) & 0xF)
-                return W12_ERR_CORRUPT; // placeholder B = 0
+            if (((word >> (4 * slot)) & 0xF) != (above ? 0xFu : 0u))
+                return W12_ERR_CORRUPT;
         }
     }
     if (K % 8) {

@@ -59,6 +59,24 @@ def test_encoder_matches_oracle_bytes(w12, name):
     assert st["bytes_total"] == len(blob)
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged", "heavy", "random_bits", "all_patterns", "empty_rows",
+                                  "empty_cols", "single", "zeros"])
+def test_count_max_encoder_matches_oracle_bytes(w12, name):
+    """Count-maximising windows: the library's blob is the oracle's, it
+    validates and decodes losslessly, and never has more escapes than the
+    max-anchored encoding of the same matrix."""
+    W = _cases()[name]
+    blob = O.encode(W, count_max=True)
+    for threads in (1, 0):
+        h = w12.w12_encode(W, n_threads=threads, count_max=True)
+        assert h.validate() == 0
+        assert h.serialize() == blob
+    assert np.array_equal(O.decode(blob), W)
+    assert O.blob_header(blob)[2] <= O.blob_header(O.encode(W))[2]
+    h2 = w12.w12_deserialize(blob)
+    assert h2.validate() == 0
+
+
 def test_encoder_full_projection_shape(w12):
     W = WL.projection_weights(5120, 5120, seed=2)
     h = w12.w12_encode(W)
@@ -124,17 +142,29 @@ def _corrupt(blob: bytes, N: int, K: int, what: str) -> bytes:
         eb = b[off_eb + n]
         e = (e & 0xFFFF0000) | ((eb + 3) << 7)
         b[off_esc:off_esc + 4] = e.to_bytes(4, "little")
+    elif what == "saturated_placeholder":
+        # an escape above its row's window must carry A = s<<3|7, E = 15
+        for i in range(n_esc):
+            e = int.from_bytes(b[off_esc + 4 * i:off_esc + 4 * i + 4], "little")
+            n_in_tile = e >> 24
+            ex = (e >> 7) & 0xFF
+            if 1 <= ex <= 254 and ex > b[off_eb + n_in_tile] + 15:
+                b[off_ae + n_in_tile * K + ((e >> 16) & 0xFF)] &= 0xF0
+                break
+        else:
+            raise AssertionError("no escape above a window")
     elif what == "truncated":
         return bytes(b[:-4])
     return bytes(b)
 
 
 @pytest.mark.parametrize("what", ["ebase_zero", "ebase_high", "unsorted", "ptr", "placeholder",
-                                  "in_window_escape", "truncated"])
+                                  "in_window_escape", "truncated", "saturated_placeholder"])
 def test_validator_rejects_corruption(w12, what):
     W = WL.projection_weights(64, 256, seed=21, outlier_frac=5e-3)
     W[0, :3] = 0  # a few escapes in row 0
-    blob = O.encode(W)
+    W[1, 5] = 0x7F00  # a huge weight that a count-maximising window leaves above it
+    blob = O.encode(W, count_max=(what == "saturated_placeholder"))
     bad = _corrupt(blob, 64, 256, what)
     with pytest.raises(w12.W12Error) as e:
         w12.w12_deserialize(bad)
@@ -169,6 +199,7 @@ def test_invalid_arguments(w12):
     assert lib.w12_encode(None, 4, 4, 0, ctypes.byref(out)) == 1
     assert lib.w12_encode(None, -1, 4, 0, ctypes.byref(out)) == 1
     assert lib.w12_validate(None) == 1
+    assert lib.w12_encode_ex(None, 0, 0, 0, 2, ctypes.byref(out)) == 1  # unknown flag
     assert lib.w12_status_string(8) == b"device wait timed out"
 
 
