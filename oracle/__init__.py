@@ -19,6 +19,9 @@ from .oracle import (  # noqa: F401
     num_tiles,
     b_row_bytes,
     round_bf16,
+    i8_quantize,
+    gemm_i8,
+    abs_gemm_i8,
     silu_mul,
     TILE_ROWS,
     TILE_COLS,

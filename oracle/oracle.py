@@ -79,6 +79,12 @@ def _declare(lib):
     lib.orc_num_tiles.restype = _I64
     lib.orc_b_row_bytes.argtypes = [_I64]
     lib.orc_b_row_bytes.restype = _I64
+    lib.orc_i8_quantize.argtypes = [_P, _I64, _I64, _P, _P]
+    lib.orc_i8_quantize.restype = None
+    lib.orc_gemm_i8.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P]
+    lib.orc_gemm_i8.restype = None
+    lib.orc_abs_gemm_i8.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P]
+    lib.orc_abs_gemm_i8.restype = None
     lib.orc_round_bf16.argtypes = [_P, _I64, _P]
     lib.orc_round_bf16.restype = None
     lib.orc_silu_mul.argtypes = [_P, _I64, _I64, _P]
@@ -235,3 +241,40 @@ def silu_mul(y, lib=None) -> np.ndarray:
     h = np.zeros((M, N // 2), dtype=np.float64)
     lib.orc_silu_mul(_ptr(a), M, N, _ptr(h))
     return h
+
+
+def i8_quantize(w_bits, lib=None):
+    """INT8 copy (R14): (q[N][K] int8, scale[N] float32) of BF16 weights."""
+    lib = lib or _get()
+    w = _u16(w_bits)
+    N, K = w.shape
+    q = np.zeros((N, K), dtype=np.int8)
+    sc = np.zeros(N, dtype=np.float32)
+    lib.orc_i8_quantize(_ptr(w), N, K, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def gemm_i8(x_bits, q, scale, lib=None) -> np.ndarray:
+    """y[M][N] = x . (q * scale)^T in float64, k ascending."""
+    lib = lib or _get()
+    x = _u16(x_bits)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    sc = np.ascontiguousarray(scale, dtype=np.float32)
+    M, K = x.shape
+    N = q.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    lib.orc_gemm_i8(_ptr(x), _ptr(q), _ptr(sc), M, N, K, _ptr(y))
+    return y
+
+
+def abs_gemm_i8(x_bits, q, scale, lib=None) -> np.ndarray:
+    """s[M][N] = sum_k |x q scale| in float64."""
+    lib = lib or _get()
+    x = _u16(x_bits)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    sc = np.ascontiguousarray(scale, dtype=np.float32)
+    M, K = x.shape
+    N = q.shape[0]
+    s = np.zeros((M, N), dtype=np.float64)
+    lib.orc_abs_gemm_i8(_ptr(x), _ptr(q), _ptr(sc), M, N, K, _ptr(s))
+    return s

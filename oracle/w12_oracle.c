@@ -62,6 +62,14 @@
  *      placeholder A = s<<3 | 7, E = 15, B = 15 -- the window's largest
  *      magnitude with the weight's sign -- so that the 8-bit view reads them
  *      as the nearest value it can hold.  Decoding is unchanged.
+ *
+ * A separate low-bit copy for the Q pass (the pages keep an INT6/INT8 copy on
+ * the smaller GPU, RTX PRO 6000 section; the plainest INT8 reading):
+ *   R14 INT8 copy: per row n, scale[n] = amax / 127 in FP32, amax the largest
+ *      |w| over the row's finite weights; q[n][k] = rint(w / scale[n]) in FP32
+ *      (round half to even), clamped to [-127, 127]; Inf goes to +-127, NaN to
+ *      0, and a row whose scale is 0 has q = 0.  The Q-pass product is
+ *      y[m][n] = scale[n] * sum_k x[m][k] q[n][k].
  */
 #include <math.h>
 #include <stdint.h>
@@ -563,6 +571,74 @@ void orc_silu_mul(const double *y, int64_t M, int64_t N, double *h)
         for (i = 0; i < N / 2; i++) {
             double g = y[m * N + 2 * i], u = y[m * N + 2 * i + 1];
             h[m * (N / 2) + i] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+}
+
+/* ---- INT8 copy for the Q pass (R14) ------------------------------------- */
+
+static float bf16_float(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+void orc_i8_quantize(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *scale)
+{
+    int64_t n, k;
+    for (n = 0; n < N; n++) {
+        float amax = 0.0f, sc;
+        for (k = 0; k < K; k++) {
+            float v = bf16_float(w[n * K + k]);
+            if (isfinite(v) && fabsf(v) > amax)
+                amax = fabsf(v);
+        }
+        sc = amax / 127.0f;
+        scale[n] = sc;
+        for (k = 0; k < K; k++) {
+            float v = bf16_float(w[n * K + k]), t;
+            if (sc == 0.0f || isnan(v)) {
+                q[n * K + k] = 0;
+                continue;
+            }
+            t = rintf(v / sc);
+            if (t > 127.0f)
+                t = 127.0f;
+            if (t < -127.0f)
+                t = -127.0f;
+            q[n * K + k] = (int8_t)t;
+        }
+    }
+}
+
+/* y[m][n] = sum_k x[m][k] * (q[n][k] * scale[n]) in double, k ascending. */
+void orc_gemm_i8(const uint16_t *x, const int8_t *q, const float *scale, int64_t M, int64_t N, int64_t K,
+                 double *y)
+{
+    int64_t m, n, k;
+    for (m = 0; m < M; m++) {
+        for (n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (k = 0; k < K; k++)
+                acc += bf16_value(x[m * K + k]) * ((double)q[n * K + k] * (double)scale[n]);
+            y[m * N + n] = acc;
+        }
+    }
+}
+
+/* s[m][n] = sum_k |x[m][k] * q[n][k] * scale[n]|: the scale of the bound. */
+void orc_abs_gemm_i8(const uint16_t *x, const int8_t *q, const float *scale, int64_t M, int64_t N, int64_t K,
+                     double *s)
+{
+    int64_t m, n, k;
+    for (m = 0; m < M; m++) {
+        for (n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (k = 0; k < K; k++)
+                acc += fabs(bf16_value(x[m * K + k]) * ((double)q[n * K + k] * (double)scale[n]));
+            s[m * N + n] = acc;
         }
     }
 }

@@ -358,6 +358,72 @@ def pin_count_max_encoding(lib=None):
     assert np.array_equal(O.decode(O.encode(pats, lib=lib, count_max=True), lib=lib), pats)
 
 
+# ---- INT8 copy for the Q pass -------------------------------------------------------
+
+def _bf16(vals):
+    """BF16 bit patterns of values that BF16 holds exactly."""
+    a = np.asarray(vals, dtype=np.float32).view(np.uint32)
+    assert np.all((a & 0xFFFF) == 0)
+    return (a >> 16).astype(np.uint16)
+
+
+def pin_i8_quantize(lib=None):
+    """Worked rows whose scale is exact (amax 127 -> scale 1, amax 254 ->
+    scale 2), so every tie is a true tie and goes to the even integer; Inf,
+    NaN and zero rows; and on random rows the properties any such
+    quantisation has: |q| <= 127, the largest finite weight maps to +-127,
+    |w - q scale| <= scale / 2, order and sign kept."""
+    inf, nan = float("inf"), float("nan")
+    rows = [
+        ([127.0, 2.5, 3.5, -2.5, 126.5, 0.5, 1.5, -1.5, inf, -inf, nan, 0.0, -0.0, 64.0],
+         [127, 2, 4, -2, 126, 0, 2, -2, 127, -127, 0, 0, 0, 64], 1.0),
+        ([254.0, 3.0, 5.0, -7.0, 1.0, -254.0, 9.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0],
+         [127, 2, 2, -4, 0, -127, 4, 0, 0, 0, 0, 0, 0, 0], 2.0),
+        ([0.0] * 14, [0] * 14, 0.0),
+    ]
+    W = np.stack([_bf16(np.array(r[0], dtype=np.float32)) for r in rows])
+    q, sc = O.i8_quantize(W, lib=lib)
+    for i, (_, want, s) in enumerate(rows):
+        assert sc[i] == np.float32(s), (i, sc[i])
+        assert q[i].tolist() == want, (i, q[i].tolist())
+    W = WL.projection_weights(64, 700, seed=98, outlier_frac=3e-3)
+    W[5, :] = 0
+    q, sc = O.i8_quantize(W, lib=lib)
+    wf = WL.bf16_bits_to_f32(W).astype(np.float64)
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    for n in range(64):
+        amax = np.abs(wf[n]).max()
+        if amax == 0:
+            assert sc[n] == 0 and not q[n].any()
+            continue
+        assert abs(float(sc[n]) - amax / 127) <= 2.0 ** -23 * amax / 127
+        assert np.abs(q[n]).max() == 127 and abs(int(q[n][np.argmax(np.abs(wf[n]))])) == 127
+        err = np.abs(wf[n] - q[n].astype(np.float64) * float(sc[n]))
+        assert np.all(err <= 0.5 * float(sc[n]) * (1 + 2.0 ** -18))
+        assert np.all((np.sign(q[n]) == np.sign(wf[n])) | (q[n] == 0))
+        o = np.argsort(wf[n], kind="stable")
+        assert np.all(np.diff(q[n][o].astype(np.int32)) >= 0)
+
+
+def pin_gemm_i8(lib=None):
+    """The INT8 product against numpy's float64 matmul of the dequantised
+    weights, and one-hot activations picking single q * scale values."""
+    W = WL.projection_weights(90, 333, seed=99, outlier_frac=2e-3)
+    q, sc = O.i8_quantize(W, lib=lib)
+    x = WL.activations(4, 333, seed=100)
+    y = O.gemm_i8(x, q, sc, lib=lib)
+    xf = WL.bf16_bits_to_f32(x).astype(np.float64)
+    deq = q.astype(np.float64) * sc.astype(np.float64)[:, None]
+    ref = xf @ deq.T
+    scale = np.abs(xf) @ np.abs(deq).T
+    assert np.all(np.abs(y - ref) <= 1e-12 * scale + 1e-300)
+    assert np.allclose(O.abs_gemm_i8(x, q, sc, lib=lib), scale, rtol=1e-12, atol=0)
+    for k0 in (0, 100, 332):
+        e = np.zeros((1, 333), dtype=np.uint16)
+        e[0, k0] = 0x3F80
+        assert np.array_equal(O.gemm_i8(e, q, sc, lib=lib)[0], deq[:, k0])
+
+
 # ---- epilogues: BF16 output and the gated-MLP product ----------------------------
 
 def _f32(bits):
@@ -502,4 +568,6 @@ FAST_PINS = (
     pin_silu_mul,
     pin_count_max_window,
     pin_count_max_encoding,
+    pin_i8_quantize,
+    pin_gemm_i8,
 )

@@ -60,6 +60,12 @@ MUTANTS = [
     ("saturated_E_zero", "    if (above_window(b, ebase))\n        return 15;\n    return 0;\n}\n\nstatic int field_B",
      "    if (above_window(b, ebase))\n        return 0;\n    return 0;\n}\n\nstatic int field_B"),
     ("saturated_B_zero", "        return 15;\n    return 0;\n}\n\n/* R6", "        return 0;\n    return 0;\n}\n\n/* R6"),
+    ("i8_round_half_away", "t = rintf(v / sc);", "t = roundf(v / sc);"),
+    ("i8_scale_over_128", "sc = amax / 127.0f;", "sc = amax / 128.0f;"),
+    ("i8_clamp_126", "if (t > 127.0f)\n                t = 127.0f;", "if (t > 126.0f)\n                t = 126.0f;"),
+    ("i8_amax_counts_inf", "if (isfinite(v) && fabsf(v) > amax)", "if (!isnan(v) && fabsf(v) > amax)"),
+    ("i8_gemm_drops_scale", "acc += bf16_value(x[m * K + k]) * ((double)q[n * K + k] * (double)scale[n]);",
+     "acc += bf16_value(x[m * K + k]) * ((double)q[n * K + k]);"),
     ("above_one_binade_late", "return is_finite_normal(b) && bf16_exp(b) > ebase + 15;",
      "return is_finite_normal(b) && bf16_exp(b) > ebase + 16;"),
 ]
