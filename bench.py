@@ -402,6 +402,29 @@ def run_w12(args):
         assert w12.w12_dev_status(dm) == 0
         res["q8_view_GBps"] = round((17408 * 5120 + 2 * 64 * 5120 + 4 * 64 * 17408) / (res["q8_us"] * 1e3), 1)
         tlv[dist_name] = res
+    # the Q pass over a separate INT8 copy of the projection draw, at M = 64
+    q8c = w12.w12_i8_from_dev(layers[0][4][1], stream)
+    for _ in range(3):
+        w12.w12_gemm_i8(x64, q8c, y64, stream)
+    torch.cuda.synchronize()
+    gq = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gq, stream=stream):
+        for _ in range(G):
+            w12.w12_gemm_i8(x64, q8c, y64, stream)
+    gq.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(short):
+        gq.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert w12.w12_i8_status(q8c) == 0
+    q_us = 1e3 * e0.elapsed_time(e1) / (short * G)
+    tlv["projection"]["q_int8_copy_us"] = round(q_us, 2)
+    tlv["projection"]["q_int8_copy_GBps"] = round((17408 * 5120 + 4 * 17408 + 2 * 64 * 5120 + 4 * 64 * 17408)
+                                                  / (q_us * 1e3), 1)
+    q8c.free()
     tlv["escape_fraction_heavy_tail"] = round(hheavy.stats()["escape_fraction"], 5)
     tlv["escape_fraction_heavy_tail_count_max_windows"] = round(hheavy_cm.stats()["escape_fraction"], 5)
     del hheavy, hheavy_cm

@@ -246,6 +246,47 @@ enum {
 w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int N, int K,
                        unsigned flags, w12_stream_t stream);
 
+/* ---- INT8 copy for the Q pass ------------------------------------------------ */
+
+/*
+ * A separate INT8 copy of a weight matrix for the Q pass (the pages keep an
+ * INT6/INT8 copy on the smaller GPU, RTX PRO 6000 section; this is the INT8
+ * form), as an alternative to the nested 8-bit view: per output row n,
+ * scale[n] = amax / 127 in FP32 (amax: the largest |w| of the row's finite
+ * weights) and q[n][k] = rint(w / scale[n]) (FP32, round half to even)
+ * clamped to [-127, 127]; Inf becomes +-127, NaN 0, and a row whose scale is
+ * 0 keeps q = 0.  1 byte per weight plus 4 per row, in one device allocation
+ * (the copy is extra memory: the W12 handle stays the lossless one).
+ */
+typedef struct w12_i8 w12_i8;
+
+/* INT8 copy of BF16 weights w_bf16[N][K] already in device memory; synchronises
+ * with `stream`.  Errors: INVALID_ARG, UNSUPPORTED (N or K above 2^31), OOM, CUDA. */
+w12_status w12_i8_encode_device(const void *w_bf16, int64_t N, int64_t K, w12_stream_t stream, w12_i8 **out);
+
+/* INT8 copy of the weights a W12 handle holds (decoded into a temporary
+ * N x K BF16 buffer, stream-ordered, then quantised). */
+w12_status w12_i8_from_dev(const w12_dev *w, w12_stream_t stream, w12_i8 **out);
+
+void w12_i8_free(w12_i8 *q);
+
+/* Copy q (N*K bytes) and/or the scales (N floats) to host buffers (either may
+ * be NULL); synchronises with `stream`. */
+w12_status w12_i8_download(const w12_i8 *q, int8_t *q_host, float *scale_host, w12_stream_t stream);
+
+/* Device status of an INT8 copy's GEMMs (as w12_dev_status), reset to OK. */
+w12_status w12_i8_status(const w12_i8 *q, w12_stream_t stream);
+
+/*
+ * The Q pass over an INT8 copy: y[m][n] = scale[n] * sum_k x[m][k] q[n][k],
+ * FP32 accumulation on the tensor cores (every q is exact in BF16).  Arguments,
+ * limits, flags (W12_GEMM_INPUT_READY, W12_GEMM_OUT_BF16, W12_GEMM_SILU_MUL;
+ * any other bit gives INVALID_ARG) and errors as w12_gemm_ex.  Every M runs on
+ * the tensor-core kernel (M padded to 16, 32, 64 or 128).
+ */
+w12_status w12_gemm_i8(const void *x_bf16, const w12_i8 *q, void *y, int M, int N, int K, unsigned flags,
+                       w12_stream_t stream);
+
 /*
  * End-to-end form of w12_gemm for host-resident activations: copies
  * x_host -> x_dev, runs w12_gemm into y_dev, copies y_dev -> y_host, all on

@@ -79,6 +79,12 @@ _sig("w12_upload", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_free", [_P], None)
 _sig("w12_encode_device", [_P, _I64, _I64, _P, ctypes.POINTER(_P)])
 _sig("w12_encode_device_ex", [_P, _I64, _I64, ctypes.c_uint, _P, ctypes.POINTER(_P)])
+_sig("w12_i8_encode_device", [_P, _I64, _I64, _P, ctypes.POINTER(_P)])
+_sig("w12_i8_from_dev", [_P, _P, ctypes.POINTER(_P)])
+_sig("w12_i8_free", [_P], None)
+_sig("w12_i8_download", [_P, _P, _P, _P])
+_sig("w12_i8_status", [_P, _P])
+_sig("w12_gemm_i8", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_download", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
@@ -100,6 +106,7 @@ EXPORTED = (
     "w12_decode", "w12_dev_status", "w12_release_workspaces", "w12_set_spin_limit",
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
     "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
+    "w12_i8_encode_device", "w12_i8_from_dev", "w12_i8_free", "w12_i8_download", "w12_i8_status", "w12_gemm_i8",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -285,6 +292,79 @@ def w12_encode_device(w, stream=None, count_max: bool = False) -> Dev:
     _check(_lib.w12_encode_device_ex(ctypes.c_void_p(w.data_ptr()), N, K, flags, _stream_ptr(stream),
                                      ctypes.byref(out)), "w12_encode_device")
     return Dev(out.value, N, K)
+
+
+class I8:
+    """An INT8 copy of a weight matrix for the Q pass (owns a ``w12_i8*``)."""
+
+    def __init__(self, ptr: int, N: int, K: int):
+        self._ptr = ptr
+        self.N, self.K = N, K
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    def free(self):
+        if getattr(self, "_ptr", None):
+            _lib.w12_i8_free(self._ptr)
+            self._ptr = None
+
+    def __del__(self):
+        self.free()
+
+
+def w12_i8_encode_device(w, stream=None) -> I8:
+    """INT8 copy (per-row FP32 scale, round half to even) of a CUDA [N][K]
+    tensor of BF16 weights (bfloat16 or its 16-bit pattern)."""
+    import torch
+    if not (isinstance(w, torch.Tensor) and w.is_cuda and w.dim() == 2 and w.is_contiguous() and w.element_size() == 2
+            and w.dtype in (torch.bfloat16, torch.int16, torch.uint16)):
+        raise TypeError("w must be a contiguous CUDA [N][K] tensor of BF16 (or its 16-bit pattern)")
+    N, K = w.shape
+    out = _P()
+    _check(_lib.w12_i8_encode_device(ctypes.c_void_p(w.data_ptr()), N, K, _stream_ptr(stream), ctypes.byref(out)),
+           "w12_i8_encode_device")
+    return I8(out.value, N, K)
+
+
+def w12_i8_from_dev(d: Dev, stream=None) -> I8:
+    """INT8 copy of the weights a W12 device handle holds."""
+    out = _P()
+    _check(_lib.w12_i8_from_dev(d.ptr, _stream_ptr(stream), ctypes.byref(out)), "w12_i8_from_dev")
+    return I8(out.value, d.N, d.K)
+
+
+def w12_i8_download(q: I8, stream=None):
+    """(q [N][K] int8, scale [N] float32) as numpy arrays."""
+    qh = np.zeros((q.N, q.K), dtype=np.int8)
+    sh = np.zeros(q.N, dtype=np.float32)
+    _check(_lib.w12_i8_download(q.ptr, qh.ctypes.data_as(_P), sh.ctypes.data_as(_P), _stream_ptr(stream)),
+           "w12_i8_download")
+    return qh, sh
+
+
+def w12_i8_status(q: I8, stream=None) -> int:
+    return int(_lib.w12_i8_status(q.ptr, _stream_ptr(stream)))
+
+
+def w12_gemm_i8(x, q: I8, y=None, stream=None, input_ready=False, out_bf16=False, silu_mul=False):
+    """The Q pass over an INT8 copy: y = scale * (x . q^T), flags as w12_gemm_ex."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
+    M, K = x.shape
+    cols = q.N // 2 if silu_mul else q.N
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    if y is None:
+        y = torch.empty((M, cols), dtype=dt, device=x.device)
+    elif y.dtype != dt or not y.is_cuda or y.numel() < M * cols:
+        raise TypeError(f"y must be a CUDA {dt} tensor of at least {M} x {cols} elements")
+    flags = ((W12_GEMM_INPUT_READY if input_ready else 0) | (W12_GEMM_OUT_BF16 if out_bf16 else 0)
+             | (W12_GEMM_SILU_MUL if silu_mul else 0))
+    _check(_lib.w12_gemm_i8(ctypes.c_void_p(x.data_ptr()), q.ptr, ctypes.c_void_p(y.data_ptr()), M, q.N, K, flags,
+                            _stream_ptr(stream)), "w12_gemm_i8")
+    return y
 
 
 def w12_download(d: Dev, stream=None) -> Host:

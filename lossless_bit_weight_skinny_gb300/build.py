@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libw12.so")
 
-CU_SOURCES = ("runtime.cu", "gemm_fma.cu", "gemm_tc.cu", "decode.cu", "noalloc.cu", "encode.cu", "reduce.cu")
+CU_SOURCES = ("runtime.cu", "gemm_fma.cu", "gemm_tc.cu", "decode.cu", "noalloc.cu", "encode.cu", "reduce.cu", "i8.cu")
 CPP_SOURCES = ("host.cpp",)
 HEADERS = ("ptx.cuh", "kernels.cuh", "w12_internal.h")
 

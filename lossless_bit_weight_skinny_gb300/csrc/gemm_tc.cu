@@ -192,7 +192,9 @@ struct EscPatcher {
 // 19 warps: 5 per SM sub-partition, whose 16K registers allow 102 per thread
 // EPI: the output goes through the output mode (BF16, SiLU*mul); the default
 // FP32 store is a kernel of its own, whose registers that code leaves alone.
-template <int MT, bool Q8, bool EPI>
+// I8 (with Q8's layout: one weight plane, no escapes): the plane holds an
+// INT8 copy, converted to BF16 exactly, and the row scales apply at the end.
+template <int MT, bool Q8, bool EPI, bool I8 = false>
 __global__ void __maxnreg__(96)
     gemm_tc_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
                    const __grid_constant__ CUtensorMap tm_b,
@@ -492,7 +494,7 @@ __global__ void __maxnreg__(96)
             // window base of a new row block: start the load before waiting
             uint32_t e_pre = 1u;
             if (rb != cur_rb && rb * 128 + row < a.N)
-                e_pre = __ldg(a.ebase + rb * 128 + row);
+                e_pre = I8 ? 1u : __ldg(a.ebase + rb * 128 + row);
             bool ok = wait_or_abort(w_full0 + 8 * s, ph, a, abort_flag);
             if (a.inject_stall)
                 ok = wait_or_abort(stall_bar, 0, a, abort_flag) && ok;
@@ -539,8 +541,13 @@ __global__ void __maxnreg__(96)
                                         bq[1].x, bq[1].y, bq[1].z, bq[1].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    decode_group<Q8>(aq[i].x, aq[i].y, bw[2 * i], eb2, v + 8 * i);
-                    decode_group<Q8>(aq[i].z, aq[i].w, bw[2 * i + 1], eb2, v + 8 * i + 4);
+                    if constexpr (I8) {
+                        decode_i8_group(aq[i].x, aq[i].y, v + 8 * i);
+                        decode_i8_group(aq[i].z, aq[i].w, v + 8 * i + 4);
+                    } else {
+                        decode_group<Q8>(aq[i].x, aq[i].y, bw[2 * i], eb2, v + 8 * i);
+                        decode_group<Q8>(aq[i].z, aq[i].w, bw[2 * i + 1], eb2, v + 8 * i + 4);
+                    }
                 }
             }
 
@@ -618,6 +625,9 @@ __global__ void __maxnreg__(96)
                 const bool direct = (c_first == c_last);
                 const int slot = direct ? 0 : sk_slot(cta, rb, grid, a.total_iters, nk);
                 const int n = row0 + row;
+                float rs = 1.f; // an INT8 copy's row scale
+                if constexpr (I8)
+                    rs = n < a.N ? __ldg(a.scale + n) : 0.f;
                 if (used) {
                     const uint32_t dcol = tmem + t_lane + kDCol + L::DW * db + c * PART;
                     const bool pair = EPI && direct && (a.out_mode & kOutSiluMul);
@@ -633,7 +643,7 @@ __global__ void __maxnreg__(96)
                         tc_wait_ld();
 #pragma unroll
                         for (int j = 0; j < CH; ++j) {
-                            const float v = __uint_as_float(d[j]);
+                            const float v = I8 ? __uint_as_float(d[j]) * rs : __uint_as_float(d[j]);
                             const int m = c * PART + h * CH + j;
                             // row + 1 (the up row of an even gate row) is lane + 1
                             const float next = pair ? __shfl_down_sync(0xffffffffu, v, 1) : 0.f;
@@ -692,12 +702,12 @@ __global__ void __maxnreg__(96)
     }
 }
 
-template <int MT, bool Q8, bool EPI>
+template <int MT, bool Q8, bool EPI, bool I8 = false>
 cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
                        const CUtensorMap *tm_x, int grid, cudaStream_t st)
 {
     using L = TcSmem<MT, Q8>;
-    auto kern = gemm_tc_kernel<MT, Q8, EPI>;
+    auto kern = gemm_tc_kernel<MT, Q8, EPI, I8>;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -721,9 +731,12 @@ int tc_smem_bytes(int mt, bool q8)
 }
 
 template <int MT>
-cudaError_t launch_mt(bool q8, const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
+cudaError_t launch_mt(bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
                       const CUtensorMap *tm_x, int grid, cudaStream_t st)
 {
+    if (i8)
+        return a.out_mode ? launch_one<MT, true, true, true>(a, tm_ae, tm_b, tm_x, grid, st)
+                          : launch_one<MT, true, false, true>(a, tm_ae, tm_b, tm_x, grid, st);
     if (a.out_mode)
         return q8 ? launch_one<MT, true, true>(a, tm_ae, tm_b, tm_x, grid, st)
                   : launch_one<MT, false, true>(a, tm_ae, tm_b, tm_x, grid, st);
@@ -731,15 +744,15 @@ cudaError_t launch_mt(bool q8, const GemmArgs &a, const CUtensorMap *tm_ae, cons
               : launch_one<MT, false, false>(a, tm_ae, tm_b, tm_x, grid, st);
 }
 
-cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
+cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae,
                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                            cudaStream_t st)
 {
     switch (mt) {
-    case 16: return launch_mt<16>(q8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 32: return launch_mt<32>(q8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 64: return launch_mt<64>(q8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 128: return launch_mt<128>(q8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 16: return launch_mt<16>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 32: return launch_mt<32>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 64: return launch_mt<64>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 128: return launch_mt<128>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -37,6 +37,7 @@ struct GemmArgs {
     int out_mode;                  // kOutBF16 | kOutSiluMul
     int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
     int defer;                     // split row blocks: leave the partials to sk_reduce_kernel
+    const float *scale;            // [N] row scales of an INT8 copy (INT8 weights only)
 };
 
 // Output modes.  kOutBF16: y holds BF16, each FP32 result rounded to the
@@ -101,6 +102,28 @@ __device__ __forceinline__ void decode_group(uint32_t a_lo, uint32_t a_hi, uint3
     out[1] = decode_pair<1, Q8>(a_lo, bw, eb2);
     out[2] = decode_pair<2, Q8>(a_hi, bw, eb2);
     out[3] = decode_pair<3, Q8>(a_hi, bw, eb2);
+}
+
+// 8 INT8 weights (two words, two's complement, weight j in byte j) -> 4 BF16x2
+// pairs, exactly: byte u = q + 128 (XOR 0x80) is placed under the exponent of
+// 2^23 by one PRMT (fp32 2^23 + u), an FP32 subtraction of 2^23 + 128 leaves q
+// exactly, and since |q| <= 127 needs at most 7 significant bits, the upper
+// halves of two such floats are the two BF16 values.
+__device__ __forceinline__ void decode_i8_group(uint32_t lo, uint32_t hi, uint32_t *out)
+{
+    const uint32_t w[2] = {lo ^ 0x80808080u, hi ^ 0x80808080u};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t src = w[p >> 1];
+        uint32_t f0, f1;
+        const uint32_t sel0 = 0x7650u | static_cast<uint32_t>((2 * p) & 3);
+        const uint32_t sel1 = 0x7650u | static_cast<uint32_t>((2 * p + 1) & 3);
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(f0) : "r"(src), "r"(0x4B000000u), "r"(sel0));
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(f1) : "r"(src), "r"(0x4B000000u), "r"(sel1));
+        const float q0 = __uint_as_float(f0) - 8388736.0f; // 2^23 + 128
+        const float q1 = __uint_as_float(f1) - 8388736.0f;
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(out[p]) : "r"(__float_as_uint(q0)), "r"(__float_as_uint(q1)));
+    }
 }
 
 // First iteration of CTA c when `iters` iterations are split over `grid` CTAs.
@@ -282,7 +305,12 @@ cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMa
 // tensor-core GEMM launched with a.defer set; nothing is launched when no row
 // block is split.  *launched tells whether it was.
 cudaError_t launch_sk_reduce(const GemmArgs &a, int gemm_grid, int rows_blk, cudaStream_t st, bool *launched);
-cudaError_t launch_gemm_tc(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
+// INT8 copy of BF16 weights on the device (i8.cu): per row, scale = amax / 127
+// over the finite weights, q = rint(w / scale) clamped to [-127, 127], Inf to
+// +-127, NaN to 0, q = 0 where the scale is 0.
+cudaError_t launch_i8_quantize(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *scale, cudaStream_t st);
+// i8: the weights are an INT8 copy (a.scale set, tm_ae over its bytes).
+cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae,
                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
                            cudaStream_t st);
 int fma_rows_blk(int mt);

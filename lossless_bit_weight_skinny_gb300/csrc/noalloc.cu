@@ -177,7 +177,7 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     const w12_tmap &tb = tc ? w->tm_b_tc : (rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
     const CUtensorMap *pae = reinterpret_cast<const CUtensorMap *>(&tae);
     const CUtensorMap *pb = reinterpret_cast<const CUtensorMap *>(&tb);
-    cudaError_t e = tc ? launch_gemm_tc(mt, false, a, pae, pb, &tmx, grid, st)
+    cudaError_t e = tc ? launch_gemm_tc(mt, false, false, a, pae, pb, &tmx, grid, st)
                        : launch_gemm_fma(mt, false, a, pae, pb, &tmx, grid, st);
     bool red = false;
     if (e == cudaSuccess && a.defer)

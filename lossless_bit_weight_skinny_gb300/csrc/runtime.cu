@@ -229,7 +229,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     }
     cudaError_t e;
     if (tc) {
-        e = launch_gemm_tc(mt, q8, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
+        e = launch_gemm_tc(mt, q8, false, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
         bool red = false;
         if (e == cudaSuccess && a.defer)
             e = launch_sk_reduce(a, grid, rows_blk, st, &red);
@@ -486,5 +486,215 @@ void w12_set_spin_limit(uint32_t limit_ns)
 void w12_debug_inject_stall(int on) { g_inject_stall.store(on ? 1 : 0); }
 
 const char *w12_last_cuda_error(void) { return g_last_error; }
+
+} // extern "C"
+
+// ---- INT8 copy for the Q pass ------------------------------------------------
+
+namespace {
+
+w12_status i8_create(int64_t N, int64_t K, cudaStream_t st, w12_i8 **out)
+{
+    *out = nullptr;
+    w12_i8 *q = new (std::nothrow) w12_i8;
+    if (!q)
+        return W12_ERR_OOM;
+    if (cudaGetDevice(&q->device) != cudaSuccess) {
+        delete q;
+        return W12_ERR_CUDA;
+    }
+    q->N = N;
+    q->K = K;
+    auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    const size_t s_status = 256, s_q = up(static_cast<size_t>(N * K)), s_sc = up(4 * static_cast<size_t>(N));
+    q->bytes = s_status + s_q + s_sc;
+    if (cudaMalloc(&q->base, q->bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete q;
+        return W12_ERR_OOM;
+    }
+    char *p = static_cast<char *>(q->base);
+    q->status = reinterpret_cast<int *>(p);
+    q->q = reinterpret_cast<int8_t *>(p + s_status);
+    q->scale = reinterpret_cast<float *>(p + s_status + s_q);
+    if (cudaMemsetAsync(q->status, 0, 256, st) != cudaSuccess) {
+        cudaFree(q->base);
+        delete q;
+        return W12_ERR_CUDA;
+    }
+    if (N > 0 && K >= 32 && K % 32 == 0)
+        q->gemm_ok = make_tmap(tmap_of(q->tm_q_tc), CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q->q, K, N, 128, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    *out = q;
+    return W12_OK;
+}
+
+w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, int K, cudaStream_t st,
+                        bool x_ready, int out_mode)
+{
+    if (!q || M < 0)
+        return W12_ERR_INVALID_ARG;
+    if (N != q->N || K != q->K)
+        return W12_ERR_SHAPE;
+    if ((out_mode & kOutSiluMul) && (N & 1))
+        return W12_ERR_SHAPE;
+    const int ldy = (out_mode & kOutSiluMul) ? N / 2 : N;
+    const size_t esz = (out_mode & kOutBF16) ? 2 : 4;
+    if (M > kMaxM)
+        return W12_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return W12_OK;
+    if (!x || !y)
+        return W12_ERR_INVALID_ARG;
+    if (M > 128) {
+        const w12_status s1 = gemm_i8_impl(x, q, y, 128, N, K, st, x_ready, out_mode);
+        if (s1 != W12_OK)
+            return s1;
+        return gemm_i8_impl(static_cast<const uint16_t *>(x) + static_cast<size_t>(128) * K, q,
+                            static_cast<char *>(y) + esz * 128 * static_cast<size_t>(ldy), M - 128, N, K, st, true,
+                            out_mode);
+    }
+    if (!aligned16(x) || !aligned16(y))
+        return W12_ERR_ALIGNMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (cur != q->device)
+        return W12_ERR_INVALID_ARG;
+    if (K == 0)
+        return cudaMemsetAsync(y, 0, esz * static_cast<size_t>(M) * ldy, st) == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+    if (!q->gemm_ok)
+        return W12_ERR_UNSUPPORTED;
+    // the tensor-core kernel for every M (M padded to 16, 32, 64 or 128)
+    const int mt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    GemmArgs a{};
+    a.y = y;
+    a.out_mode = out_mode;
+    a.ldy = ldy;
+    a.scale = q->scale;
+    a.status = q->status;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.tiles_c = static_cast<int>(ceil_div(K, kTileCols));
+    a.n_rowblk = static_cast<int>(ceil_div(N, kTcRows));
+    a.n_kstep = static_cast<int>(ceil_div(K, kTcKStep));
+    const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
+    if (iters > (1ll << 30) || a.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
+        return W12_ERR_UNSUPPORTED;
+    a.total_iters = static_cast<int>(iters);
+    a.limit_ns = g_limit_ns.load();
+    a.inject_stall = g_inject_stall.load();
+    a.x_ready = x_ready ? 1 : 0;
+    a.defer = tc_defer(M);
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur), tc_min_iters(M));
+    const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * kTcRows;
+    w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters);
+    if (ws != W12_OK)
+        return ws;
+    CUtensorMap tmx;
+    if (!make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, mt, CU_TENSOR_MAP_SWIZZLE_128B)) {
+        g_last_error = "cuTensorMapEncodeTiled failed for x";
+        return W12_ERR_CUDA;
+    }
+    const CUtensorMap *tq = tmap_of(q->tm_q_tc);
+    cudaError_t e = launch_gemm_tc(mt, true, true, a, tq, tq, &tmx, grid, st);
+    bool red = false;
+    if (e == cudaSuccess && a.defer)
+        e = launch_sk_reduce(a, grid, kTcRows, st, &red);
+    return e == cudaSuccess ? W12_OK : cuda_fail(e);
+}
+
+} // namespace
+
+extern "C" {
+
+w12_status w12_i8_encode_device(const void *w_bf16, int64_t N, int64_t K, w12_stream_t stream, w12_i8 **out)
+{
+    if (!out || N < 0 || K < 0 || (N * K > 0 && !w_bf16))
+        return W12_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return W12_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    w12_i8 *q = nullptr;
+    w12_status r = i8_create(N, K, st, &q);
+    if (r != W12_OK)
+        return r;
+    if (launch_i8_quantize(static_cast<const uint16_t *>(w_bf16), N, K, q->q, q->scale, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        w12_i8_free(q);
+        return W12_ERR_CUDA;
+    }
+    *out = q;
+    return W12_OK;
+}
+
+w12_status w12_i8_from_dev(const w12_dev *w, w12_stream_t stream, w12_i8 **out)
+{
+    if (!w || !out)
+        return W12_ERR_INVALID_ARG;
+    *out = nullptr;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *tmp = nullptr;
+    const size_t bytes = 2 * static_cast<size_t>(w->N) * static_cast<size_t>(w->K);
+    if (bytes && cudaMallocAsync(&tmp, bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return W12_ERR_OOM;
+    }
+    w12_status r = w12_decode(w, static_cast<uint16_t *>(tmp), stream);
+    if (r == W12_OK)
+        r = w12_i8_encode_device(tmp, w->N, w->K, stream, out);
+    if (tmp)
+        cudaFreeAsync(tmp, st);
+    return r;
+}
+
+void w12_i8_free(w12_i8 *q)
+{
+    if (!q)
+        return;
+    cudaFree(q->base);
+    delete q;
+}
+
+w12_status w12_i8_download(const w12_i8 *q, int8_t *q_host, float *scale_host, w12_stream_t stream)
+{
+    if (!q)
+        return W12_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    bool ok = true;
+    if (q_host && q->N * q->K > 0)
+        ok = cudaMemcpyAsync(q_host, q->q, static_cast<size_t>(q->N * q->K), cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (ok && scale_host && q->N > 0)
+        ok = cudaMemcpyAsync(scale_host, q->scale, 4 * static_cast<size_t>(q->N), cudaMemcpyDeviceToHost, st) ==
+             cudaSuccess;
+    return ok && cudaStreamSynchronize(st) == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+w12_status w12_i8_status(const w12_i8 *q, w12_stream_t stream)
+{
+    if (!q)
+        return W12_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (cudaMemcpy(&v, q->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (v != 0 && cudaMemset(q->status, 0, sizeof v) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return static_cast<w12_status>(v);
+}
+
+w12_status w12_gemm_i8(const void *x_bf16, const w12_i8 *q, void *y, int M, int N, int K, unsigned flags,
+                       w12_stream_t stream)
+{
+    if (flags & ~static_cast<unsigned>(W12_GEMM_INPUT_READY | W12_GEMM_OUT_BF16 | W12_GEMM_SILU_MUL))
+        return W12_ERR_INVALID_ARG;
+    const int out_mode = ((flags & W12_GEMM_OUT_BF16) ? kOutBF16 : 0) | ((flags & W12_GEMM_SILU_MUL) ? kOutSiluMul : 0);
+    return gemm_i8_impl(x_bf16, q, y, M, N, K, reinterpret_cast<cudaStream_t>(stream),
+                        (flags & W12_GEMM_INPUT_READY) != 0, out_mode);
+}
 
 } // extern "C"

@@ -54,3 +54,16 @@ struct w12_dev {
     w12_tmap tm_ae_fma128, tm_ae_fma64, tm_b_fma128, tm_b_fma64;
     w12_tmap tm_ae_tc, tm_b_tc;
 };
+
+// INT8 copy of a weight matrix for the Q pass (one allocation).
+struct w12_i8 {
+    int device = 0;
+    int64_t N = 0, K = 0;
+    void *base = nullptr;
+    size_t bytes = 0;
+    int8_t *q = nullptr;   // [N][K]
+    float *scale = nullptr; // [N]
+    int *status = nullptr;  // device status word
+    bool gemm_ok = false;   // K % 32 == 0 and the tensor map built
+    w12_tmap tm_q_tc;       // swizzled 128 x 128 boxes, as the tensor-core kernel's AE plane
+};
