@@ -63,21 +63,25 @@ struct TcSmem {
     static constexpr int PL_LO = 64;
     static constexpr int PL_LIST = 80;
     static constexpr int PL = Q8 ? 0 : PL_LIST + 4 * kPCap * kDecodeWarps;
-    // tensor memory (512 columns): NA decoded A tiles of 128 columns, then two
+    // tensor memory (512 columns): NA decoded A tiles of 128 columns, then ND
     // FP32 accumulator buffers of DW columns (MT <= 64: 3 x 128 + 2 x 64;
-    // MT = 128: 2 x 128 + 2 x 128)
-    static constexpr int NA = MT == 128 ? 2 : 3;
+    // MT = 128: 2 x 128 + 2 x 128; MT = 256: 2 x 128 + 1 x 256, so a row
+    // block's MMAs wait for the previous one's epilogue)
+    static constexpr int NA = MT >= 128 ? 2 : 3;
     static constexpr uint32_t DCOL = NA * 128;
-    static constexpr uint32_t DW = MT <= 64 ? 64 : 128;
+    static constexpr uint32_t DW = MT <= 64 ? 64 : MT;
+    static constexpr int ND = MT == 256 ? 1 : 2;
     // activations: a unit needs four 64-column sub-tiles of MT rows (128-byte
     // swizzle); a ring slot holds SPS of them -- the whole unit's (SPS = 4)
-    // up to 64 rows, one sub-tile (SPS = 1) at 128 rows, where a unit's 64 KB
-    // would leave too little room for the weights
+    // up to 64 rows, one sub-tile (SPS = 1) from 128 rows, where a unit's 64
+    // or 128 KB would leave too little room for the weights (at 256 rows three
+    // slots, fewer than a unit's four: a slot is reloaded within the unit as
+    // soon as the MMAs that read it complete)
     static constexpr int XSUB = MT * 128;
-    static constexpr int SPS = MT == 128 ? 1 : 4;
+    static constexpr int SPS = MT >= 128 ? 1 : 4;
     static constexpr int SPU = 4 / SPS;       // slots per unit
     static constexpr int XSLOT = SPS * XSUB;
-    static constexpr int XST = MT <= 32 ? 3 : MT == 64 ? 2 : W12_TC_XST128; // activation slots
+    static constexpr int XST = MT <= 32 ? 3 : MT == 64 ? 2 : MT == 128 ? W12_TC_XST128 : 3; // activation slots
     // per decode warp: one row of 32 BF16 pairs, for patching escapes
     static constexpr int SCR_PITCH = 144;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * SCR_PITCH;
@@ -93,9 +97,9 @@ struct TcSmem {
     static constexpr int NBARS = 2 * WST + 2 * XST + 2 * NA + 4 + 2 + 2 * WST;
     static constexpr int TOTAL = BARS + 8 * NBARS + 32 + 1024; // + slack to align the base
     static constexpr int W_TX = AE + B;
-    static_assert(DCOL + 2 * DW <= 512 && DW >= MT, "tensor memory budget");
-    static_assert(WST >= 3 || (MT == 128 && WST >= 2), "weight ring too shallow");
-    static_assert(XST >= SPU, "activation ring shallower than a unit");
+    static_assert(DCOL + ND * DW <= 512 && DW >= MT, "tensor memory budget");
+    static_assert(WST >= 3 || (MT >= 128 && WST >= 2), "weight ring too shallow");
+    static_assert(XST >= 2, "activation ring too shallow");
     static_assert(TOTAL <= 227 * 1024, "shared memory budget");
 };
 
@@ -364,11 +368,11 @@ __global__ void __maxnreg__(96)
             for (int it = 0; it < n_it; ++it) {
                 const bool seg_start = (it == 0) || (ks == 0);
                 const bool seg_end = (ks == nk - 1) || (it == n_it - 1);
-                const int db = seg & 1;
+                const int db = seg % L::ND;
                 bool ok = true;
-                // accumulator buffer db was last read by the epilogue of segment seg - 2
-                if (seg_start && seg >= 2)
-                    ok = wait_or_abort(acc_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
+                // accumulator buffer db was last read by the epilogue of segment seg - ND
+                if (seg_start && seg >= L::ND)
+                    ok = wait_or_abort(acc_empty0 + 8 * db, ((seg / L::ND) - 1) & 1, a, abort_flag);
                 ok = wait_or_abort(a_full0 + 8 * b, pha, a, abort_flag) && ok;
                 const uint32_t d = tmem + kDCol + L::DW * db;
                 const uint32_t a0 = tmem + b * 128;
@@ -613,8 +617,8 @@ __global__ void __maxnreg__(96)
                 // nothing is written before the previous kernel in the stream
                 // has completed (at once when the activation load waited for it)
                 pdl_wait_prior_grid();
-                const int db = seg & 1;
-                wait_or_abort(acc_full0 + 8 * db, (seg >> 1) & 1, a, abort_flag);
+                const int db = seg % L::ND;
+                wait_or_abort(acc_full0 + 8 * db, (seg / L::ND) & 1, a, abort_flag);
                 __syncwarp();
                 tc_fence_after();
                 constexpr int PART = MT / 4;              // accumulator columns read by this warp
@@ -726,7 +730,8 @@ int tc_smem_bytes(int mt, bool q8)
     case 16: return q8 ? TcSmem<16, true>::TOTAL : TcSmem<16, false>::TOTAL;
     case 32: return q8 ? TcSmem<32, true>::TOTAL : TcSmem<32, false>::TOTAL;
     case 64: return q8 ? TcSmem<64, true>::TOTAL : TcSmem<64, false>::TOTAL;
-    default: return q8 ? TcSmem<128, true>::TOTAL : TcSmem<128, false>::TOTAL;
+    case 128: return q8 ? TcSmem<128, true>::TOTAL : TcSmem<128, false>::TOTAL;
+    default: return q8 ? TcSmem<256, true>::TOTAL : TcSmem<256, false>::TOTAL;
     }
 }
 
@@ -753,6 +758,7 @@ cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const CU
     case 32: return launch_mt<32>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
     case 64: return launch_mt<64>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
     case 128: return launch_mt<128>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 256: return launch_mt<256>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
     }
     return cudaErrorInvalidValue;
 }

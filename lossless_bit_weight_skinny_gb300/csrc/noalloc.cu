@@ -126,7 +126,8 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
         return W12_ERR_UNSUPPORTED;
 
     const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
+                      : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     int sms = 0;
@@ -195,14 +196,5 @@ extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, flo
         return W12_ERR_SHAPE;
     if (M > 256)
         return W12_ERR_UNSUPPORTED;
-    if (M <= 128)
-        return noalloc_impl(x_bf16, w, y, M, N, K, st, false);
-    // 128 activation rows per launch, as w12_gemm
-    if (!x_bf16 || !y)
-        return W12_ERR_INVALID_ARG;
-    const w12_status s1 = noalloc_impl(x_bf16, w, y, 128, N, K, st, false);
-    if (s1 != W12_OK)
-        return s1;
-    return noalloc_impl(static_cast<const uint16_t *>(x_bf16) + static_cast<size_t>(128) * K, w,
-                        y + static_cast<size_t>(128) * N, M - 128, N, K, st, true);
+    return noalloc_impl(x_bf16, w, y, M, N, K, st, false);
 }

@@ -148,19 +148,6 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
         return W12_ERR_UNSUPPORTED;
     if (M == 0 || N == 0)
         return W12_OK;
-    if (M > 128) {
-        // 128 activation rows per launch: the first 128, then the rest (whose
-        // x was complete before the first launch started)
-        if (!x || !y)
-            return W12_ERR_INVALID_ARG;
-        const size_t esz = (out_mode & kOutBF16) ? 2 : 4;
-        w12_status s1 = gemm_impl(x, w, y, 128, N, K, st, q8, x_ready, out_mode);
-        if (s1 != W12_OK)
-            return s1;
-        return gemm_impl(static_cast<const uint16_t *>(x) + static_cast<size_t>(128) * K, w,
-                         static_cast<char *>(y) + esz * 128 * static_cast<size_t>(ldy), M - 128, N, K, st, q8,
-                         true, out_mode);
-    }
     if (!x || !y)
         return W12_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y))
@@ -181,7 +168,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     // kernel for M <= 2; from 3 rows on, the tensor-core kernel (M padded to
     // 16, 32 or 64) is faster than four FMAs per weight.
     const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128) : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
+    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
+                      : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
     const int kstep = tc ? kTcKStep : kFmaKStep;
     GemmArgs a{};
@@ -546,14 +534,6 @@ w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, i
         return W12_OK;
     if (!x || !y)
         return W12_ERR_INVALID_ARG;
-    if (M > 128) {
-        const w12_status s1 = gemm_i8_impl(x, q, y, 128, N, K, st, x_ready, out_mode);
-        if (s1 != W12_OK)
-            return s1;
-        return gemm_i8_impl(static_cast<const uint16_t *>(x) + static_cast<size_t>(128) * K, q,
-                            static_cast<char *>(y) + esz * 128 * static_cast<size_t>(ldy), M - 128, N, K, st, true,
-                            out_mode);
-    }
     if (!aligned16(x) || !aligned16(y))
         return W12_ERR_ALIGNMENT;
     int cur = -1;
@@ -565,8 +545,8 @@ w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, i
         return cudaMemsetAsync(y, 0, esz * static_cast<size_t>(M) * ldy, st) == cudaSuccess ? W12_OK : W12_ERR_CUDA;
     if (!q->gemm_ok)
         return W12_ERR_UNSUPPORTED;
-    // the tensor-core kernel for every M (M padded to 16, 32, 64 or 128)
-    const int mt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+    // the tensor-core kernel for every M (M padded to 16, 32, 64, 128 or 256)
+    const int mt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     GemmArgs a{};
     a.y = y;
     a.out_mode = out_mode;
