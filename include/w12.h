@@ -186,9 +186,8 @@ w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device
  * FP32 [M][N], 16-byte aligned; both caller-owned.  1 <= M <= 256 (M = 0 is
  * a no-op), N and K must equal the handle's; K % 32 == 0 (else UNSUPPORTED).
  * Kernel choice is a function of M only: M <= 2 CUDA-core FMAs with warp
- * reductions, 3..128 tcgen05 tensor cores with TMEM accumulators (one
- * launch; every weight is read once), 129..256 two launches of up to 128
- * activation rows each (the weights are read twice).  Uses a
+ * reductions, 3..256 tcgen05 tensor cores with TMEM accumulators (one
+ * launch; every weight is read once).  Uses a
  * library-owned workspace cached per (device, stream); the first call on a
  * stream allocates it (stream-ordered), so make that first call outside any
  * stream capture.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM,
@@ -282,7 +281,7 @@ w12_status w12_i8_status(const w12_i8 *q, w12_stream_t stream);
  * FP32 accumulation on the tensor cores (every q is exact in BF16).  Arguments,
  * limits, flags (W12_GEMM_INPUT_READY, W12_GEMM_OUT_BF16, W12_GEMM_SILU_MUL;
  * any other bit gives INVALID_ARG) and errors as w12_gemm_ex.  Every M runs on
- * the tensor-core kernel (M padded to 16, 32, 64 or 128).
+ * the tensor-core kernel (M padded to 16, 32, 64, 128 or 256).
  */
 w12_status w12_gemm_i8(const void *x_bf16, const w12_i8 *q, void *y, int M, int N, int K, unsigned flags,
                        w12_stream_t stream);
@@ -304,9 +303,9 @@ w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, 
  * convenience.)  Same arguments, result and errors as w12_gemm, but the
  * split-K scratch comes from one fixed 16 MiB array in device memory that
  * every GPU loading this library holds until exit; a call needing more
- * (over 8192 row blocks, or more than 2 * CTAs * M * 128 FP32 partial sums,
- * M counted per launch of at most 128 rows -- on a 152-SM GB300 that is M
- * above about 107) fails with W12_ERR_UNSUPPORTED.  All calls on a device share the
+ * (over 8192 row blocks, or more than 2 * CTAs * M * 128 FP32 partial sums
+ * -- on a 152-SM GB300, M above about 107 on most shapes) fails with
+ * W12_ERR_UNSUPPORTED.  All calls on a device share the
  * array, so calls whose kernels overlap on the GPU (other streams, other
  * threads) race: serialise them.  The first call on each device looks up the
  * array, clears its counters and synchronises the device; make it before any
