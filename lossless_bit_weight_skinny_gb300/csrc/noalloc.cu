@@ -150,7 +150,8 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     a.n_kstep = static_cast<int>(ceil_div(K, kstep));
     const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
     const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sms * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep, tc ? sms : sms * fma_ctas_per_sm(mt) - W12_FMA_SM_RESERVE,
+                                 min_iters);
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     // the fixed array must hold the counters and the partial sums of this call
     if (iters > (int64_t(1) << 30) || static_cast<size_t>(a.n_rowblk) * 8 > kNoAllocCounterBytes ||

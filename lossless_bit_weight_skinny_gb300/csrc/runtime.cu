@@ -199,7 +199,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     // streams several times the weight bytes of the partial sums it writes
     // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
     const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur) * (tc ? 1 : fma_ctas_per_sm(mt)), min_iters);
+    const int grid = choose_grid(a.n_rowblk, a.n_kstep,
+                                 tc ? sm_count(cur) : sm_count(cur) * fma_ctas_per_sm(mt) - W12_FMA_SM_RESERVE, min_iters);
 
     const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
     w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters);
