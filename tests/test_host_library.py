@@ -211,3 +211,18 @@ def test_no_oracle_on_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f
+
+
+def test_c_client_compiles_and_runs(w12, tmp_path):
+    """include/w12.h is plain C99, and a C program linked against the library
+    drives the host-side calls without Python or a GPU."""
+    src = os.path.join(ROOT, "tests", "c_abi", "host_roundtrip.c")
+    exe = str(tmp_path / "host_roundtrip")
+    libdir = os.path.dirname(w12.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe,
+                    "-L", libdir, "-lw12", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("ok")
+    esc = [int(line.split()[3]) for line in r.stdout.splitlines() if line.startswith("window rule")]
+    assert len(esc) == 2 and esc[1] <= esc[0]
