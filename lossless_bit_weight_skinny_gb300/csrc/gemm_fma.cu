@@ -664,11 +664,29 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     // thread 0's release-acquire arrival (cumulativity), and that
                     // arrival before everyone's reads of the other partials
                     named_bar_sync(1, CW * 32);
-                    if (threadIdx.x == 0)
-                        *seg_last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1 : 0;
-                    named_bar_sync(1, CW * 32);
-                    if (*seg_last)
-                        sk_reduce_block<true>(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
+                    if constexpr (MT == 1) {
+                        // one row's partials are 512 bytes a contributor: warp 0
+                        // alone arrives and, if last, sums them (the warp barrier
+                        // orders lane 0's acquire before its lanes' reads) while
+                        // the other warps go on with the next stage (measured on
+                        // GB300: a single-row layer step 108.9 -> 108.0 us; at
+                        // two rows one warp is too few)
+                        if (warp == 0) {
+                            uint32_t last = 0u;
+                            if (lane == 0)
+                                last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1u : 0u;
+                            last = __shfl_sync(0xffffffffu, last, 0);
+                            __syncwarp();
+                            if (last)
+                                sk_reduce_block<true>(a, rb, RBLK, grid, c_first, c_last, lane, 32);
+                        }
+                    } else {
+                        if (threadIdx.x == 0)
+                            *seg_last = sk_arrive(a.counters + rb, c_last - c_first + 1) ? 1 : 0;
+                        named_bar_sync(1, CW * 32);
+                        if (*seg_last)
+                            sk_reduce_block<true>(a, rb, RBLK, grid, c_first, c_last, threadIdx.x, CW * 32);
+                    }
                 }
             }
             // next iteration: (row block, k step) and ring slot
