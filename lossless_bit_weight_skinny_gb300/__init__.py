@@ -356,10 +356,7 @@ def w12_gemm_i8(x, q: I8, y=None, stream=None, input_ready=False, out_bf16=False
     M, K = x.shape
     cols = q.N // 2 if silu_mul else q.N
     dt = torch.bfloat16 if out_bf16 else torch.float32
-    if y is None:
-        y = torch.empty((M, cols), dtype=dt, device=x.device)
-    elif y.dtype != dt or not y.is_cuda or y.numel() < M * cols:
-        raise TypeError(f"y must be a CUDA {dt} tensor of at least {M} x {cols} elements")
+    y = _out(x, y, M, cols, dt)
     flags = ((W12_GEMM_INPUT_READY if input_ready else 0) | (W12_GEMM_OUT_BF16 if out_bf16 else 0)
              | (W12_GEMM_SILU_MUL if silu_mul else 0))
     _check(_lib.w12_gemm_i8(ctypes.c_void_p(x.data_ptr()), q.ptr, ctypes.c_void_p(y.data_ptr()), M, q.N, K, flags,
@@ -374,13 +371,25 @@ def w12_download(d: Dev, stream=None) -> Host:
     return Host(out.value, d.N, d.K)
 
 
+def _out(x, y, M, cols, dt):
+    """The output buffer: a new [M][cols] tensor of dtype dt, or the caller's,
+    which must be a contiguous CUDA tensor of that dtype on x's device with at
+    least M * cols elements."""
+    import torch
+    if y is None:
+        return torch.empty((M, cols), dtype=dt, device=x.device)
+    if not (isinstance(y, torch.Tensor) and y.is_cuda and y.dtype == dt and y.is_contiguous()
+            and y.device == x.device and y.numel() >= M * cols):
+        raise TypeError(f"y must be a contiguous CUDA {dt} tensor on {x.device} of at least {M} x {cols} elements")
+    return y
+
+
 def _gemm(fn, name, x, d: Dev, y=None, stream=None):
     import torch
     if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
         raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
     M, K = x.shape
-    if y is None:
-        y = torch.empty((M, d.N), dtype=torch.float32, device=x.device)
+    y = _out(x, y, M, d.N, torch.float32)
     _check(fn(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
               _stream_ptr(stream)), name)
     return y
@@ -409,10 +418,7 @@ def w12_gemm_ex(x, d: Dev, y=None, stream=None, q8view=False, input_ready=False,
     M, K = x.shape
     cols = d.N // 2 if silu_mul else d.N
     dt = torch.bfloat16 if out_bf16 else torch.float32
-    if y is None:
-        y = torch.empty((M, cols), dtype=dt, device=x.device)
-    elif y.dtype != dt or not y.is_cuda or y.numel() < M * cols:
-        raise TypeError(f"y must be a CUDA {dt} tensor of at least {M} x {cols} elements")
+    y = _out(x, y, M, cols, dt)
     flags = ((W12_GEMM_Q8VIEW if q8view else 0) | (W12_GEMM_INPUT_READY if input_ready else 0)
              | (W12_GEMM_OUT_BF16 if out_bf16 else 0) | (W12_GEMM_SILU_MUL if silu_mul else 0))
     _check(_lib.w12_gemm_ex(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
