@@ -197,6 +197,36 @@ def pin_escape_list_structure(lib=None):
 
 # ---- the 8-bit view ------------------------------------------------------------
 
+def pin_tiny_composition(lib=None):
+    """The 512 x 256 configuration: its 13 forced zeros escape at their
+    positions; each row holding a +-50 outlier has window base 117 (50 =
+    1.5625 * 2^5, biased exponent 132, minus 15) and escapes exactly its
+    weights below 2^-10 (plus its zeros); every other escape is a zero or lies
+    below its own row's window."""
+    W, _, zpos, opos = WL.tiny_weights(1)
+    N, K = W.shape
+    blob = O.encode(W, lib=lib)
+    ebase, ae, bpl, tptr, esc = _blob_arrays(blob, N, K)
+    tiles_c = (K + 255) // 256
+    escaped = set()
+    for t in range(len(tptr) - 1):
+        n0, k0 = (t // tiles_c) * 128, (t % tiles_c) * 256
+        for e in esc[tptr[t]:tptr[t + 1]]:
+            escaped.add((n0 + (int(e) >> 24), k0 + ((int(e) >> 16) & 0xFF)))
+    assert len(escaped) == len(esc)
+    for p in zpos:
+        assert (p // K, p % K) in escaped
+    orows = sorted({int(p) // K for p in opos})
+    for n in orows:
+        assert int(ebase[n]) == 117, (n, int(ebase[n]))
+        row = W[n].astype(np.int32)
+        small = ((row & 0x7FFF) < (117 << 7))  # |w| < 2^-10, zeros included
+        assert {(n, k) for k in range(K) if small[k]} == {(n, k) for (m, k) in escaped if m == n}
+    for (n, k) in escaped:
+        e = (int(W[n, k]) >> 7) & 0xFF
+        assert (int(W[n, k]) & 0x7FFF) == 0 or e < int(ebase[n])
+
+
 def pin_q8_nesting(lib=None):
     """Q8 = the weight with its low four mantissa bits cleared (in window);
     escaped slots read +-2^(ebase-127); the AE byte is the record's top byte."""
@@ -561,6 +591,7 @@ FAST_PINS = (
     pin_roundtrip,
     pin_escape_list_structure,
     pin_q8_nesting,
+    pin_tiny_composition,
     pin_gemm_numpy,
     pin_gemm_one_hot,
     pin_gemm_exact_integers,

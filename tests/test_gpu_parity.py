@@ -132,6 +132,24 @@ def test_gemm_parity(w12, name, M):
     _check(_gemm(w12, d, x), x, Wdec, what=f"{name} M={M}")
 
 
+def test_error_statistics_logged(w12, capsys):
+    """The gating bound is 2^-8 sum|x w|; this logs how far inside it the
+    results are (largest ratio, and the share of elements above 2^-16)."""
+    W, Wdec, Wq, d = _prepared(w12, "rows_200x4096")
+    lines = []
+    for M in (1, 2, 16, 64, 128, 256):
+        x = WL.activations(M, W.shape[1], seed=5000 + M)
+        y = _gemm(w12, d, x)
+        ref = O.gemm_rows(x, Wdec)
+        scale = O.abs_gemm(x, Wdec)
+        r = np.abs(y - ref) / np.maximum(scale, 1e-300)
+        assert r.max() <= BOUND
+        lines.append(f"M={M}: max err/sum|xw| = 2^{np.log2(max(r.max(), 2.0 ** -60)):.1f}, "
+                     f"share above 2^-16 = {np.mean(r > 2.0 ** -16):.4f}")
+    with capsys.disabled():
+        print("\n" + "\n".join(lines))
+
+
 @pytest.mark.parametrize("M", (1, 2, 4, 8, 16, 32, 64, 128, 256))
 @pytest.mark.parametrize("name", list(SHAPES.keys()))
 def test_q8view_parity(w12, name, M):
