@@ -278,6 +278,18 @@ def run_w12(args):
             graph_ev.replay()
             torch.cuda.synchronize()
     clocks = sampler.stop()
+    # per-replay spread of the same graph (after the timed region): each
+    # replay between its own event pair, so median and minimum per step
+    n_rep = min(reps, 50)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+    for e0, e1 in rev:
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per_step = sorted(1e3 * e0.elapsed_time(e1) / G for e0, e1 in rev)
+    step_stats = {"median_us": round(per_step[len(per_step) // 2], 2), "min_us": round(per_step[0], 2),
+                  "max_us": round(per_step[-1], 2), "replays": n_rep, "steps_per_replay": G}
     args.steps = reps * G
     step_bytes = _step_bytes(layers[0], M)
     ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * args.steps, dist, "cuda")
@@ -661,6 +673,7 @@ def run_w12(args):
             "e2e": e2e,
             "gpu_launches": n_launch,
             "clocks": clocks,
+            "us_per_layer_spread": step_stats,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -701,6 +714,25 @@ def _oracle_pass(sample, threads):
         list(ex.map(job, sample))
 
 
+def _cpu_model() -> str:
+    import platform
+
+    info = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    info.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    if "model name" in info:
+        return info["model name"]
+    if "cpu part" in info:  # Arm: implementer and part number
+        return f"{platform.machine()} (CPU implementer {info.get('cpu implementer', '?')}, part {info['cpu part']})"
+    return f"{platform.machine()} {platform.processor()}".strip()
+
+
 def cpu_baseline(seconds_budget: float):
     """The oracle as it stands, timed on this host's cores on a bounded sample."""
     import oracle as O
@@ -720,7 +752,11 @@ def cpu_baseline(seconds_budget: float):
         _oracle_pass(sample, threads)
     dt = (time.perf_counter() - t) / reps
     nbytes = sum(s[5] for s in sample)
+    t = time.perf_counter()
+    _oracle_pass(sample, 1)
+    dt1 = time.perf_counter() - t
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "value_1_thread": round(nbytes / dt1 / 1e9, 4), "cpu_model": _cpu_model(),
             "kind": "oracle",
             "sample": f"first 1/{frac} of the rows of each of the 7 projections of one layer, "
                       f"M=1: oracle decode + float64 GEMM, projections in parallel threads, "
