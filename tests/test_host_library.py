@@ -8,6 +8,7 @@ format round-trips.
 import os
 import re
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -226,3 +227,17 @@ def test_c_client_compiles_and_runs(w12, tmp_path):
     assert r.stdout.strip().endswith("ok")
     esc = [int(line.split()[3]) for line in r.stdout.splitlines() if line.startswith("window rule")]
     assert len(esc) == 2 and esc[1] <= esc[0]
+
+
+def test_package_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package without its built library refuses to import:
+    there is no fallback path."""
+    import shutil
+
+    pkg = tmp_path / "lossless_bit_weight_skinny_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "lossless_bit_weight_skinny_gb300", "__init__.py"), pkg / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import lossless_bit_weight_skinny_gb300"], cwd=str(tmp_path),
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "not built" in r.stderr
