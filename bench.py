@@ -772,8 +772,18 @@ def run_reference(args):
     O.build()
     cores = len(os.sched_getaffinity(0))
     threads = min(cores, len(WL.LAYER_PROJECTIONS))
+    # each step is a bounded sample (the first 1/frac of every projection's
+    # rows), sized so that warm-up + steps take about 150 s in all
     frac = 64
     sample = _oracle_sample(frac)
+    t = time.perf_counter()
+    _oracle_pass(sample, threads)
+    probe = time.perf_counter() - t
+    per_step = min(0.25, 150.0 / max(1, args.steps + args.warmup))
+    while frac < 8192 and probe * 64 / frac > per_step:
+        frac *= 2
+    if frac != 64:
+        sample = _oracle_sample(frac)
     for _ in range(args.warmup):
         _oracle_pass(sample, threads)
     t = time.perf_counter()
