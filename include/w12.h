@@ -205,6 +205,31 @@ w12_status w12_gemm(const void *x_bf16, const w12_dev *w, float *y, int M, int N
 w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
                            w12_stream_t stream);
 
+/*
+ * The launch a GEMM of M x N x K makes on a GPU with `sm_count` SMs (0: the
+ * current device's), without running it -- the same planning w12_gemm uses.
+ * kernel: 1 the CUDA-core kernel (M <= 2), 2 the tensor-core kernel; 0 when
+ * nothing is launched (M, N or K zero).  The weights are split into
+ * row_blocks x k_steps units of block_rows x 256; split_row_blocks counts row
+ * blocks shared by several CTAs, whose partial sums a split-K fix-up combines
+ * (inside the GEMM, or as a second kernel when separate_fixup is 1), using
+ * partial_bytes of scratch.  Errors: INVALID_ARG, UNSUPPORTED (as w12_gemm:
+ * M above 256, K % 32 != 0), CUDA (no device to ask for its SM count).
+ */
+typedef struct {
+    int kernel;
+    int tile_rows;       /* activation rows per tile: 1, 2, 16, 32, 64, 128 or 256 */
+    int block_rows;      /* weight rows per row block: 64 or 128 */
+    int grid;            /* CTAs */
+    int64_t row_blocks;
+    int64_t k_steps;
+    int64_t split_row_blocks;
+    int separate_fixup;
+    size_t partial_bytes;
+} w12_gemm_plan_t;
+
+w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count, w12_gemm_plan_t *out);
+
 /* Flags of w12_gemm_ex. */
 enum {
     W12_GEMM_Q8VIEW = 1,      /* the Q pass (as w12_gemm_q8view) instead of the exact GEMM */

@@ -44,6 +44,17 @@ _I = ctypes.c_int
 _ST = ctypes.c_int
 
 
+class GemmPlan(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int), ("tile_rows", ctypes.c_int), ("block_rows", ctypes.c_int),
+        ("grid", ctypes.c_int), ("row_blocks", ctypes.c_int64), ("k_steps", ctypes.c_int64),
+        ("split_row_blocks", ctypes.c_int64), ("separate_fixup", ctypes.c_int), ("partial_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
 class Stats(ctypes.Structure):
     _fields_ = [
         ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("n_escapes", ctypes.c_int64),
@@ -85,6 +96,7 @@ _sig("w12_i8_free", [_P], None)
 _sig("w12_i8_download", [_P, _P, _P, _P])
 _sig("w12_i8_status", [_P, _P])
 _sig("w12_gemm_i8", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
+_sig("w12_gemm_plan", [_I, _I64, _I64, _I, ctypes.POINTER(GemmPlan)])
 _sig("w12_download", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
@@ -107,6 +119,7 @@ EXPORTED = (
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
     "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
     "w12_i8_encode_device", "w12_i8_from_dev", "w12_i8_free", "w12_i8_download", "w12_i8_status", "w12_gemm_i8",
+    "w12_gemm_plan",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -470,3 +483,11 @@ def w12_debug_inject_stall(on: bool):
 def lib():
     """The loaded ctypes library (for tests that call the C ABI directly)."""
     return _lib
+
+
+def w12_gemm_plan(M: int, N: int, K: int, sm_count: int = 0) -> dict:
+    """The launch w12_gemm makes for M x N x K on a GPU with sm_count SMs
+    (0: the current device's): kernel, tile rows, grid, split-K shape."""
+    p = GemmPlan()
+    _check(_lib.w12_gemm_plan(M, N, K, sm_count, ctypes.byref(p)), "w12_gemm_plan")
+    return p.as_dict()

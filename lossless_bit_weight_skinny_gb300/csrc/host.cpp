@@ -186,7 +186,7 @@ const char *w12_status_string(w12_status s)
     case W12_ERR_INVALID_ARG: return "invalid argument";
     case W12_ERR_SHAPE: return "shape does not match the encoded matrix";
     case W12_ERR_ALIGNMENT: return "device buffer not 16-byte aligned";
-    case W12_ERR_UNSUPPORTED: return "unsupported size (M must be 1..64, K % 32 == 0)";
+    case W12_ERR_UNSUPPORTED: return "unsupported size (M must be 0..256, K % 32 == 0)";
     case W12_ERR_OOM: return "out of memory";
     case W12_ERR_CUDA: return "CUDA error";
     case W12_ERR_CORRUPT: return "encoded matrix is corrupt";

@@ -133,6 +133,44 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 constexpr int kMaxM = 256;
 
+// The launch of one GEMM: kernel, tile rows, grid and split-K shape.  Kernel
+// choice is a function of M only (measured on GB300): the CUDA-core kernel for
+// M <= 2; from 3 rows on, the tensor-core kernel (M padded to 16, 32, 64, 128
+// or 256) is faster than four FMAs per weight.
+struct Plan {
+    bool tc = false;
+    int mt = 0, rows_blk = 0, kstep = 0, grid = 0;
+    int64_t n_rowblk = 0, n_kstep = 0, iters = 0;
+    bool defer = false;
+    size_t part_bytes = 0;
+};
+
+w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p)
+{
+    Plan q;
+    q.tc = M >= W12_TC_MIN_M;
+    q.mt = q.tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
+                : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
+    q.rows_blk = q.tc ? kTcRows : fma_rows_blk(q.mt);
+    q.kstep = q.tc ? kTcKStep : kFmaKStep;
+    q.n_rowblk = ceil_div(N, q.rows_blk);
+    q.n_kstep = ceil_div(K, q.kstep);
+    q.iters = q.n_rowblk * q.n_kstep;
+    if (q.iters > (1ll << 30) || q.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
+        return W12_ERR_UNSUPPORTED;
+    q.defer = q.tc && tc_defer(M);
+    // one CTA per SM (four left out for the CUDA-core kernel); for large M on
+    // few row blocks, fewer CTAs so that each streams several times the weight
+    // bytes of the partial sums it writes (a 128 x 256 tensor-core unit reads
+    // 48 KB of W12, its partial is M x 512 B)
+    const int64_t min_iters = q.tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
+    q.grid = choose_grid(q.n_rowblk, q.n_kstep, q.tc ? sms : sms * fma_ctas_per_sm(q.mt) - W12_FMA_SM_RESERVE,
+                         min_iters);
+    q.part_bytes = sizeof(float) * 2 * static_cast<size_t>(q.grid) * M * q.rows_blk;
+    *p = q;
+    return W12_OK;
+}
+
 w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
                      cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
 {
@@ -164,14 +202,12 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     if (!w->gemm_ok)
         return W12_ERR_UNSUPPORTED;
 
-    // Kernel choice, a function of M only (measured on GB300): the CUDA-core
-    // kernel for M <= 2; from 3 rows on, the tensor-core kernel (M padded to
-    // 16, 32 or 64) is faster than four FMAs per weight.
-    const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
-                      : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
-    const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
-    const int kstep = tc ? kTcKStep : kFmaKStep;
+    Plan pl;
+    const w12_status ps = make_plan(M, N, K, sm_count(cur), &pl);
+    if (ps != W12_OK)
+        return ps;
+    const bool tc = pl.tc;
+    const int mt = pl.mt, rows_blk = pl.rows_blk, grid = pl.grid;
     GemmArgs a{};
     a.ebase = w->ebase;
     a.tile_ptr = w->tile_ptr;
@@ -185,25 +221,15 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     a.N = N;
     a.K = K;
     a.tiles_c = static_cast<int>(w->tiles_c);
-    a.n_rowblk = static_cast<int>(ceil_div(N, rows_blk));
-    a.n_kstep = static_cast<int>(ceil_div(K, kstep));
-    const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
-    if (iters > (1ll << 30) || a.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
-        return W12_ERR_UNSUPPORTED;
-    a.total_iters = static_cast<int>(iters);
+    a.n_rowblk = static_cast<int>(pl.n_rowblk);
+    a.n_kstep = static_cast<int>(pl.n_kstep);
+    a.total_iters = static_cast<int>(pl.iters);
     a.limit_ns = g_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
     a.x_ready = x_ready ? 1 : 0;
-    a.defer = tc && tc_defer(M);
-    // one CTA per SM; for large M on few row blocks, fewer CTAs so that each
-    // streams several times the weight bytes of the partial sums it writes
-    // (a 128 x 256 tensor-core unit reads 48 KB of W12, its partial is M x 512 B)
-    const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep,
-                                 tc ? sm_count(cur) : sm_count(cur) * fma_ctas_per_sm(mt) - W12_FMA_SM_RESERVE, min_iters);
+    a.defer = pl.defer;
 
-    const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
-    w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters);
+    w12_status ws = get_workspace(cur, st, pl.part_bytes, &a.partials, &a.counters);
     if (ws != W12_OK)
         return ws;
 
@@ -383,6 +409,48 @@ w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M
                            w12_stream_t stream)
 {
     return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count_arg, w12_gemm_plan_t *out)
+{
+    if (!out || M < 0 || N < 0 || K < 0)
+        return W12_ERR_INVALID_ARG;
+    *out = w12_gemm_plan_t{};
+    if (M > kMaxM || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return W12_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0 || K == 0)
+        return W12_OK; // nothing is launched
+    if (K % 32 != 0)
+        return W12_ERR_UNSUPPORTED;
+    int sms = sm_count_arg;
+    if (sms <= 0) {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess)
+            return W12_ERR_CUDA;
+        sms = sm_count(cur);
+        if (sms <= 0)
+            return W12_ERR_CUDA;
+    }
+    Plan pl;
+    const w12_status ps = make_plan(M, N, K, sms, &pl);
+    if (ps != W12_OK)
+        return ps;
+    out->kernel = pl.tc ? 2 : 1;
+    out->tile_rows = pl.mt;
+    out->block_rows = pl.rows_blk;
+    out->grid = pl.grid;
+    out->row_blocks = pl.n_rowblk;
+    out->k_steps = pl.n_kstep;
+    int64_t split = 0;
+    const int it = static_cast<int>(pl.iters);
+    for (int64_t rb = 0; rb < pl.n_rowblk; ++rb)
+        if (sk_owner(static_cast<int>(rb * pl.n_kstep), pl.grid, it) !=
+            sk_owner(static_cast<int>((rb + 1) * pl.n_kstep - 1), pl.grid, it))
+            ++split;
+    out->split_row_blocks = split;
+    out->separate_fixup = pl.defer && split > 0 ? 1 : 0;
+    out->partial_bytes = split > 0 ? pl.part_bytes : 0;
+    return W12_OK;
 }
 
 w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int N, int K,

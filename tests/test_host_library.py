@@ -241,3 +241,48 @@ def test_package_fails_loudly_without_the_library(tmp_path):
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
     assert "ImportError" in r.stderr and "not built" in r.stderr
+
+
+@pytest.mark.parametrize("M,N,K,kernel,tile,grid,split", [
+    (1, 17408, 5120, 1, 1, 136, 0),    # aligned: one whole row block per CTA
+    (1, 1024, 5120, 1, 1, 80, 8),      # aligned: 10 CTAs share each of 8 row blocks
+    (1, 5120, 5120, 1, 1, 148, 40),    # stream-K over 152 - 4 SMs
+    (1, 5120, 17408, 1, 1, 148, 40),
+    (2, 5120, 5120, 1, 2, 148, 40),
+    (3, 5120, 5120, 2, 16, 152, 40),   # tensor cores from 3 rows
+    (16, 17408, 5120, 2, 16, 136, 0),
+    (64, 17408, 5120, 2, 64, 136, 0),
+    (65, 1024, 5120, 2, 128, 80, 8),
+    (256, 17408, 5120, 2, 256, 136, 0),
+])
+def test_gemm_plan_projection_shapes(w12, M, N, K, kernel, tile, grid, split):
+    """The launch planning w12_gemm uses, for the projection shapes on a
+    152-SM GB300 (kernel by M, tile rows, grid, split row blocks)."""
+    p = w12.w12_gemm_plan(M, N, K, 152)
+    assert (p["kernel"], p["tile_rows"], p["grid"], p["split_row_blocks"]) == (kernel, tile, grid, split)
+    assert p["separate_fixup"] == (1 if (M > 64 and split) else 0)
+
+
+def test_gemm_plan_invariants(w12):
+    rng = np.random.Generator(np.random.PCG64(77))
+    for _ in range(300):
+        M = int(rng.integers(1, 257))
+        N = int(rng.integers(1, 40000))
+        K = 32 * int(rng.integers(1, 700))
+        sms = int(rng.choice([8, 76, 132, 152]))
+        p = w12.w12_gemm_plan(M, N, K, sms)
+        units = p["row_blocks"] * p["k_steps"]
+        assert p["kernel"] == (1 if M <= 2 else 2)
+        assert p["tile_rows"] >= M and (p["tile_rows"] == M or p["tile_rows"] // 2 < M or p["tile_rows"] == 16)
+        assert p["row_blocks"] == -(-N // p["block_rows"]) and p["k_steps"] == -(-K // 256)
+        assert 1 <= p["grid"] <= min(units, sms - (4 if M <= 2 else 0))
+        assert 0 <= p["split_row_blocks"] <= p["row_blocks"]
+        if p["split_row_blocks"]:
+            assert p["partial_bytes"] == 4 * 2 * p["grid"] * M * p["block_rows"]
+        else:
+            assert p["partial_bytes"] == 0
+    assert w12.w12_gemm_plan(0, 5, 5, 152)["kernel"] == 0
+    with pytest.raises(w12.W12Error):
+        w12.w12_gemm_plan(1, 64, 200, 152)   # K % 32 != 0
+    with pytest.raises(w12.W12Error):
+        w12.w12_gemm_plan(257, 64, 256, 152)
