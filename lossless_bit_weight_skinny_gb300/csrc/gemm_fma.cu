@@ -3,7 +3,7 @@
 //
 // y[m][n] = sum_k x[m][k] * W[n][k], W decoded from its W12 planes to exact
 // BF16 values (SpecPilot, Figure 5(a) caption) in registers and accumulated in
-// FP32 with packed f32x2 FMAs.
+// FP32 with BF16 x BF16 -> FP32 FMAs (packed FP32 FMAs with W12_FMA_MIXED=0).
 //
 // Work split: the matrix is cut into blocks of RBLK rows x 256 columns (one
 // escape tile wide); the (row block, k step) iterations are split evenly over
@@ -23,9 +23,11 @@
 // work at all.  The escape warps (even and odd units) walk each stage's list
 // and keep, per output, the two correction sums sum(-x * placeholder) and
 // sum(x * exact value) in shared memory; the consumers add them to the output
-// in that order at the end of the row block.  With a single non-zero product (one-hot x) this gives
-// the exact escaped value back, Inf/NaN escapes propagate, and otherwise the
-// result is the same sum in another (fixed) order.
+// in that order at the end of the row block.  With a single non-zero product
+// (one-hot x) this gives the exact escaped value back, Inf/NaN escapes
+// propagate, and otherwise the result is the same sum in another (fixed)
+// order.  The final store goes through the output mode (FP32, BF16, SiLU*mul
+// of interleaved gate/up rows).
 #include "kernels.cuh"
 
 namespace w12 {

@@ -1,5 +1,5 @@
 // gemm_tc.cu -- W12 skinny GEMM on the tcgen05 tensor cores (activation rows
-// padded to MT = 16, 32 or 64).
+// padded to MT = 16, 32, 64, 128 or 256).
 //
 // The product is computed transposed: D[n][m] = sum_k W[n][k] x[m][k], with the
 // decoded weight tile as the MMA "A" operand (128 output channels x 16 k per
@@ -11,25 +11,33 @@
 // reads A from there, so decoded weights never touch shared memory.
 //
 // Work unit: 128 rows x 256 columns, exactly one escape tile.  The (row block,
-// k step) units are split evenly over one persistent CTA per SM (stream-K);
-// row blocks shared by several CTAs are combined by the last contributor in a
-// fixed order.
+// k step) units are split over one persistent CTA per SM (stream-K, or whole
+// row blocks when that is cheaper); row blocks shared by several CTAs are
+// combined in a fixed order, by the last contributor or, above 64 rows, by the
+// separate fix-up kernel (reduce.cu).
 //
 // CTA = 16 decode warps + a weight-TMA warp + an activation-TMA warp + an MMA
-// warp, over three independent rings:
-//   * weights (AE, B, the tile's escape entries) in shared memory;
-//   * activations (the MMA's B operand) in shared memory, released by the MMA;
+// warp + an escape warp, over three rings:
+//   * weights (AE and B planes) in shared memory, handed back by the decode
+//     warps as soon as they hold their raw planes in registers;
+//   * activations (the MMA's B operand) in shared memory, released by the MMA:
+//     a unit's four 64-column sub-tiles per slot up to 64 rows, one sub-tile
+//     per slot from 128 rows;
 //   * decoded weights (the A operand, 128 TMEM columns per unit), released by
 //     the MMA.
 // Decode warp (q, c) owns rows 32q..32q+31 of the unit (its TMEM lane
 // quadrant) and columns 64c..64c+63.  Each thread decodes 64 weights of its
-// row into 32 BF16x2 registers and stores them with one tcgen05.st.  Escapes
-// are then patched in tensor memory: the warp finds the entries of its
-// quadrant that fall in its columns with one ballot, and for each rewrites the
-// one 32-bit column holding the slot (load, replace the 16-bit half in the
-// owning lane, store back; every other lane writes its own value back).
-// Accumulators are double buffered so that the epilogue of one row block
-// overlaps the first products of the next.
+// row into 32 BF16x2 registers.  The escape warp reads each unit's escape list
+// from global memory, up to a ring ahead, and sorts it into one short list per
+// decode warp; after decoding, a decode warp overwrites its escaped slots in
+// registers (through a small per-warp scratch row) and stores the 32 registers
+// with one tcgen05.st.  Accumulators are double buffered up to 128 rows, so
+// the epilogue of one row block overlaps the first products of the next; at
+// 256 rows there is one 256-column buffer.
+//
+// Template flags: Q8 (the Q pass over the AE plane alone), EPI (the output
+// modes: BF16, SiLU*mul; the plain FP32 store is a kernel of its own) and I8
+// (an INT8 copy's bytes in place of the AE plane, row scales at the end).
 #include "kernels.cuh"
 
 namespace w12 {
