@@ -584,6 +584,18 @@ def pin_bits_per_weight(lib=None):
     return bpw
 
 
+def pin_converted_size(lib=None):
+    """The pages' converted size: 44.67 GB of BF16 layers become 33.58 GB,
+    i.e. 16 * 33.58 / 44.67 = 12.03 bits per weight.  The format's own
+    accounting on normal weights (every byte of the blob) must land within
+    0.5 % of that."""
+    fig = printed_figures()
+    bpw = pin_bits_per_weight(lib)
+    predicted = fig["converted_gb_before"] * bpw / 16.0
+    assert abs(predicted - fig["converted_gb_after"]) <= 0.005 * fig["converted_gb_after"], (predicted, bpw)
+    return predicted
+
+
 FAST_PINS = (
     pin_worked_example,
     pin_all_patterns,

@@ -21,3 +21,8 @@ def test_escape_fraction_k17408():
 def test_bits_per_weight():
     bpw = P.pin_bits_per_weight(None)
     assert bpw < 12.01
+
+
+def test_converted_size_matches_printed():
+    predicted = P.pin_converted_size()
+    print(f"predicted converted size {predicted:.2f} GB (printed 33.58 GB)")
