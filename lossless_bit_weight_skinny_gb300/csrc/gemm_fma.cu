@@ -100,16 +100,18 @@ struct FmaSmem {
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const GemmArgs &a,
                                               volatile int *abort_flag)
 {
-    if (*abort_flag)
-        return false;
+    // the flag (a shared-memory load, queued behind this warp's other loads)
+    // is read only once the phase is found incomplete
     if (mbar_try_wait(bar, parity))
         return true;
+    if (*abort_flag)
+        return false;
+    // each try suspends the warp until the phase completes (or the suspend
+    // hint passes), so a waiting warp takes no issue slots from the others
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity))
-                return true;
+        if (mbar_try_wait(bar, parity))
+            return true;
         if (*abort_flag)
             return false;
         if (globaltimer_ns() - t0 > a.limit_ns) {

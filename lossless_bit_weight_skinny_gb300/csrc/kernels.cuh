@@ -38,6 +38,10 @@ struct GemmArgs {
     int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
     int defer;                     // split row blocks: leave the partials to sk_reduce_kernel
     const float *scale;            // [N] row scales of an INT8 copy (INT8 weights only)
+    // 2^28, 2^24, 2^20: multipliers whose high product words are the B word
+    // shifted right by 4, 8, 12 bits (a kernel argument, so that the shifts
+    // run as multiplies on the FMA pipe beside the decode's logic operations)
+    uint32_t bshift_mul[3];
 };
 
 // Output modes.  kOutBF16: y holds BF16, each FP32 result rounded to the
@@ -263,6 +267,72 @@ __device__ W12_SK_INL void sk_reduce_range(const GemmArgs &a, int rb, int rows_b
                         emit_y(a, m, row0 + r + q, v4[q], v4[(q + 1) & 3]);
                     else
                         static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + row0 + r + q] = v4[q];
+                }
+            }
+        }
+    }
+}
+
+// The last contributor's fix-up with few threads: each thread takes GPT float4
+// groups of (m, 4 rows) at a stride of nthreads and sums every contributor's
+// partial of them in contributor order, two contributors' GPT loads in flight
+// at a time.  The order is fixed, so results are bitwise reproducible.
+template <bool EPI, int GPT>
+__device__ __forceinline__ void sk_reduce_wide(const GemmArgs &a, int rb, int rows_blk, int grid, int c_first,
+                                               int c_last, int tid, int nthreads)
+{
+    const int row0 = rb * rows_blk;
+    const int groups = a.M * rows_blk / 4;
+    const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
+    const float4 *base = reinterpret_cast<const float4 *>(a.partials);
+    const int slot_first = sk_slot(c_first, rb, grid, a.total_iters, a.n_kstep);
+    for (int g0 = tid; g0 < groups; g0 += GPT * nthreads) {
+        float4 acc[GPT];
+#pragma unroll
+        for (int i = 0; i < GPT; ++i)
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = c_first; c <= c_last; c += 2) {
+            const float4 *p0 = base + static_cast<size_t>(c == c_first ? slot_first : 2 * c) * slot4;
+            const bool two = c + 1 <= c_last;
+            const float4 *p1 = base + static_cast<size_t>(2 * (c + 1)) * slot4;
+            float4 v0[GPT], v1[GPT];
+#pragma unroll
+            for (int i = 0; i < GPT; ++i) {
+                const int g = g0 + i * nthreads;
+                if (g < groups) {
+                    v0[i] = __ldcg(p0 + g);
+                    if (two)
+                        v1[i] = __ldcg(p1 + g);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < GPT; ++i) {
+                acc[i].x += v0[i].x;
+                acc[i].y += v0[i].y;
+                acc[i].z += v0[i].z;
+                acc[i].w += v0[i].w;
+                if (two) {
+                    acc[i].x += v1[i].x;
+                    acc[i].y += v1[i].y;
+                    acc[i].z += v1[i].z;
+                    acc[i].w += v1[i].w;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < GPT; ++i) {
+            const int g = g0 + i * nthreads;
+            if (g >= groups)
+                continue;
+            const int m = (4 * g) / rows_blk, r = (4 * g) % rows_blk;
+            const float v4[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (row0 + r + j < a.N) {
+                    if constexpr (EPI)
+                        emit_y(a, m, row0 + r + j, v4[j], v4[(j + 1) & 3]);
+                    else
+                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + row0 + r + j] = v4[j];
                 }
             }
         }
