@@ -190,8 +190,14 @@ w12_status w12_dev_info(const w12_dev *d, int64_t *N, int64_t *K, size_t *device
  * launch; every weight is read once).  Uses a
  * library-owned workspace cached per (device, stream); the first call on a
  * stream allocates it (stream-ordered), so make that first call outside any
- * stream capture.  Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM,
- * CUDA.  Device-side failures are reported by w12_dev_status.
+ * stream capture.  It holds the partial sums of M = 128 on every SM; a later
+ * uncaptured call that needs more (M > 128) moves the stream to a larger
+ * workspace, and the old one stays allocated until w12_release_workspaces, so
+ * CUDA graphs captured earlier keep valid addresses (capturing a call that
+ * would need to grow fails with UNSUPPORTED).  Release workspaces only when
+ * no captured graph that uses them will be replayed again.  Errors:
+ * INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, OOM, CUDA.  Device-side
+ * failures are reported by w12_dev_status.
  */
 w12_status w12_gemm(const void *x_bf16, const w12_dev *w, float *y, int M, int N, int K,
                      w12_stream_t stream);
@@ -352,7 +358,9 @@ w12_status w12_decode(const w12_dev *w, uint16_t *w_bf16_out, w12_stream_t strea
  */
 w12_status w12_dev_status(const w12_dev *w, w12_stream_t stream);
 
-/* Release every cached GEMM workspace of the current device (synchronises). */
+/* Release every cached GEMM workspace of the current device, including those
+ * a growing workspace replaced (synchronises).  CUDA graphs captured with
+ * them must not be replayed afterwards. */
 w12_status w12_release_workspaces(void);
 
 /*

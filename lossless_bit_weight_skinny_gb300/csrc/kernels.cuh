@@ -467,6 +467,33 @@ inline int choose_grid(int64_t n_rowblk, int64_t n_kstep, int sms, int64_t min_i
     return static_cast<int>(best);
 }
 
+// ---- host-side runtime shared by the entry points (runtime.cu) ----
+
+constexpr size_t kCounterBytes = 1 << 16; // split-K arrival counters: room for 8192 row blocks
+
+// The launch of one GEMM: kernel, tile rows, grid and split-K shape.
+struct Plan {
+    bool tc = false;
+    int mt = 0, rows_blk = 0, kstep = 0, grid = 0;
+    int64_t n_rowblk = 0, n_kstep = 0, iters = 0;
+    bool defer = false;
+    size_t part_bytes = 0; // split-K partial sums of the launch
+};
+w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p);
+// 2-D TMA map over a row-major [rows][cols] array of `esize`-byte elements.
+bool make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols,
+               uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+// The activations' map of a GEMM launch with tile rows mt.
+bool make_x_tmap(CUtensorMap *m, const void *x, int M, int K, bool tc, int mt);
+int sm_count(int dev);
+// The wall-time limit of bounded device waits and the stall test hook, as set
+// by w12_set_spin_limit / w12_debug_inject_stall.
+uint64_t spin_limit_ns();
+int inject_stall();
+// Record a CUDA error for w12_last_cuda_error and return W12_ERR_CUDA.
+w12_status cuda_fail(cudaError_t e);
+void set_last_error(const char *msg);
+
 } // namespace w12
 
 struct w12_dev;

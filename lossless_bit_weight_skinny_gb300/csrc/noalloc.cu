@@ -13,9 +13,12 @@
 // Costs and limits:
 //   * every GPU that loads this library reserves kNoAllocScratchBytes (16 MiB)
 //     for the array until the process exits, whether or not it is used;
-//   * calls that would need more scratch than that are rejected with
-//     W12_ERR_UNSUPPORTED (only extreme shapes: more than 8192 row blocks, or a
-//     GPU with so many SMs that 2 * SMs * M * 128 partial sums do not fit);
+//   * the array holds the split-K arrival counters (64 KiB: 8192 row blocks)
+//     and the launch's partial sums, 2 x CTAs x M x 128 FP32 values; a call
+//     that needs more is rejected with W12_ERR_UNSUPPORTED.  On a 152-SM GB300
+//     that is any tensor-core call above about 107 rows whose grid fills every
+//     SM (e.g. 5120 x 5120 or 17408 x 5120 at 128 rows), and matrices of more
+//     than 8192 row blocks;
 //   * every call on a device shares the one array and leaves its contents
 //     behind, so two calls whose kernels overlap on the GPU (different
 //     streams, or different host threads) race and give wrong results --
@@ -35,8 +38,8 @@ using namespace w12;
 
 namespace {
 
-constexpr size_t kNoAllocCounterBytes = size_t(64) << 10; // arrival counters: 8192 row blocks
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20; // counters + split-K partial sums
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20; // arrival counters + split-K partial sums
+static_assert(kCounterBytes < kNoAllocScratchBytes, "scratch too small for the counters");
 
 } // namespace
 
@@ -60,7 +63,7 @@ w12_status noalloc_setup(int dev, unsigned char **out)
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
             return W12_ERR_CUDA;
-        if (cudaMemset(p, 0, kNoAllocCounterBytes) != cudaSuccess)
+        if (cudaMemset(p, 0, kCounterBytes) != cudaSuccess)
             return W12_ERR_CUDA;
         if (cudaDeviceSynchronize() != cudaSuccess)
             return W12_ERR_CUDA;
@@ -68,36 +71,6 @@ w12_status noalloc_setup(int dev, unsigned char **out)
     }
     *out = static_cast<unsigned char *>(g_na_ptr[dev]);
     return W12_OK;
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// TMA descriptor of the activations x[M][K] (BF16), as w12_gemm builds it.
-bool x_tmap(CUtensorMap *m, const void *x, int M, int K, uint32_t box_k, uint32_t box_m,
-            CUtensorMapSwizzle sw)
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    if (!fn)
-        return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {box_k, box_m};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -114,25 +87,26 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     if (!aligned16(x_bf16) || !aligned16(y))
         return W12_ERR_ALIGNMENT;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return W12_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     if (dev != w->device)
         return W12_ERR_INVALID_ARG;
-    if (K == 0)
-        return cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st) == cudaSuccess
-                   ? W12_OK
-                   : W12_ERR_CUDA;
+    if (K == 0) {
+        e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(M) * N, st);
+        return e == cudaSuccess ? W12_OK : cuda_fail(e);
+    }
     if (!w->gemm_ok)
         return W12_ERR_UNSUPPORTED;
 
-    const bool tc = M >= W12_TC_MIN_M;
-    const int mt = tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
-                      : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
-    const int rows_blk = tc ? kTcRows : fma_rows_blk(mt);
-    const int kstep = tc ? kTcKStep : kFmaKStep;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return W12_ERR_CUDA;
+    // the same launch as w12_gemm's (kernel, tile rows, grid, split-K shape)
+    Plan pl;
+    const w12_status ps = make_plan(M, N, K, sm_count(dev), &pl);
+    if (ps != W12_OK)
+        return ps;
+    // the fixed array must hold the counters and the partial sums of this call
+    if (static_cast<size_t>(pl.n_rowblk) * 8 > kCounterBytes || kCounterBytes + pl.part_bytes > kNoAllocScratchBytes)
+        return W12_ERR_UNSUPPORTED;
 
     GemmArgs a{};
     a.ebase = w->ebase;
@@ -146,45 +120,36 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     a.N = N;
     a.K = K;
     a.tiles_c = static_cast<int>(w->tiles_c);
-    a.n_rowblk = static_cast<int>(ceil_div(N, rows_blk));
-    a.n_kstep = static_cast<int>(ceil_div(K, kstep));
-    const int64_t iters = static_cast<int64_t>(a.n_rowblk) * a.n_kstep;
-    const int64_t min_iters = tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
-    const int grid = choose_grid(a.n_rowblk, a.n_kstep, tc ? sms : sms * fma_ctas_per_sm(mt) - W12_FMA_SM_RESERVE,
-                                 min_iters);
-    const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(grid) * M * rows_blk;
-    // the fixed array must hold the counters and the partial sums of this call
-    if (iters > (int64_t(1) << 30) || static_cast<size_t>(a.n_rowblk) * 8 > kNoAllocCounterBytes ||
-        kNoAllocCounterBytes + part_bytes > kNoAllocScratchBytes)
-        return W12_ERR_UNSUPPORTED;
-    a.total_iters = static_cast<int>(iters);
-    a.limit_ns = 200ull * 1000 * 1000;
-    a.inject_stall = 0;
+    a.n_rowblk = static_cast<int>(pl.n_rowblk);
+    a.n_kstep = static_cast<int>(pl.n_kstep);
+    a.total_iters = static_cast<int>(pl.iters);
+    a.limit_ns = spin_limit_ns();
+    a.inject_stall = inject_stall();
     a.x_ready = x_ready ? 1 : 0;
-    a.defer = tc && tc_defer(M);
+    a.defer = pl.defer;
 
     unsigned char *scratch = nullptr;
     const w12_status s = noalloc_setup(dev, &scratch);
     if (s != W12_OK)
         return s;
     a.counters = reinterpret_cast<unsigned long long *>(scratch);
-    a.partials = reinterpret_cast<float *>(scratch + kNoAllocCounterBytes);
+    a.partials = reinterpret_cast<float *>(scratch + kCounterBytes);
 
     CUtensorMap tmx;
-    const bool okx = tc ? x_tmap(&tmx, x_bf16, M, K, 64, mt, CU_TENSOR_MAP_SWIZZLE_128B)
-                        : x_tmap(&tmx, x_bf16, M, K, 256, mt, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!okx)
+    if (!make_x_tmap(&tmx, x_bf16, M, K, pl.tc, pl.mt)) {
+        set_last_error("cuTensorMapEncodeTiled failed for x");
         return W12_ERR_CUDA;
-    const w12_tmap &tae = tc ? w->tm_ae_tc : (rows_blk == 128 ? w->tm_ae_fma128 : w->tm_ae_fma64);
-    const w12_tmap &tb = tc ? w->tm_b_tc : (rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
+    }
+    const w12_tmap &tae = pl.tc ? w->tm_ae_tc : (pl.rows_blk == 128 ? w->tm_ae_fma128 : w->tm_ae_fma64);
+    const w12_tmap &tb = pl.tc ? w->tm_b_tc : (pl.rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
     const CUtensorMap *pae = reinterpret_cast<const CUtensorMap *>(&tae);
     const CUtensorMap *pb = reinterpret_cast<const CUtensorMap *>(&tb);
-    cudaError_t e = tc ? launch_gemm_tc(mt, false, false, a, pae, pb, &tmx, grid, st)
-                       : launch_gemm_fma(mt, false, a, pae, pb, &tmx, grid, st);
+    e = pl.tc ? launch_gemm_tc(pl.mt, false, false, a, pae, pb, &tmx, pl.grid, st)
+              : launch_gemm_fma(pl.mt, false, a, pae, pb, &tmx, pl.grid, st);
     bool red = false;
     if (e == cudaSuccess && a.defer)
-        e = launch_sk_reduce(a, grid, rows_blk, st, &red);
-    return e == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+        e = launch_sk_reduce(a, pl.grid, pl.rows_blk, st, &red);
+    return e == cudaSuccess ? W12_OK : cuda_fail(e);
 }
 
 extern "C" w12_status w12_gemm_noalloc(const void *x_bf16, const w12_dev *w, float *y, int M, int N,

@@ -21,13 +21,24 @@ namespace {
 
 std::atomic<uint64_t> g_limit_ns{200ull * 1000 * 1000}; // bounded waits: 200 ms
 thread_local const char *g_last_error = "no error";
+std::atomic<int> g_inject_stall{0};
+
+} // namespace
+
+namespace w12 {
 
 w12_status cuda_fail(cudaError_t e)
 {
     g_last_error = cudaGetErrorName(e);
     return W12_ERR_CUDA;
 }
-std::atomic<int> g_inject_stall{0};
+void set_last_error(const char *msg) { g_last_error = msg; }
+uint64_t spin_limit_ns() { return g_limit_ns.load(); }
+int inject_stall() { return g_inject_stall.load(); }
+
+} // namespace w12
+
+namespace {
 
 // ---- TMA descriptor encoding through the driver entry point -----------------
 
@@ -51,6 +62,10 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+} // namespace
+
+namespace w12 {
+
 // 2-D map over a row-major [rows][cols] array of `esize`-byte elements.
 bool make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols,
                uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
@@ -65,6 +80,14 @@ bool make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *ba
     return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The activations' map of a GEMM launch: 64-column swizzled boxes of mt rows
+// for the tensor-core kernel, 256-column plain boxes for the CUDA-core one.
+bool make_x_tmap(CUtensorMap *m, const void *x, int M, int K, bool tc, int mt)
+{
+    return tc ? make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, mt, CU_TENSOR_MAP_SWIZZLE_128B)
+              : make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 256, mt, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 CUtensorMap *tmap_of(w12_tmap &t) { return reinterpret_cast<CUtensorMap *>(&t); }
@@ -84,6 +107,10 @@ int sm_count(int dev)
     return cache[dev];
 }
 
+} // namespace w12
+
+namespace {
+
 // ---- workspace cache: one growable buffer per (device, stream) --------------
 
 struct Workspace {
@@ -93,8 +120,9 @@ struct Workspace {
 
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
-
-constexpr size_t kCounterBytes = 1 << 16; // room for 8192 row blocks
+// Workspaces replaced by a larger one.  A CUDA graph captured earlier may
+// still hold their addresses, so they are kept until w12_release_workspaces.
+std::vector<std::pair<int, void *>> g_ws_retired;
 
 // Returns partial-sum and counter pointers for a call that needs `part_bytes`
 // of partial sums.
@@ -113,7 +141,7 @@ w12_status get_workspace(int dev, cudaStream_t st, size_t part_bytes, float **pa
         const size_t most = kCounterBytes + sizeof(float) * 2 * static_cast<size_t>(sm_count(dev)) * 128 * 128;
         const size_t grow = need < most ? most : need;
         if (w.ptr)
-            cudaFreeAsync(w.ptr, st);
+            g_ws_retired.emplace_back(dev, w.ptr);
         w.ptr = nullptr;
         w.bytes = 0;
         void *p = nullptr;
@@ -133,18 +161,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 constexpr int kMaxM = 256;
 
+} // namespace
+
+namespace w12 {
+
 // The launch of one GEMM: kernel, tile rows, grid and split-K shape.  Kernel
 // choice is a function of M only (measured on GB300): the CUDA-core kernel for
 // M <= 2; from 3 rows on, the tensor-core kernel (M padded to 16, 32, 64, 128
 // or 256) is faster than four FMAs per weight.
-struct Plan {
-    bool tc = false;
-    int mt = 0, rows_blk = 0, kstep = 0, grid = 0;
-    int64_t n_rowblk = 0, n_kstep = 0, iters = 0;
-    bool defer = false;
-    size_t part_bytes = 0;
-};
-
 w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p)
 {
     Plan q;
@@ -170,6 +194,10 @@ w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p)
     *p = q;
     return W12_OK;
 }
+
+} // namespace w12
+
+namespace {
 
 w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
                      cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
@@ -224,8 +252,8 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     a.n_rowblk = static_cast<int>(pl.n_rowblk);
     a.n_kstep = static_cast<int>(pl.n_kstep);
     a.total_iters = static_cast<int>(pl.iters);
-    a.limit_ns = g_limit_ns.load();
-    a.inject_stall = g_inject_stall.load();
+    a.limit_ns = spin_limit_ns();
+    a.inject_stall = inject_stall();
     a.x_ready = x_ready ? 1 : 0;
     a.defer = pl.defer;
 
@@ -234,10 +262,7 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
         return ws;
 
     CUtensorMap tmx;
-    const bool okx = tc ? make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, mt,
-                                    CU_TENSOR_MAP_SWIZZLE_128B)
-                        : make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 256, mt,
-                                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    const bool okx = make_x_tmap(&tmx, x, M, K, tc, mt);
     if (!okx) {
         g_last_error = "cuTensorMapEncodeTiled failed for x";
         return W12_ERR_CUDA;
@@ -532,6 +557,14 @@ w12_status w12_release_workspaces(void)
             ++it;
         }
     }
+    for (auto it = g_ws_retired.begin(); it != g_ws_retired.end();) {
+        if (it->first == cur) {
+            cudaFree(it->second);
+            it = g_ws_retired.erase(it);
+        } else {
+            ++it;
+        }
+    }
     return W12_OK;
 }
 
@@ -632,8 +665,8 @@ w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, i
     if (iters > (1ll << 30) || a.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
         return W12_ERR_UNSUPPORTED;
     a.total_iters = static_cast<int>(iters);
-    a.limit_ns = g_limit_ns.load();
-    a.inject_stall = g_inject_stall.load();
+    a.limit_ns = spin_limit_ns();
+    a.inject_stall = inject_stall();
     a.x_ready = x_ready ? 1 : 0;
     a.defer = tc_defer(M);
     const int grid = choose_grid(a.n_rowblk, a.n_kstep, sm_count(cur), tc_min_iters(M));

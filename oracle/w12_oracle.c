@@ -21,7 +21,7 @@
  *          escape fraction 7.3e-5.
  *   [KC3]  ai.info page, Key Contributions item 3: the Q pass is zero-copy.
  *
- * Readings of what the pages leave open (every one is listed in the design doc):
+ * Readings of what the pages leave open:
  *   R1 window anchor: a channel's window is the 16 binades ending at the
  *      largest finite normal exponent of that channel (row n of W[N][K]);
  *      ebase = max(emax, 16) - 15, so ebase is in [1, 239];
