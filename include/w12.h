@@ -318,6 +318,26 @@ w12_status w12_gemm_i8(const void *x_bf16, const w12_i8 *q, void *y, int M, int 
                        w12_stream_t stream);
 
 /*
+ * Several W12 matrices that read the same activations, in one launch:
+ * y_i[M][N_i] = x[M][K] . W_i^T for i < n, 1 <= n <= W12_MAX_GROUP (4), e.g.
+ * the q, k and v projections of a layer, or its gate and up projections.
+ * The row blocks of all n matrices are laid end to end and split over one
+ * persistent grid, so the small matrices share the launch's start-up and
+ * tail instead of paying one each; every weight is read once.  Each y_i
+ * meets the same bound as a w12_gemm_ex call on W_i alone (the split of row
+ * blocks over CTAs, hence the order in which partial sums are added, may
+ * differ).  ws[i]: device handles, all with the same K and on
+ * the current device; ys[i]: device outputs [M][N_i], FP32 or (flag
+ * W12_GEMM_OUT_BF16) BF16, 16-byte aligned, caller-owned.  Flags:
+ * W12_GEMM_Q8VIEW, W12_GEMM_INPUT_READY, W12_GEMM_OUT_BF16 (W12_GEMM_SILU_MUL
+ * and other bits give INVALID_ARG).  Workspace, limits and errors as
+ * w12_gemm_ex; a timeout is recorded in every handle's status word.
+ */
+#define W12_MAX_GROUP 4
+w12_status w12_gemm_grouped(const void *x_bf16, const w12_dev *const *ws, void *const *ys, int n, int M, int K,
+                            unsigned flags, w12_stream_t stream);
+
+/*
  * End-to-end form of w12_gemm for host-resident activations: copies
  * x_host -> x_dev, runs w12_gemm into y_dev, copies y_dev -> y_host, all on
  * `stream` (use pinned host memory for asynchronous copies).  Every buffer is

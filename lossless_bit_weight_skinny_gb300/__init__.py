@@ -102,6 +102,7 @@ _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POI
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_ex", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
+_sig("w12_gemm_grouped", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_noalloc", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_last_cuda_error", [], ctypes.c_char_p)
@@ -119,7 +120,7 @@ EXPORTED = (
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
     "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
     "w12_i8_encode_device", "w12_i8_from_dev", "w12_i8_free", "w12_i8_download", "w12_i8_status", "w12_gemm_i8",
-    "w12_gemm_plan",
+    "w12_gemm_plan", "w12_gemm_grouped",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -437,6 +438,35 @@ def w12_gemm_ex(x, d: Dev, y=None, stream=None, q8view=False, input_ready=False,
     _check(_lib.w12_gemm_ex(ctypes.c_void_p(x.data_ptr()), d.ptr, ctypes.c_void_p(y.data_ptr()), M, d.N, K,
                             flags, _stream_ptr(stream)), "w12_gemm_ex")
     return y
+
+
+W12_MAX_GROUP = 4
+
+
+def w12_gemm_grouped(x, devs, ys=None, stream=None, q8view=False, input_ready=False, out_bf16=False):
+    """y_i = x . W_i^T for every handle in devs (all with x's K), in ONE
+    launch: the q/k/v or gate/up projections that read the same activations.
+    Returns the list of outputs (new tensors, or the caller's ys)."""
+    import torch
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()):
+        raise TypeError("x must be a contiguous CUDA bfloat16 [M][K] tensor")
+    devs = list(devs)
+    n = len(devs)
+    if not 1 <= n <= W12_MAX_GROUP:
+        raise ValueError(f"between 1 and {W12_MAX_GROUP} matrices per launch, not {n}")
+    M, K = x.shape
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    ys = [None] * n if ys is None else list(ys)
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+    ys = [_out(x, y, M, d.N, dt) for y, d in zip(ys, devs)]
+    hs = (_P * n)(*[d.ptr for d in devs])
+    ps = (_P * n)(*[y.data_ptr() for y in ys])
+    flags = ((W12_GEMM_Q8VIEW if q8view else 0) | (W12_GEMM_INPUT_READY if input_ready else 0)
+             | (W12_GEMM_OUT_BF16 if out_bf16 else 0))
+    _check(_lib.w12_gemm_grouped(ctypes.c_void_p(x.data_ptr()), hs, ps, n, M, K, flags, _stream_ptr(stream)),
+           "w12_gemm_grouped")
+    return ys
 
 
 def w12_gemm_noalloc(x, d: Dev, y, stream=None):

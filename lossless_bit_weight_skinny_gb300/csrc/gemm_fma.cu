@@ -116,7 +116,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
             return false;
         if (globaltimer_ns() - t0 > a.limit_ns) {
             *abort_flag = 1;
-            report(a.status, kStatusTimeout);
+            report(a, kStatusTimeout);
             return false;
         }
     }
@@ -182,7 +182,7 @@ struct XReduce {
 // correction totals in shared memory.  The chunks' loads and scans are
 // independent and interleaved; the additions happen in list order.
 template <int MT, int RBLK, int NC>
-__device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *list_s, bool big,
+__device__ __forceinline__ void esc_chunks(const MatArgs &mm, const uint32_t *list_s, bool big,
                                            uint32_t lo, uint32_t cnt, uint32_t j1, uint32_t rbase,
                                            int row0, const uint8_t *eb_s, const uint8_t *xs,
                                            float *cneg, float *cpos, int lane)
@@ -194,7 +194,7 @@ __device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *li
         e4[u] = 0u;
         if (j < cnt) {
             if (big)
-                e4[u] = __ldg(a.esc + lo + j);
+                e4[u] = __ldg(mm.esc + lo + j);
             else
                 e4[u] = list_s[j];
         }
@@ -207,7 +207,7 @@ __device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *li
         const uint32_t j = j1 + 32 * u + static_cast<uint32_t>(lane);
         const uint32_t e = e4[u];
         const uint32_t r = (e >> 24) - rbase; // row in the block
-        in[u] = j < cnt && r < static_cast<uint32_t>(RBLK) && row0 + static_cast<int>(r) < a.N;
+        in[u] = j < cnt && r < static_cast<uint32_t>(RBLK) && row0 + static_cast<int>(r) < mm.N;
         rr[u] = r;
         const uint32_t k8 = (e >> 16) & 0xFFu;
         const uint32_t eb = in[u] ? eb_s[r] : 0u;
@@ -263,9 +263,7 @@ __device__ __forceinline__ void esc_chunks(const GemmArgs &a, const uint32_t *li
 
 template <int MT, bool Q8>
 __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
-    gemm_fma_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
-                    const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ CUtensorMap tm_x)
+    gemm_fma_kernel(const GemmArgs a, const __grid_constant__ TmapSet tm)
 {
     using S = FmaShape<MT>;
     using L = FmaSmem<MT, Q8>;
@@ -322,12 +320,13 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
 
     if (warp == WARP_P) {
         // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            prefetch_tmap(&tm_ae);
-            prefetch_tmap(&tm_x);
+        if (lane < a.n_mat) {
+            prefetch_tmap(&tm.ae[lane]);
             if (!Q8)
-                prefetch_tmap(&tm_b);
+                prefetch_tmap(&tm.b[lane]);
         }
+        if (lane == 0)
+            prefetch_tmap(&tm.x);
         int issued = 0;
         int rb = it0 / nk, ks = it0 % nk, s = 0;
         uint32_t ph = 0;
@@ -335,7 +334,9 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const bool ok = __all_sync(0xffffffffu, wait_or_abort(empty0 + 8 * s, ph ^ 1, a, abort_flag));
             if (!ok)
                 break;
-            const int row0 = rb * RBLK, k0 = ks * 256;
+            const int g = mat_of(a, rb);
+            const MatArgs &mm = a.mat[g];
+            const int row0 = (rb - mm.rb0) * RBLK, k0 = ks * 256; // rows of matrix g
             uint8_t *st = smem + s * L::STAGE;
             const uint32_t fb = full0 + 8 * s;
             // The first ring's worth of weights streams before the previous
@@ -346,15 +347,15 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int pre = a.x_ready ? 0 : (n_it < STAGES ? n_it : STAGES);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::TX_BYTES);
-                tma_load_2d(smem_u32(st + L::OFF_AE), &tm_ae, k0, row0, fb);
+                tma_load_2d(smem_u32(st + L::OFF_AE), &tm.ae[g], k0, row0, fb);
                 if (!Q8)
-                    tma_load_2d(smem_u32(st + L::OFF_B), &tm_b, k0 / 2, row0, fb);
+                    tma_load_2d(smem_u32(st + L::OFF_B), &tm.b[g], k0 / 2, row0, fb);
                 if (it >= pre)
-                    tma_load_2d(smem_u32(st + L::OFF_X), &tm_x, k0, 0, fb);
+                    tma_load_2d(smem_u32(st + L::OFF_X), &tm.x, k0, 0, fb);
                 if (it == pre - 1) {
                     pdl_wait_prior_grid();
                     for (int j = 0; j < pre; ++j)
-                        tma_load_2d(smem_u32(smem + j * L::STAGE + L::OFF_X), &tm_x,
+                        tma_load_2d(smem_u32(smem + j * L::STAGE + L::OFF_X), &tm.x,
                                     ((it0 + j) % nk) * 256, 0, full0 + 8 * j);
                 }
             }
@@ -363,7 +364,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 uint8_t *esc_area = st + L::OFF_ESC;
                 if (lane < 2)
                     cp_async_4(smem_u32(esc_area + 4 * lane),
-                               a.tile_ptr + (row0 / 128) * a.tiles_c + ks + lane);
+                               mm.tile_ptr + (row0 / 128) * a.tiles_c + ks + lane);
                 if (it > 0 && (it & 31) == 0) { // next window; prefetch the one after
                     w_lo = w_nlo;
                     w_hi = w_nhi;
@@ -374,7 +375,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 const uint32_t cnt = min(hi - lo, static_cast<uint32_t>(L::ESC_CAP));
                 uint32_t *list = reinterpret_cast<uint32_t *>(esc_area + L::ESC_LIST);
                 for (uint32_t idx = lane; idx < cnt; idx += 32)
-                    cp_async_4(smem_u32(list + idx), a.esc + lo + idx);
+                    cp_async_4(smem_u32(list + idx), mm.esc + lo + idx);
                 cp_async_arrive_noinc(fb);
             }
             issued = it + 1;
@@ -418,13 +419,16 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                         wait_or_abort(corr_empty0 + 8 * db, ((seg >> 1) - 1) & 1, a, abort_flag);
                     for (int i = lane; i < 2 * RBLK * MT; i += 32)
                         cneg[i] = 0.f;
+                    const MatArgs &mm = a.mat[mat_of(a, rb)];
+                    const int lr0 = (rb - mm.rb0) * RBLK;
                     for (int r = lane; r < RBLK; r += 32)
-                        eb_s[r] = rb * RBLK + r < a.N ? __ldg(a.ebase + rb * RBLK + r) : 0;
+                        eb_s[r] = lr0 + r < mm.N ? __ldg(mm.ebase + lr0 + r) : 0;
                     __syncwarp();
                 }
                 bool ok = wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
-                const int row0 = rb * RBLK;
+                const MatArgs &mm = a.mat[mat_of(a, rb)];
+                const int row0 = (rb - mm.rb0) * RBLK; // rows of its matrix
                 const uint8_t *st = smem + s * L::STAGE;
                 if (ok && (NE == 1 || ((it0 + it) & 1) == ew)) {
                     const uint8_t *esc_area = st + L::OFF_ESC;
@@ -435,10 +439,10 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     const uint32_t rbase = static_cast<uint32_t>(row0 & 127);
                     for (uint32_t j1 = 0; j1 < cnt; j1 += 128) {
                         if (cnt - j1 <= 32)
-                            esc_chunks<MT, RBLK, 1>(a, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                            esc_chunks<MT, RBLK, 1>(mm, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
                                                     st + L::OFF_X, cneg, cpos, lane);
                         else
-                            esc_chunks<MT, RBLK, 4>(a, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                            esc_chunks<MT, RBLK, 4>(mm, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
                                                     st + L::OFF_X, cneg, cpos, lane);
                     }
                 }
@@ -472,17 +476,18 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
         for (int it = 0; it < n_it; ++it) {
             // window bases of a new row block: start the load before waiting
             uint32_t e_pre = 1u;
+            const MatArgs &mm = a.mat[mat_of(a, rb)];
+            const int row0 = (rb - mm.rb0) * RBLK; // rows of its matrix
             if (rb != cur_rb) {
-                const int n = rb * RBLK + wrow + lane;
-                if (lane < RW && n < a.N)
-                    e_pre = __ldg(a.ebase + n);
+                const int n = row0 + wrow + lane;
+                if (lane < RW && n < mm.N)
+                    e_pre = __ldg(mm.ebase + n);
             }
             wait_or_abort(full0 + 8 * s, ph, a, abort_flag);
             if (a.inject_stall)
                 wait_or_abort(stall_bar, 0, a, abort_flag);
             // After an abort the loop keeps its shape (every warp still meets
             // every barrier) but works on stale data.
-            const int row0 = rb * RBLK;
             const uint8_t *st = smem + s * L::STAGE;
 
             if (rb != cur_rb) { // a new row block: reset the sums, fetch window bases
@@ -650,8 +655,8 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                     const int n = row0 + wrow + r;
                     if (writer && m < a.M) {
                         if (direct) {
-                            if (n < a.N)
-                                emit_y(a, m, n, total, next);
+                            if (n < mm.N)
+                                emit_y(a, mm, m, n, total, next);
                         } else {
                             a.partials[(static_cast<size_t>(slot) * a.M + m) * RBLK + wrow + r] = total;
                         }
@@ -708,8 +713,7 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
 }
 
 template <int MT, bool Q8>
-cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
-                       const CUtensorMap *tm_x, int grid, cudaStream_t st)
+cudaError_t launch_one(const GemmArgs &a, const TmapSet &tm, int grid, cudaStream_t st)
 {
     using L = FmaSmem<MT, Q8>;
     auto kern = gemm_fma_kernel<MT, Q8>;
@@ -720,7 +724,7 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtens
             return e;
         attr_done = true;
     }
-    return launch_pdl(kern, grid, FmaShape<MT>::THREADS, L::TOTAL, st, a, *tm_ae, *tm_b, *tm_x);
+    return launch_pdl(kern, grid, FmaShape<MT>::THREADS, L::TOTAL, st, a, tm);
 }
 
 } // namespace
@@ -739,17 +743,12 @@ int fma_smem_bytes(int mt, bool q8)
     }
 }
 
-cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
-                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
-                            cudaStream_t st)
+cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const TmapSet &tm, int grid, cudaStream_t st)
 {
     switch (mt) {
-    case 1: return q8 ? launch_one<1, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                      : launch_one<1, false>(a, tm_ae, tm_b, tm_x, grid, st);
-    case 2: return q8 ? launch_one<2, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                      : launch_one<2, false>(a, tm_ae, tm_b, tm_x, grid, st);
-    case 4: return q8 ? launch_one<4, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                      : launch_one<4, false>(a, tm_ae, tm_b, tm_x, grid, st);
+    case 1: return q8 ? launch_one<1, true>(a, tm, grid, st) : launch_one<1, false>(a, tm, grid, st);
+    case 2: return q8 ? launch_one<2, true>(a, tm, grid, st) : launch_one<2, false>(a, tm, grid, st);
+    case 4: return q8 ? launch_one<4, true>(a, tm, grid, st) : launch_one<4, false>(a, tm, grid, st);
     }
     return cudaErrorInvalidValue;
 }

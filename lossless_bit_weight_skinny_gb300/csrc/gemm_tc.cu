@@ -112,7 +112,7 @@ struct TcSmem {
     static constexpr int WSTAGE = AE + B;
     static constexpr int EB = 128;
     // escape list of a unit: header u32[8] = {first entry, count, quadrant
-    // bounds[5]}, then up to kEscCap entries
+    // bounds[5], matrix}, then up to kEscCap entries
     static constexpr int PL_HDR = 32;
     static constexpr int PL = Q8 ? 0 : PL_HDR + 4 * kEscCap;
     static constexpr int SCR = Q8 ? 0 : kDecodeWarps * kPark * kParkPitch;
@@ -177,7 +177,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
             return false;
         if (globaltimer_ns() - t0 > a.limit_ns) {
             *abort_flag = 1;
-            report(a.status, kStatusTimeout);
+            report(a, kStatusTimeout);
             return false;
         }
     }
@@ -211,20 +211,24 @@ __device__ __forceinline__ uint32_t dec_pair(uint32_t ae_word, uint32_t bw, uint
 
 // Escape-list bounds and quadrant splits of the units it0 + first + lane (one
 // per lane): first entry, count, and the counts below rows 32, 64, 96 of the
-// tile (from the row-group index), packed as g12 = rows<32 | rows<64 << 16.
+// tile (from the row-group index), packed as g12 = rows<32 | rows<64 << 16,
+// with the unit's matrix in the top byte of g3.
 __device__ __forceinline__ void esc_window(const GemmArgs &a, int it0, int n_it, int first, int lane,
                                            uint32_t &lo, uint32_t &cnt, uint32_t &g12, uint32_t &g3)
 {
     lo = cnt = g12 = g3 = 0u;
     if (first + lane < n_it) {
         const int u = it0 + first + lane;
-        const size_t t = static_cast<size_t>(u / a.n_kstep) * a.tiles_c + u % a.n_kstep;
-        lo = __ldg(a.tile_ptr + t);
-        const uint32_t hi = __ldg(a.tile_ptr + t + 1);
+        const int rb = u / a.n_kstep;
+        const int g = mat_of(a, rb);
+        const MatArgs &mm = a.mat[g];
+        const size_t t = static_cast<size_t>(rb - mm.rb0) * a.tiles_c + u % a.n_kstep;
+        lo = __ldg(mm.tile_ptr + t);
+        const uint32_t hi = __ldg(mm.tile_ptr + t + 1);
         cnt = hi >= lo ? hi - lo : 0u;
-        const uint16_t *gp = a.gptr + 16 * t;
+        const uint16_t *gp = mm.gptr + 16 * t;
         g12 = static_cast<uint32_t>(__ldg(gp + 4)) | (static_cast<uint32_t>(__ldg(gp + 8)) << 16);
-        g3 = __ldg(gp + 12);
+        g3 = static_cast<uint32_t>(__ldg(gp + 12)) | (static_cast<uint32_t>(g) << 24);
     }
 }
 
@@ -341,9 +345,7 @@ __device__ __forceinline__ void patch_entries(uint32_t qlo, uint32_t qn, uint32_
 // the row scales apply at the end.
 template <int MT, bool Q8, bool EPI, bool I8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap tm_ae,
-                   const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_x)
+    gemm_tc_kernel(const GemmArgs a, const __grid_constant__ TmapSet tm)
 {
     using L = TcSmem<MT, Q8>;
     constexpr int WST = L::WST, XST = L::XST, kNA = L::NA, ND = L::ND;
@@ -430,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegHelper));
     if (warp == kWarpW) {
         // --------------------------- weight producer ---------------------------
-        if (lane == 0) {
-            prefetch_tmap(&tm_ae);
+        if (lane < a.n_mat) {
+            prefetch_tmap(&tm.ae[lane]);
             if (!Q8)
-                prefetch_tmap(&tm_b);
+                prefetch_tmap(&tm.b[lane]);
         }
         int issued = 0;
         for (int it = 0; it < n_it; ++it) {
@@ -443,17 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             const int u = it0 + it;
-            const int row0 = (u / nk) * 128, k0 = (u % nk) * 256;
+            const int rb = u / nk, g = mat_of(a, rb);
+            const int row0 = (rb - a.mat[g].rb0) * 128, k0 = (u % nk) * 256; // rows of matrix g
             uint8_t *st = smem + L::OFF_W + s * L::WSTAGE;
             const uint32_t fb = w_full0 + 8 * (kGroups * s + it % kGroups);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::W_TX + (I8 ? 0 : L::EB));
-                tma_load_2d(smem_u32(st), &tm_ae, k0, row0, fb);
-                tma_load_2d(smem_u32(st + L::AE_HALF), &tm_ae, k0 + 128, row0, fb);
+                tma_load_2d(smem_u32(st), &tm.ae[g], k0, row0, fb);
+                tma_load_2d(smem_u32(st + L::AE_HALF), &tm.ae[g], k0 + 128, row0, fb);
                 if (!Q8)
-                    tma_load_2d(smem_u32(st + L::AE), &tm_b, k0 / 2, row0, fb);
+                    tma_load_2d(smem_u32(st + L::AE), &tm.b[g], k0 / 2, row0, fb);
                 if (!I8)
-                    bulk_load_1d(smem_u32(smem + L::OFF_EB + s * L::EB), a.ebase + row0, L::EB, fb);
+                    bulk_load_1d(smem_u32(smem + L::OFF_EB + s * L::EB), a.mat[g].ebase + row0, L::EB, fb);
             }
             issued = it + 1;
         }
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpX) {
         // ------------------------- activation producer -------------------------
         if (lane == 0) {
-            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm.x);
             // weights stream before the previous kernel in the stream has
             // finished; activations, which it may have written, only after it
             // has -- unless the caller declared them complete before that
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, L::XSLOT);
 #pragma unroll
                     for (int j = 0; j < L::SPS; ++j)
-                        tma_load_2d(smem_u32(xs + j * L::XSUB), &tm_x, k0 + 64 * (h * L::SPS + j), 0, fb);
+                        tma_load_2d(smem_u32(xs + j * L::XSUB), &tm.x, k0 + 64 * (h * L::SPS + j), 0, fb);
                     ++issued;
                     if (++s == XST) {
                         s = 0;
@@ -588,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *pl = smem + L::OFF_PL + s * L::PL;
                 const uint32_t fb = pl_full0 + 8 * s;
                 const uint32_t ncp = ok ? min(cnt, static_cast<uint32_t>(kEscCap)) : 0u;
+                const uint32_t *esc = a.mat[g3 >> 24].esc;
                 for (uint32_t j = lane; j < ncp; j += 32)
-                    cp_async_4(smem_u32(pl + L::PL_HDR + 4 * j), a.esc + lo + j);
+                    cp_async_4(smem_u32(pl + L::PL_HDR + 4 * j), esc + lo + j);
                 cp_async_arrive_noinc(fb);
                 if (lane == 0) {
                     uint32_t *h = reinterpret_cast<uint32_t *>(pl);
@@ -597,12 +601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     h[1] = cnt;
                     const uint32_t b1 = min(g12 & 0xFFFFu, cnt);
                     const uint32_t b2 = max(b1, min(g12 >> 16, cnt));
-                    const uint32_t b3 = max(b2, min(g3, cnt));
+                    const uint32_t b3 = max(b2, min(g3 & 0xFFFFu, cnt));
                     h[2] = 0u;
                     h[3] = b1;
                     h[4] = b2;
                     h[5] = b3;
                     h[6] = cnt;
+                    h[7] = g3 >> 24; // the unit's matrix
                     mbar_arrive(fb);
                 }
             }
@@ -664,7 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qlo_ = min(hp_[2 + q], cnt_);                                                                 \
                 const uint32_t qhi_ = min(hp_[3 + q], cnt_);                                                  \
                 qn_ = qhi_ > qlo_ ? qhi_ - qlo_ : 0u;                                                         \
-                esrc_ = cnt_ > static_cast<uint32_t>(kEscCap) ? a.esc + lo_ : hp_ + L::PL_HDR / 4;           \
+                esrc_ = cnt_ > static_cast<uint32_t>(kEscCap) ? a.mat[hp_[7] & 3].esc + lo_                  \
+                                                               : hp_ + L::PL_HDR / 4;                         \
                 if (static_cast<uint32_t>(lane) < qn_)                                                        \
                     e_first_ = esrc_[qlo_ + lane];                                                            \
             }                                                                                                 \
@@ -731,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_or_abort(acc_full0 + 8 * (kGroups * db + grp), use & 1u, a, abort_flag);
                 __syncwarp();
                 tc_fence_after();
-                const int row0 = rb * 128;
+                const MatArgs &mm = a.mat[mat_of(a, rb)];
+                const int row0 = (rb - mm.rb0) * 128; // rows of its matrix
                 const int c_first = sk_owner(rb * nk, grid, a.total_iters);
                 const int c_last = sk_owner((rb + 1) * nk - 1, grid, a.total_iters);
                 const bool direct = (c_first == c_last);
@@ -739,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = row0 + row;
                 float rs = 1.f; // an INT8 copy's row scale
                 if constexpr (I8)
-                    rs = n < a.N ? __ldg(a.scale + n) : 0.f;
+                    rs = n < mm.N ? __ldg(mm.scale + n) : 0.f;
                 const uint32_t dcol = tmem + t_lane + kDCol + L::DW * db;
                 const bool pair = EPI && direct && (a.out_mode & kOutSiluMul);
                 // this warp's share of the MT accumulator columns: half hh
@@ -764,11 +771,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float next = pair ? __shfl_down_sync(0xffffffffu, v, 1) : 0.f;
                         if (m < a.M) {
                             if (direct) {
-                                if (n < a.N) {
+                                if (n < mm.N) {
                                     if constexpr (EPI)
-                                        emit_y(a, m, n, v, next);
+                                        emit_y(a, mm, m, n, v, next);
                                     else
-                                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + n] = v;
+                                        static_cast<float *>(mm.y)[static_cast<size_t>(m) * mm.N + n] = v;
                                 }
                             } else {
                                 a.partials[(static_cast<size_t>(slot) * a.M + m) * 128 + row] = v;
@@ -807,8 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MT, bool Q8, bool EPI, bool I8 = false>
-cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
-                       const CUtensorMap *tm_x, int grid, cudaStream_t st)
+cudaError_t launch_one(const GemmArgs &a, const TmapSet &tm, int grid, cudaStream_t st)
 {
     using L = TcSmem<MT, Q8>;
     auto kern = gemm_tc_kernel<MT, Q8, EPI, I8>;
@@ -832,7 +838,7 @@ cudaError_t launch_one(const GemmArgs &a, const CUtensorMap *tm_ae, const CUtens
     b.bshift_mul[0] = 1u << 28;
     b.bshift_mul[1] = 1u << 24;
     b.bshift_mul[2] = 1u << 20;
-    return launch_pdl(kern, grid, kThreads, L::TOTAL, st, b, *tm_ae, *tm_b, *tm_x);
+    return launch_pdl(kern, grid, kThreads, L::TOTAL, st, b, tm);
 }
 
 } // namespace
@@ -849,29 +855,25 @@ int tc_smem_bytes(int mt, bool q8)
 }
 
 template <int MT>
-cudaError_t launch_mt(bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae, const CUtensorMap *tm_b,
-                      const CUtensorMap *tm_x, int grid, cudaStream_t st)
+cudaError_t launch_mt(bool q8, bool i8, const GemmArgs &a, const TmapSet &tm, int grid, cudaStream_t st)
 {
     if (i8)
-        return a.out_mode ? launch_one<MT, true, true, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                          : launch_one<MT, true, false, true>(a, tm_ae, tm_b, tm_x, grid, st);
+        return a.out_mode ? launch_one<MT, true, true, true>(a, tm, grid, st)
+                          : launch_one<MT, true, false, true>(a, tm, grid, st);
     if (a.out_mode)
-        return q8 ? launch_one<MT, true, true>(a, tm_ae, tm_b, tm_x, grid, st)
-                  : launch_one<MT, false, true>(a, tm_ae, tm_b, tm_x, grid, st);
-    return q8 ? launch_one<MT, true, false>(a, tm_ae, tm_b, tm_x, grid, st)
-              : launch_one<MT, false, false>(a, tm_ae, tm_b, tm_x, grid, st);
+        return q8 ? launch_one<MT, true, true>(a, tm, grid, st) : launch_one<MT, false, true>(a, tm, grid, st);
+    return q8 ? launch_one<MT, true, false>(a, tm, grid, st) : launch_one<MT, false, false>(a, tm, grid, st);
 }
 
-cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae,
-                           const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
+cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const TmapSet &tm, int grid,
                            cudaStream_t st)
 {
     switch (mt) {
-    case 16: return launch_mt<16>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 32: return launch_mt<32>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 64: return launch_mt<64>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 128: return launch_mt<128>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
-    case 256: return launch_mt<256>(q8, i8, a, tm_ae, tm_b, tm_x, grid, st);
+    case 16: return launch_mt<16>(q8, i8, a, tm, grid, st);
+    case 32: return launch_mt<32>(q8, i8, a, tm, grid, st);
+    case 64: return launch_mt<64>(q8, i8, a, tm, grid, st);
+    case 128: return launch_mt<128>(q8, i8, a, tm, grid, st);
+    case 256: return launch_mt<256>(q8, i8, a, tm, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -17,32 +17,61 @@ namespace w12 {
 constexpr int kStatusTimeout = 8;
 constexpr int kStatusCorrupt = 7;
 
-struct GemmArgs {
+// Matrices of one launch: a grouped launch runs several W12 matrices that
+// read the same activations x; their row blocks are laid end to end, matrix i
+// owning row blocks [rb0, next matrix's rb0).
+constexpr int kMaxGroup = 4;
+
+struct MatArgs {
     const uint8_t *ebase;          // [N] window base per row
     const uint32_t *tile_ptr;      // [T + 1]
     const uint32_t *esc;           // escape entries
     const uint16_t *gptr;          // [T][16]: entries of tile t in rows < 8g
     void *y;                       // [M][ldy]: FP32, or BF16 under kOutBF16
+    int *status;                   // device status word of the handle
+    const float *scale;            // [N] row scales of an INT8 copy (INT8 weights only)
+    int N;                         // rows of the matrix
+    int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
+    int rb0;                       // its first row block in the launch
+};
+
+struct GemmArgs {
+    MatArgs mat[kMaxGroup];
+    int n_mat;                     // matrices of the launch (1 .. kMaxGroup)
     float *partials;               // [2 * grid][M][rows_blk] split-K partial sums
     unsigned long long *counters;  // [n_rowblk] arrivals (zero between launches)
-    int *status;                   // device status word of the handle
-    int M, N, K;
+    int M, K;
     int tiles_c;                   // ceil(K / 256): escape tiles per row band
-    int n_rowblk;                  // row blocks
+    int n_rowblk;                  // row blocks of all matrices
     int n_kstep;                   // k steps per row block
     int total_iters;               // n_rowblk * n_kstep
     uint64_t limit_ns;             // bounded-wait limit
     int inject_stall;              // test hook: wait on a barrier nobody arrives on
     int x_ready;                   // x was complete before the previous launch: load it at once
     int out_mode;                  // kOutBF16 | kOutSiluMul
-    int ldy;                       // elements per row of y: N, or N / 2 under kOutSiluMul
     int defer;                     // split row blocks: leave the partials to sk_reduce_kernel
-    const float *scale;            // [N] row scales of an INT8 copy (INT8 weights only)
     // 2^28, 2^24, 2^20: multipliers whose high product words are the B word
     // shifted right by 4, 8, 12 bits (a kernel argument, so that the shifts
     // run as multiplies on the FMA pipe beside the decode's logic operations)
     uint32_t bshift_mul[3];
 };
+
+// TMA maps of a launch: each matrix's AE and B planes, and the activations.
+struct alignas(64) TmapSet {
+    CUtensorMap ae[kMaxGroup];
+    CUtensorMap b[kMaxGroup];
+    CUtensorMap x;
+};
+
+// The matrix that owns row block rb of the launch.
+__host__ __device__ __forceinline__ int mat_of(const GemmArgs &a, int rb)
+{
+    int g = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        g += (i < a.n_mat && rb >= a.mat[i].rb0) ? 1 : 0;
+    return g;
+}
 
 // Output modes.  kOutBF16: y holds BF16, each FP32 result rounded to the
 // nearest BF16 (ties to even).  kOutSiluMul: the matrix's rows come in
@@ -52,24 +81,25 @@ struct GemmArgs {
 constexpr int kOutBF16 = 1;
 constexpr int kOutSiluMul = 2;
 
-__device__ __forceinline__ void put_y(const GemmArgs &a, int m, int col, float v)
+__device__ __forceinline__ void put_y(const GemmArgs &a, const MatArgs &mm, int m, int col, float v)
 {
-    const size_t i = static_cast<size_t>(m) * a.ldy + col;
+    const size_t i = static_cast<size_t>(m) * mm.ldy + col;
     if (a.out_mode & kOutBF16)
-        static_cast<__nv_bfloat16 *>(a.y)[i] = __float2bfloat16_rn(v);
+        static_cast<__nv_bfloat16 *>(mm.y)[i] = __float2bfloat16_rn(v);
     else
-        static_cast<float *>(a.y)[i] = v;
+        static_cast<float *>(mm.y)[i] = v;
 }
 
-// The final value v of y[m][n] (n < N); `next` is the final value of row n + 1
-// (read only under kOutSiluMul, where N is even and a gate row n is even).
-__device__ __forceinline__ void emit_y(const GemmArgs &a, int m, int n, float v, float next)
+// The final value v of y[m][n] of matrix mm (n < mm.N); `next` is the final
+// value of row n + 1 (read only under kOutSiluMul, where N is even and a gate
+// row n is even).
+__device__ __forceinline__ void emit_y(const GemmArgs &a, const MatArgs &mm, int m, int n, float v, float next)
 {
     if (a.out_mode & kOutSiluMul) {
         if ((n & 1) == 0)
-            put_y(a, m, n >> 1, v / (1.0f + expf(-v)) * next);
+            put_y(a, mm, m, n >> 1, v / (1.0f + expf(-v)) * next);
     } else {
-        put_y(a, m, n, v);
+        put_y(a, mm, m, n, v);
     }
 }
 
@@ -177,15 +207,19 @@ __device__ __forceinline__ void load_tile_window(const GemmArgs &a, int it0, int
 {
     if (first + lane < n_it) {
         const int u = it0 + first + lane;
-        const int t = ((u / a.n_kstep) * rows_blk / 128) * a.tiles_c + u % a.n_kstep;
-        lo = __ldg(a.tile_ptr + t);
-        hi = __ldg(a.tile_ptr + t + 1);
+        const int rb = u / a.n_kstep;
+        const MatArgs &mm = a.mat[mat_of(a, rb)];
+        const int t = ((rb - mm.rb0) * rows_blk / 128) * a.tiles_c + u % a.n_kstep;
+        lo = __ldg(mm.tile_ptr + t);
+        hi = __ldg(mm.tile_ptr + t + 1);
     }
 }
 
-__device__ __forceinline__ void report(int *status, int code)
+// Record a device-side failure in the status word of every matrix of the launch.
+__device__ __forceinline__ void report(const GemmArgs &a, int code)
 {
-    atomicCAS(status, 0, code);
+    for (int g = 0; g < a.n_mat; ++g)
+        atomicCAS(a.mat[g].status, 0, code);
 }
 
 // The last contributor sums every partial of row block rb and writes y.
@@ -212,7 +246,8 @@ template <bool EPI, int U = W12_SK_UNROLL>
 __device__ W12_SK_INL void sk_reduce_range(const GemmArgs &a, int rb, int rows_blk, int grid, int c_first,
                                            int c_last, int tid, int nthreads, int g_lo, int g_hi)
 {
-    const int row0 = rb * rows_blk;
+    const MatArgs &mm = a.mat[mat_of(a, rb)];
+    const int row0 = (rb - mm.rb0) * rows_blk; // first row of the block in its matrix
     const int groups = g_hi; // float4 groups [g_lo, g_hi) of the partial
     const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
     const float4 *base = reinterpret_cast<const float4 *>(a.partials);
@@ -262,11 +297,11 @@ __device__ W12_SK_INL void sk_reduce_range(const GemmArgs &a, int rb, int rows_b
             const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                if (row0 + r + q < a.N) {
+                if (row0 + r + q < mm.N) {
                     if constexpr (EPI)
-                        emit_y(a, m, row0 + r + q, v4[q], v4[(q + 1) & 3]);
+                        emit_y(a, mm, m, row0 + r + q, v4[q], v4[(q + 1) & 3]);
                     else
-                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + row0 + r + q] = v4[q];
+                        static_cast<float *>(mm.y)[static_cast<size_t>(m) * mm.N + row0 + r + q] = v4[q];
                 }
             }
         }
@@ -281,7 +316,8 @@ template <bool EPI, int GPT>
 __device__ __forceinline__ void sk_reduce_wide(const GemmArgs &a, int rb, int rows_blk, int grid, int c_first,
                                                int c_last, int tid, int nthreads)
 {
-    const int row0 = rb * rows_blk;
+    const MatArgs &mm = a.mat[mat_of(a, rb)];
+    const int row0 = (rb - mm.rb0) * rows_blk; // first row of the block in its matrix
     const int groups = a.M * rows_blk / 4;
     const size_t slot4 = static_cast<size_t>(a.M) * rows_blk / 4;
     const float4 *base = reinterpret_cast<const float4 *>(a.partials);
@@ -328,11 +364,11 @@ __device__ __forceinline__ void sk_reduce_wide(const GemmArgs &a, int rb, int ro
             const float v4[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (row0 + r + j < a.N) {
+                if (row0 + r + j < mm.N) {
                     if constexpr (EPI)
-                        emit_y(a, m, row0 + r + j, v4[j], v4[(j + 1) & 3]);
+                        emit_y(a, mm, m, row0 + r + j, v4[j], v4[(j + 1) & 3]);
                     else
-                        static_cast<float *>(a.y)[static_cast<size_t>(m) * a.N + row0 + r + j] = v4[j];
+                        static_cast<float *>(mm.y)[static_cast<size_t>(m) * mm.N + row0 + r + j] = v4[j];
                 }
             }
         }
@@ -352,7 +388,7 @@ __device__ __forceinline__ void sk_reduce_block(const GemmArgs &a, int rb, int r
 // pdl_wait_prior_grid() before touching anything that kernel may write.
 template <typename Kern>
 cudaError_t launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t st, const GemmArgs &a,
-                       const CUtensorMap &t0, const CUtensorMap &t1, const CUtensorMap &t2)
+                       const TmapSet &tm)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -364,13 +400,11 @@ cudaError_t launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, t0, t1, t2);
+    return cudaLaunchKernelEx(&cfg, kern, a, tm);
 }
 
 // Launchers (defined in gemm_fma.cu / gemm_tc.cu / decode.cu).
-cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const CUtensorMap *tm_ae,
-                            const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
-                            cudaStream_t st);
+cudaError_t launch_gemm_fma(int mt, bool q8, const GemmArgs &a, const TmapSet &tm, int grid, cudaStream_t st);
 // Split-K fix-up as a kernel of its own (reduce.cu), chained after a
 // tensor-core GEMM launched with a.defer set; nothing is launched when no row
 // block is split.  *launched tells whether it was.
@@ -379,9 +413,8 @@ cudaError_t launch_sk_reduce(const GemmArgs &a, int gemm_grid, int rows_blk, cud
 // over the finite weights, q = rint(w / scale) clamped to [-127, 127], Inf to
 // +-127, NaN to 0, q = 0 where the scale is 0.
 cudaError_t launch_i8_quantize(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *scale, cudaStream_t st);
-// i8: the weights are an INT8 copy (a.scale set, tm_ae over its bytes).
-cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const CUtensorMap *tm_ae,
-                           const CUtensorMap *tm_b, const CUtensorMap *tm_x, int grid,
+// i8: the weights are an INT8 copy (mat[].scale set, tm.ae over its bytes).
+cudaError_t launch_gemm_tc(int mt, bool q8, bool i8, const GemmArgs &a, const TmapSet &tm, int grid,
                            cudaStream_t st);
 int fma_rows_blk(int mt);
 int fma_ctas_per_sm(int mt);
@@ -480,6 +513,8 @@ struct Plan {
     size_t part_bytes = 0; // split-K partial sums of the launch
 };
 w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p);
+// The launch over several matrices of rows Ns[0..n) that read the same x.
+w12_status make_plan_group(int M, const int64_t *Ns, int n, int64_t K, int sms, Plan *p);
 // 2-D TMA map over a row-major [rows][cols] array of `esize`-byte elements.
 bool make_tmap(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols,
                uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);

@@ -109,15 +109,20 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
         return W12_ERR_UNSUPPORTED;
 
     GemmArgs a{};
-    a.ebase = w->ebase;
-    a.tile_ptr = w->tile_ptr;
-    a.esc = w->esc;
-    a.gptr = w->gptr;
-    a.y = y;
-    a.ldy = N;
-    a.status = w->status;
+    MatArgs &mm = a.mat[0];
+    mm.ebase = w->ebase;
+    mm.tile_ptr = w->tile_ptr;
+    mm.esc = w->esc;
+    mm.gptr = w->gptr;
+    mm.y = y;
+    mm.ldy = N;
+    mm.status = w->status;
+    mm.N = N;
+    mm.rb0 = 0;
+    a.n_mat = 1;
+    for (int i = 1; i < kMaxGroup; ++i)
+        a.mat[i] = a.mat[0];
     a.M = M;
-    a.N = N;
     a.K = K;
     a.tiles_c = static_cast<int>(w->tiles_c);
     a.n_rowblk = static_cast<int>(pl.n_rowblk);
@@ -135,17 +140,16 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     a.counters = reinterpret_cast<unsigned long long *>(scratch);
     a.partials = reinterpret_cast<float *>(scratch + kCounterBytes);
 
-    CUtensorMap tmx;
-    if (!make_x_tmap(&tmx, x_bf16, M, K, pl.tc, pl.mt)) {
+    TmapSet tm;
+    if (!make_x_tmap(&tm.x, x_bf16, M, K, pl.tc, pl.mt)) {
         set_last_error("cuTensorMapEncodeTiled failed for x");
         return W12_ERR_CUDA;
     }
     const w12_tmap &tae = pl.tc ? w->tm_ae_tc : (pl.rows_blk == 128 ? w->tm_ae_fma128 : w->tm_ae_fma64);
     const w12_tmap &tb = pl.tc ? w->tm_b_tc : (pl.rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
-    const CUtensorMap *pae = reinterpret_cast<const CUtensorMap *>(&tae);
-    const CUtensorMap *pb = reinterpret_cast<const CUtensorMap *>(&tb);
-    e = pl.tc ? launch_gemm_tc(pl.mt, false, false, a, pae, pb, &tmx, pl.grid, st)
-              : launch_gemm_fma(pl.mt, false, a, pae, pb, &tmx, pl.grid, st);
+    tm.ae[0] = *reinterpret_cast<const CUtensorMap *>(&tae);
+    tm.b[0] = *reinterpret_cast<const CUtensorMap *>(&tb);
+    e = pl.tc ? launch_gemm_tc(pl.mt, false, false, a, tm, pl.grid, st) : launch_gemm_fma(pl.mt, false, a, tm, pl.grid, st);
     bool red = false;
     if (e == cudaSuccess && a.defer)
         e = launch_sk_reduce(a, pl.grid, pl.rows_blk, st, &red);

@@ -171,13 +171,22 @@ namespace w12 {
 // or 256) is faster than four FMAs per weight.
 w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p)
 {
+    return make_plan_group(M, &N, 1, K, sms, p);
+}
+
+// The launch over several matrices of rows Ns[0..n) read with the same x:
+// their row blocks end to end.
+w12_status make_plan_group(int M, const int64_t *Ns, int n, int64_t K, int sms, Plan *p)
+{
     Plan q;
     q.tc = M >= W12_TC_MIN_M;
     q.mt = q.tc ? (M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256)
                 : (M <= 1 ? 1 : M <= 2 ? 2 : 4);
     q.rows_blk = q.tc ? kTcRows : fma_rows_blk(q.mt);
     q.kstep = q.tc ? kTcKStep : kFmaKStep;
-    q.n_rowblk = ceil_div(N, q.rows_blk);
+    q.n_rowblk = 0;
+    for (int i = 0; i < n; ++i)
+        q.n_rowblk += ceil_div(Ns[i], q.rows_blk);
     q.n_kstep = ceil_div(K, q.kstep);
     q.iters = q.n_rowblk * q.n_kstep;
     if (q.iters > (1ll << 30) || q.n_rowblk * 8 > static_cast<int64_t>(kCounterBytes))
@@ -199,56 +208,91 @@ w12_status make_plan(int M, int64_t N, int64_t K, int sms, Plan *p)
 
 namespace {
 
-w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
-                     cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
+// One launch over n matrices (1 <= n <= kMaxGroup) that read the same x:
+// y_i[M][N_i] = x[M][K] . W_i^T.
+w12_status gemm_group_impl(const void *x, const w12_dev *const *ws, void *const *ys, int n, int M, int K,
+                           cudaStream_t st, bool q8, bool x_ready, int out_mode)
 {
-    if (!w || M < 0)
+    if (n < 1 || n > kMaxGroup || !ws || !ys || M < 0)
         return W12_ERR_INVALID_ARG;
-    if (N != w->N || K != w->K)
-        return W12_ERR_SHAPE;
-    if ((out_mode & kOutSiluMul) && (N & 1))
-        return W12_ERR_SHAPE;
-    const int ldy = (out_mode & kOutSiluMul) ? N / 2 : N;
-    const size_t ybytes = ((out_mode & kOutBF16) ? 2 : 4) * static_cast<size_t>(M) * ldy;
+    for (int i = 0; i < n; ++i) {
+        if (!ws[i])
+            return W12_ERR_INVALID_ARG;
+        if (K != ws[i]->K)
+            return W12_ERR_SHAPE;
+        if ((out_mode & kOutSiluMul) && (ws[i]->N & 1))
+            return W12_ERR_SHAPE;
+    }
     if (M > kMaxM)
         return W12_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0)
+    if (M == 0)
         return W12_OK;
-    if (!x || !y)
-        return W12_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(y))
-        return W12_ERR_ALIGNMENT;
+    if (!x || !aligned16(x))
+        return x ? W12_ERR_ALIGNMENT : W12_ERR_INVALID_ARG;
     int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess)
-        return W12_ERR_CUDA;
-    if (cur != w->device)
-        return W12_ERR_INVALID_ARG;
-    if (K == 0)
-        return cudaMemsetAsync(y, 0, ybytes, st) == cudaSuccess
-                   ? W12_OK
-                   : W12_ERR_CUDA;
-    if (!w->gemm_ok)
-        return W12_ERR_UNSUPPORTED;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    int64_t Ns[kMaxGroup] = {0};
+    for (int i = 0; i < n; ++i) {
+        if (ws[i]->N > 0 && !ys[i])
+            return W12_ERR_INVALID_ARG;
+        if (ys[i] && !aligned16(ys[i]))
+            return W12_ERR_ALIGNMENT;
+        if (ws[i]->device != cur)
+            return W12_ERR_INVALID_ARG;
+        Ns[i] = ws[i]->N;
+    }
+    if (K == 0) {
+        for (int i = 0; i < n; ++i) {
+            const int64_t ldy = (out_mode & kOutSiluMul) ? Ns[i] / 2 : Ns[i];
+            const size_t ybytes = ((out_mode & kOutBF16) ? 2 : 4) * static_cast<size_t>(M) * ldy;
+            if (ybytes && (e = cudaMemsetAsync(ys[i], 0, ybytes, st)) != cudaSuccess)
+                return cuda_fail(e);
+        }
+        return W12_OK;
+    }
+    for (int i = 0; i < n; ++i)
+        if (Ns[i] > 0 && !ws[i]->gemm_ok)
+            return W12_ERR_UNSUPPORTED;
 
     Plan pl;
-    const w12_status ps = make_plan(M, N, K, sm_count(cur), &pl);
+    const w12_status ps = make_plan_group(M, Ns, n, K, sm_count(cur), &pl);
     if (ps != W12_OK)
         return ps;
-    const bool tc = pl.tc;
-    const int mt = pl.mt, rows_blk = pl.rows_blk, grid = pl.grid;
+    if (pl.n_rowblk == 0)
+        return W12_OK;
     GemmArgs a{};
-    a.ebase = w->ebase;
-    a.tile_ptr = w->tile_ptr;
-    a.esc = w->esc;
-    a.gptr = w->gptr;
-    a.y = y;
+    TmapSet tm;
+    int rb = 0, g = 0;
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] == 0)
+            continue; // no rows: nothing to compute or store
+        const w12_dev *w = ws[i];
+        MatArgs &mm = a.mat[g];
+        mm.ebase = w->ebase;
+        mm.tile_ptr = w->tile_ptr;
+        mm.esc = w->esc;
+        mm.gptr = w->gptr;
+        mm.y = ys[i];
+        mm.status = w->status;
+        mm.N = static_cast<int>(Ns[i]);
+        mm.ldy = (out_mode & kOutSiluMul) ? mm.N / 2 : mm.N;
+        mm.rb0 = rb;
+        rb += static_cast<int>(ceil_div(Ns[i], pl.rows_blk));
+        const w12_tmap &tae = pl.tc ? w->tm_ae_tc : (pl.rows_blk == 128 ? w->tm_ae_fma128 : w->tm_ae_fma64);
+        const w12_tmap &tb = pl.tc ? w->tm_b_tc : (pl.rows_blk == 128 ? w->tm_b_fma128 : w->tm_b_fma64);
+        tm.ae[g] = *tmap_of(tae);
+        tm.b[g] = *tmap_of(tb);
+        ++g;
+    }
+    a.n_mat = g;
+    for (int i = g; i < kMaxGroup; ++i)
+        a.mat[i] = a.mat[0];
     a.out_mode = out_mode;
-    a.ldy = ldy;
-    a.status = w->status;
     a.M = M;
-    a.N = N;
     a.K = K;
-    a.tiles_c = static_cast<int>(w->tiles_c);
+    a.tiles_c = static_cast<int>(ws[0]->tiles_c);
     a.n_rowblk = static_cast<int>(pl.n_rowblk);
     a.n_kstep = static_cast<int>(pl.n_kstep);
     a.total_iters = static_cast<int>(pl.iters);
@@ -257,27 +301,38 @@ w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int
     a.x_ready = x_ready ? 1 : 0;
     a.defer = pl.defer;
 
-    w12_status ws = get_workspace(cur, st, pl.part_bytes, &a.partials, &a.counters);
-    if (ws != W12_OK)
-        return ws;
-
-    CUtensorMap tmx;
-    const bool okx = make_x_tmap(&tmx, x, M, K, tc, mt);
-    if (!okx) {
+    w12_status wst = get_workspace(cur, st, pl.part_bytes, &a.partials, &a.counters);
+    if (wst != W12_OK)
+        return wst;
+    if (!make_x_tmap(&tm.x, x, M, K, pl.tc, pl.mt)) {
         g_last_error = "cuTensorMapEncodeTiled failed for x";
         return W12_ERR_CUDA;
     }
-    cudaError_t e;
-    if (tc) {
-        e = launch_gemm_tc(mt, q8, false, a, tmap_of(w->tm_ae_tc), tmap_of(w->tm_b_tc), &tmx, grid, st);
+    if (pl.tc) {
+        e = launch_gemm_tc(pl.mt, q8, false, a, tm, pl.grid, st);
         bool red = false;
         if (e == cudaSuccess && a.defer)
-            e = launch_sk_reduce(a, grid, rows_blk, st, &red);
-    } else if (rows_blk == 128)
-        e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma128), tmap_of(w->tm_b_fma128), &tmx, grid, st);
-    else
-        e = launch_gemm_fma(mt, q8, a, tmap_of(w->tm_ae_fma64), tmap_of(w->tm_b_fma64), &tmx, grid, st);
+            e = launch_sk_reduce(a, pl.grid, pl.rows_blk, st, &red);
+    } else {
+        e = launch_gemm_fma(pl.mt, q8, a, tm, pl.grid, st);
+    }
     return e == cudaSuccess ? W12_OK : cuda_fail(e);
+}
+
+w12_status gemm_impl(const void *x, const w12_dev *w, void *y, int M, int N, int K,
+                     cudaStream_t st, bool q8, bool x_ready = false, int out_mode = 0)
+{
+    if (!w || M < 0)
+        return W12_ERR_INVALID_ARG;
+    if (N != w->N || K != w->K)
+        return W12_ERR_SHAPE;
+    if (M > kMaxM)
+        return W12_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0)
+        return W12_OK;
+    if (!x || !y)
+        return W12_ERR_INVALID_ARG;
+    return gemm_group_impl(x, &w, &y, 1, M, K, st, q8, x_ready, out_mode);
 }
 
 } // namespace
@@ -489,6 +544,16 @@ w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int
                      (flags & W12_GEMM_Q8VIEW) != 0, (flags & W12_GEMM_INPUT_READY) != 0, out_mode);
 }
 
+w12_status w12_gemm_grouped(const void *x_bf16, const w12_dev *const *ws, void *const *ys, int n, int M, int K,
+                            unsigned flags, w12_stream_t stream)
+{
+    if (flags & ~static_cast<unsigned>(W12_GEMM_Q8VIEW | W12_GEMM_INPUT_READY | W12_GEMM_OUT_BF16))
+        return W12_ERR_INVALID_ARG;
+    const int out_mode = (flags & W12_GEMM_OUT_BF16) ? kOutBF16 : 0;
+    return gemm_group_impl(x_bf16, ws, ys, n, M, K, reinterpret_cast<cudaStream_t>(stream),
+                           (flags & W12_GEMM_Q8VIEW) != 0, (flags & W12_GEMM_INPUT_READY) != 0, out_mode);
+}
+
 w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, float *y_dev,
                          float *y_host, int M, int N, int K, w12_stream_t stream)
 {
@@ -650,13 +715,18 @@ w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, i
     // the tensor-core kernel for every M (M padded to 16, 32, 64, 128 or 256)
     const int mt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     GemmArgs a{};
-    a.y = y;
+    MatArgs &mm = a.mat[0];
+    mm.y = y;
+    mm.ldy = ldy;
+    mm.scale = q->scale;
+    mm.status = q->status;
+    mm.N = N;
+    mm.rb0 = 0;
+    a.n_mat = 1;
+    for (int i = 1; i < kMaxGroup; ++i)
+        a.mat[i] = a.mat[0];
     a.out_mode = out_mode;
-    a.ldy = ldy;
-    a.scale = q->scale;
-    a.status = q->status;
     a.M = M;
-    a.N = N;
     a.K = K;
     a.tiles_c = static_cast<int>(ceil_div(K, kTileCols));
     a.n_rowblk = static_cast<int>(ceil_div(N, kTcRows));
@@ -674,13 +744,14 @@ w12_status gemm_i8_impl(const void *x, const w12_i8 *q, void *y, int M, int N, i
     w12_status ws = get_workspace(cur, st, part_bytes, &a.partials, &a.counters);
     if (ws != W12_OK)
         return ws;
-    CUtensorMap tmx;
-    if (!make_tmap(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, 64, mt, CU_TENSOR_MAP_SWIZZLE_128B)) {
+    TmapSet tm;
+    if (!make_x_tmap(&tm.x, x, M, K, true, mt)) {
         g_last_error = "cuTensorMapEncodeTiled failed for x";
         return W12_ERR_CUDA;
     }
-    const CUtensorMap *tq = tmap_of(q->tm_q_tc);
-    cudaError_t e = launch_gemm_tc(mt, true, true, a, tq, tq, &tmx, grid, st);
+    tm.ae[0] = *tmap_of(q->tm_q_tc);
+    tm.b[0] = tm.ae[0];
+    cudaError_t e = launch_gemm_tc(mt, true, true, a, tm, grid, st);
     bool red = false;
     if (e == cudaSuccess && a.defer)
         e = launch_sk_reduce(a, grid, kTcRows, st, &red);
