@@ -433,16 +433,19 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
                 if (ok && (NE == 1 || ((it0 + it) & 1) == ew)) {
                     const uint8_t *esc_area = st + L::OFF_ESC;
                     const uint2 lohi = *reinterpret_cast<const uint2 *>(esc_area);
-                    const uint32_t cnt = lohi.y - lohi.x;
+                    // a stage read after an abort may hold another unit's
+                    // bounds: keep every global read inside this matrix's list
+                    const uint32_t lo_c = min(lohi.x, mm.n_esc);
+                    const uint32_t cnt = min(lohi.y - lohi.x, mm.n_esc - lo_c);
                     const bool big = cnt > static_cast<uint32_t>(L::ESC_CAP);
                     const uint32_t *list_s = reinterpret_cast<const uint32_t *>(esc_area + L::ESC_LIST);
                     const uint32_t rbase = static_cast<uint32_t>(row0 & 127);
                     for (uint32_t j1 = 0; j1 < cnt; j1 += 128) {
                         if (cnt - j1 <= 32)
-                            esc_chunks<MT, RBLK, 1>(mm, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                            esc_chunks<MT, RBLK, 1>(mm, list_s, big, lo_c, cnt, j1, rbase, row0, eb_s,
                                                     st + L::OFF_X, cneg, cpos, lane);
                         else
-                            esc_chunks<MT, RBLK, 4>(mm, list_s, big, lohi.x, cnt, j1, rbase, row0, eb_s,
+                            esc_chunks<MT, RBLK, 4>(mm, list_s, big, lo_c, cnt, j1, rbase, row0, eb_s,
                                                     st + L::OFF_X, cneg, cpos, lane);
                     }
                 }

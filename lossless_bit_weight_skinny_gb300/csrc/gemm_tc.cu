@@ -665,11 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             p_ = __all_sync(0xffffffffu, p_) && (ok_);                                                        \
             const uint32_t *hp_ = reinterpret_cast<const uint32_t *>(smem + L::OFF_PL + sp_ * L::PL);        \
             if (p_) {                                                                                         \
-                const uint32_t lo_ = hp_[0], cnt_ = hp_[1];                                                   \
+                /* a header read after an abort may mix two units: every read */                              \
+                /* of the matrix's list stays below its entry count */                                        \
+                const MatArgs &hm_ = a.mat[hp_[7] % kMaxGroup];                                                 \
+                const uint32_t lo_ = min(hp_[0], hm_.n_esc), cnt_ = min(hp_[1], hm_.n_esc - lo_);             \
                 qlo_ = min(hp_[2 + q], cnt_);                                                                 \
                 const uint32_t qhi_ = min(hp_[3 + q], cnt_);                                                  \
                 qn_ = qhi_ > qlo_ ? qhi_ - qlo_ : 0u;                                                         \
-                esrc_ = cnt_ > static_cast<uint32_t>(kEscCap) ? a.mat[hp_[7] & 3].esc + lo_                  \
+                esrc_ = cnt_ > static_cast<uint32_t>(kEscCap) ? hm_.esc + lo_                                \
                                                                : hp_ + L::PL_HDR / 4;                         \
                 if (static_cast<uint32_t>(lane) < qn_)                                                        \
                     e_first_ = esrc_[qlo_ + lane];                                                            \

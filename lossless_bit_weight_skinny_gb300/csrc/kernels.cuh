@@ -26,6 +26,7 @@ struct MatArgs {
     const uint8_t *ebase;          // [N] window base per row
     const uint32_t *tile_ptr;      // [T + 1]
     const uint32_t *esc;           // escape entries
+    uint32_t n_esc;                // their count: every read of esc stays below it
     const uint16_t *gptr;          // [T][16]: entries of tile t in rows < 8g
     void *y;                       // [M][ldy]: FP32, or BF16 under kOutBF16
     int *status;                   // device status word of the handle

@@ -113,6 +113,7 @@ static w12_status noalloc_impl(const void *x_bf16, const w12_dev *w, float *y, i
     mm.ebase = w->ebase;
     mm.tile_ptr = w->tile_ptr;
     mm.esc = w->esc;
+    mm.n_esc = static_cast<uint32_t>(w->n_esc);
     mm.gptr = w->gptr;
     mm.y = y;
     mm.ldy = N;

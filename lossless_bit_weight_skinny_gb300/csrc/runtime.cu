@@ -273,6 +273,7 @@ w12_status gemm_group_impl(const void *x, const w12_dev *const *ws, void *const 
         mm.ebase = w->ebase;
         mm.tile_ptr = w->tile_ptr;
         mm.esc = w->esc;
+        mm.n_esc = static_cast<uint32_t>(w->n_esc);
         mm.gptr = w->gptr;
         mm.y = ys[i];
         mm.status = w->status;

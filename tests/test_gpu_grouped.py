@@ -153,3 +153,31 @@ def test_grouped_refusals(w12):
     assert call(devs, 3, flags=w12.W12_GEMM_SILU_MUL) == INVALID_ARG
     assert call(devs, 3, flags=1 << 20) == INVALID_ARG
     assert call(devs, 3) == 0
+
+
+@pytest.mark.parametrize("M", (1, 16))
+def test_grouped_timeout_then_correct(w12, M):
+    """A wait that nothing satisfies (test hook) ends the grouped launch with
+    W12_ERR_TIMEOUT in every handle of the group, not a hang; after the abort
+    the kernels run on whatever their rings hold, and every read of an escape
+    list stays inside its own matrix's list.  The next call is correct."""
+    TIMEOUT = 8
+    Ws, Wdec, _, devs = _prepared(w12, "heavy_mix_1024")
+    K = Ws[0].shape[1]
+    x = WL.activations(M, K, seed=950 + M)
+    xd = _xdev(x)
+    w12.w12_set_spin_limit(2_000_000)  # 2 ms
+    w12.w12_debug_inject_stall(True)
+    try:
+        w12.w12_gemm_grouped(xd, devs)
+        for W, d in zip(Ws, devs):
+            assert w12.w12_dev_status(d) == (TIMEOUT if W.shape[0] else 0)
+    finally:
+        w12.w12_debug_inject_stall(False)
+        w12.w12_set_spin_limit(0)
+    ys = w12.w12_gemm_grouped(xd, devs)
+    for W, Wd, y, d in zip(Ws, Wdec, ys, devs):
+        assert w12.w12_dev_status(d) == 0
+        if W.shape[0]:
+            got = y.cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(got - O.gemm(x, Wd)) <= BOUND * O.abs_gemm(x, W)), f"M={M}"
