@@ -5,11 +5,12 @@ with hidden 5120 / intermediate 17408 / 8 KV heads of 128 -- q 5120x5120,
 k 1024x5120, v 1024x5120, o 5120x5120, gate 17408x5120, up 17408x5120,
 down 5120x17408 -- with W ~ N(0, 0.02^2) x per-row U(0.5, 2) and 1e-4
 Student-t(2) x 0.5 outliers, x ~ N(0, 1).  One step = the 7 W12 GEMMs of one
-layer, launched as a decode step would: q/k/v read one activation vector and
-gate/up another, so k, v and up are launched input-ready (they may overlap the
-tail of the GEMM before them); q, o, gate and down wait for the kernel before
-them.  Steps rotate over several independently drawn layers, each ~0.5 GB of
-W12 data, so every step streams its weights from HBM (inputs > L2).
+layer in 4 launches, as a decode step issues them: q/k/v read one activation
+vector and run as one grouped launch, o alone, gate/up (one vector) as one
+grouped launch, down alone; every launch waits for the kernel before it
+(its input is, in a decode step, that kernel's output or produced after it).
+Steps rotate over several independently drawn layers, each ~0.5 GB of W12
+data, so every step streams its weights from HBM (inputs larger than L2).
 
 Prints one JSON line (rank 0).  `--impl reference` times the scalar CPU oracle
 on a bounded sample of the same workload instead.
@@ -17,6 +18,8 @@ on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
+import ctypes
 import hashlib
 import json
 import os
@@ -38,14 +41,13 @@ WORKLOAD = ("single-row decode projections, M=1: q/o 5120x5120, k/v 1024x5120, g
             "1e-4 Student-t(2)x0.5 outliers)")
 FALLBACK_HBM_GBS = 6800.0
 
-# Activations of one dense layer's projections: q, k and v read one vector,
-# gate and up another; o and down read the outputs of attention and of the MLP
-# activation.  In a decode step, the launches of k, v and up therefore find
-# their input complete before the preceding GEMM starts (input-ready launch);
-# q, o, gate and down wait for the kernel before them.
-ACT_GROUPS = {"qkv": 5120, "o": 5120, "gate_up": 5120, "down": 17408}
-PROJ_GROUP = {"q": "qkv", "k": "qkv", "v": "qkv", "o": "o", "gate": "gate_up", "up": "gate_up", "down": "down"}
-READY_IN_LAYER = {"k", "v", "up"}
+# The launches of one layer: (group, projections, K).  q/k/v read one
+# activation vector, gate/up another; o reads attention's output and down the
+# MLP activation.
+GROUPS = (("qkv", ("q", "k", "v"), 5120), ("o", ("o",), 5120), ("gate_up", ("gate", "up"), 5120),
+          ("down", ("down",), 17408))
+PROJ_GROUP = {p: g for g, ps, _ in GROUPS for p in ps}
+SIDE_G, SIDE_REPLAYS = 12, 10  # graph steps and replays of every leg besides the headline
 
 
 def _peaks():
@@ -58,15 +60,19 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _kernel_hash():
+def _kernel_hash(files):
     h = hashlib.sha256()
-    for f in ("gemm_fma.cu", "kernels.cuh", "ptx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "lossless_bit_weight_skinny_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic(name, alg_bytes_per_launch):
+KERNEL_FILES = {"gemm_fma": ("gemm_fma.cu", "kernels.cuh", "ptx.cuh"),
+                "gemm_tc": ("gemm_tc.cu", "kernels.cuh", "ptx.cuh")}
+
+
+def _traffic(name, kernel, alg_bytes_per_launch):
     """DRAM bytes per launch, from a committed ncu capture of one large launch
     of the same kernel: its DRAM/algorithmic byte ratio times this run's
     algorithmic bytes per launch (traffic grows in proportion to the weights
@@ -77,7 +83,7 @@ def _traffic(name, alg_bytes_per_launch):
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_sha") != _kernel_hash():
+    if d.get("kernel_sha") != _kernel_hash(KERNEL_FILES[kernel]):
         return None
     return int(d["traffic_over_algorithmic"] * alg_bytes_per_launch)
 
@@ -133,36 +139,6 @@ class ClockSampler:
                 "samples": len(loaded), "reasons": reasons}
 
 
-# ---------------------------------------------------------------------------------------
-# the CUDA path
-# ---------------------------------------------------------------------------------------
-
-def _make_layers(w12, torch, n_layers, seed0=1000):
-    """Draw, encode and upload `n_layers` layers; returns [[(name, Dev, stats)]]."""
-    layers = []
-    for li in range(n_layers):
-        projs = []
-        for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
-            wb = WL.projection_weights_torch(N, K, seed=seed0 + 16 * li + pi)
-            host = wb.cpu().numpy().view(np.uint16)
-            del wb
-            h = w12.w12_encode(host)
-            st = h.stats()
-            d = w12.w12_upload(h)
-            torch.cuda.synchronize()
-            projs.append((name, d, st))
-        layers.append(projs)
-    return layers
-
-
-def _step_bytes(layer, M):
-    """Algorithmic bytes of one step: W12 arrays (incl. metadata) + x + y."""
-    tot = 0
-    for name, d, st in layer:
-        tot += st["bytes_total"] - 40 + 2 * M * d.K + 4 * M * d.N
-    return tot
-
-
 def replica_aggregate(ms, rank_bytes, dist=None, device="cpu"):
     """Whole-job throughput of independent replicas: every rank streamed
     `rank_bytes` in its own `ms` of timed region; the job's time is the slowest
@@ -170,9 +146,7 @@ def replica_aggregate(ms, rank_bytes, dist=None, device="cpu"):
     (max ms, GB/s of the whole job)."""
     import torch
 
-    world = 1
     if dist is not None:
-        world = dist.get_world_size()
         t = torch.tensor([float(ms), float(rank_bytes)], dtype=torch.float64, device=device)
         tm = t[:1].clone()
         dist.all_reduce(tm, op=dist.ReduceOp.MAX)
@@ -182,6 +156,116 @@ def replica_aggregate(ms, rank_bytes, dist=None, device="cpu"):
     else:
         total = float(rank_bytes)
     return ms, total / (ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def _alg_bytes(st, M, N, K):
+    """Algorithmic bytes of one GEMM: its W12 arrays (incl. metadata) + x + y."""
+    return st["bytes_total"] - 40 + 2 * M * K + 4 * M * N
+
+
+def _make_layers(w12, torch, n_layers, seed0=1000):
+    """Draw, encode (host encoder) and upload `n_layers` layers:
+    [{name: (Dev, stats)}]."""
+    layers = []
+    for li in range(n_layers):
+        lay = {}
+        for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
+            wb = WL.projection_weights_torch(N, K, seed=seed0 + 16 * li + pi)
+            host = wb.cpu().numpy().view(np.uint16)
+            del wb
+            h = w12.w12_encode(host)
+            st = h.stats()
+            lay[name] = (w12.w12_upload(h), st)
+            torch.cuda.synchronize()
+        layers.append(lay)
+    return layers
+
+
+def _step_bytes(layer, M):
+    return sum(_alg_bytes(st, M, d.N, d.K) for d, st in layer.values())
+
+
+class Runner:
+    """Launches and graph timing on one stream."""
+
+    def __init__(self, w12, torch, stream):
+        self.w12, self.torch, self.stream = w12, torch, stream
+
+    def layer(self, lay, xs, ys, ready=False):
+        """One layer in 4 launches (grouped q/k/v and gate/up)."""
+        w12, st = self.w12, self.stream
+        for g, ps, _ in GROUPS:
+            if len(ps) > 1:
+                w12.w12_gemm_grouped(xs[g], [lay[p][0] for p in ps], [ys[p] for p in ps], st, input_ready=ready)
+            else:
+                w12.w12_gemm_ex(xs[g], lay[ps[0]][0], ys[ps[0]], st, input_ready=ready)
+
+    def layer_separate(self, lay, xs, ys):
+        """One layer in 7 launches; k, v and up input-ready (their input exists
+        before the GEMM ahead of them starts)."""
+        for name, _, _ in WL.LAYER_PROJECTIONS:
+            self.w12.w12_gemm_ex(xs[PROJ_GROUP[name]], lay[name][0], ys[name], self.stream,
+                                 input_ready=name in ("k", "v", "up"))
+
+    def capture(self, fn, G, warm=3):
+        torch = self.torch
+        for i in range(warm):
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(G):
+                fn(i)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(self, g, reps):
+        """ms of `reps` back-to-back replays, CUDA events on the stream."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def us_per_step(self, fn, G=SIDE_G, reps=SIDE_REPLAYS):
+        g = self.capture(fn, G)
+        return 1e3 * self.time_graph(g, reps) / (reps * G)
+
+
+def _layer_calls(lib, lay, xs, ys, M, stream, ready=False):
+    """The C calls of one layer (4 launches) with their argument lists:
+    [(function, args)]."""
+    P = ctypes.c_void_p
+    flags = 2 if ready else 0  # W12_GEMM_INPUT_READY
+    out = []
+    for g, ps, K in GROUPS:
+        x = P(xs[g].data_ptr())
+        if len(ps) > 1:
+            n = len(ps)
+            out.append((lib.w12_gemm_grouped, (x, (P * n)(*[lay[p][0].ptr for p in ps]),
+                                               (P * n)(*[ys[p].data_ptr() for p in ps]), n, M, K, flags,
+                                               P(stream.cuda_stream))))
+        else:
+            d = lay[ps[0]][0]
+            out.append((lib.w12_gemm_ex, (x, d.ptr, P(ys[ps[0]].data_ptr()), M, d.N, K, flags,
+                                          P(stream.cuda_stream))))
+    return out
+
+
+def _roofline(kernel, achieved, peak, peak_kind, traffic, launch_us, bytes_per_launch):
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "frac_of_8TBps": round(achieved / 8000.0, 4),
+            "traffic": traffic, "launch_us": round(launch_us, 3), "bytes_per_launch": int(bytes_per_launch)}
 
 
 def run_w12(args):
@@ -203,63 +287,48 @@ def run_w12(args):
         dist.init_process_group("nccl")
 
     layers = _make_layers(w12, torch, args.layers)
-    M = 1
-
-    def acts(Mx, seed):
-        """One activation vector per group (q/k/v share one, gate/up another)."""
-        return {g: torch.from_numpy(WL.activations(Mx, K, seed=seed + gi).view(np.int16)).cuda()
-                .view(torch.bfloat16) for gi, (g, K) in enumerate(ACT_GROUPS.items())}
-
-    xs = acts(M, 7)
-    ys = {name: torch.empty((M, N), dtype=torch.float32, device="cuda") for name, N, K in WL.LAYER_PROJECTIONS}
+    nl = len(layers)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    n_proj = len(WL.LAYER_PROJECTIONS)
+    R = Runner(w12, torch, stream)
+    peak, peak_kind = _peaks()
 
-    def launch(mode, name, d, x, y):
-        ready = mode == "independent" or (mode == "layer" and name in READY_IN_LAYER)
-        w12.w12_gemm_ex(x, d, y, stream, input_ready=ready)
+    def acts(Mx, seed):
+        """One activation tensor per launch group."""
+        return {g: torch.from_numpy(WL.activations(Mx, K, seed=seed + gi).view(np.int16)).cuda()
+                .view(torch.bfloat16) for gi, (g, _, K) in enumerate(GROUPS)}
 
-    def step(i, ev=None, mode="layer"):
-        layer = layers[i % len(layers)]
-        for j, (name, d, st) in enumerate(layer):
-            if ev is not None:
-                ev[j][0].record(stream)
-            launch(mode, name, d, xs[PROJ_GROUP[name]], ys[name])
-            if ev is not None:
-                ev[j][1].record(stream)
+    def outs(Mx):
+        return {name: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for name, N, K in WL.LAYER_PROJECTIONS}
 
-    for i in range(args.warmup):
-        step(i)
+    def check_status(lays):
+        for lay in lays:
+            for d, _ in lay.values():
+                assert w12.w12_dev_status(d) == 0, "device status"
+
+    M = 1
+    xs, ys = acts(M, 7), outs(M)
+    step_bytes = _step_bytes(layers[0], M)
+    n_launch_step = len(GROUPS)
+
+    # ---- headline: exactly --steps steps, launched one after another ----
+    # A plain host loop over the library's C entry points (argument lists
+    # built once), so that no graph boundary falls between two steps; the
+    # launches queue up ahead of the GPU (each takes a few microseconds to
+    # issue, each kernel runs 13-50).
+    lib = w12.lib()
+    calls = [_layer_calls(lib, lay, xs, ys, M, stream) for lay in layers]
+
+    def run_steps(n, i0=0):
+        for i in range(i0, i0 + n):
+            for fn, a in calls[i % nl]:
+                st_ = fn(*a)
+                if st_:
+                    raise RuntimeError(f"W12 GEMM launch failed: status {st_}")
+
+    run_steps(args.warmup)
     torch.cuda.synchronize()
-    for layer in layers:
-        for _, d, _ in layer:
-            assert w12.w12_dev_status(d) == 0
-
-    # The timed region replays one CUDA graph of G steps (rotating over the
-    # layers), with nothing between the GEMM launches so that each may overlap
-    # the previous one's tail (programmatic dependent launch).  Right after it,
-    # still on the same warm state, a second graph with an event pair around
-    # every launch gives each kernel's own duration (without that overlap).
-    G = args.graph_steps
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            step(i)
-    graph.replay()
-    torch.cuda.synchronize()
-    try:
-        evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-                for _ in range(n_proj)] for _ in range(G)]
-        graph_ev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_ev, stream=stream):
-            for i in range(G):
-                step(i, evs[i], mode="none")
-        graph_ev.replay()
-        torch.cuda.synchronize()
-    except TypeError:
-        evs, graph_ev = None, None
-    reps = max(1, args.steps // G)
+    check_status(layers)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     with sampler:
@@ -268,19 +337,20 @@ def run_w12(args):
             dist.barrier()
         torch.cuda.synchronize()
         t0.record(stream)
-        for _ in range(reps):
-            graph.replay()
+        run_steps(args.steps)
         t1.record(stream)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        if graph_ev is not None:
-            graph_ev.replay()
-            torch.cuda.synchronize()
     clocks = sampler.stop()
-    # per-replay spread of the same graph (after the timed region): each
-    # replay between its own event pair, so median and minimum per step
-    n_rep = min(reps, 50)
+    steps_timed = args.steps
+    ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * steps_timed, dist, "cuda")
+    check_status(layers)
+    us_layer = 1e3 * ms / steps_timed
+    # spread: the same steps as CUDA graphs of G steps, each replay between
+    # its own events (after the timed region)
+    G, n_rep = SIDE_G, 20
+    graph = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), G, warm=0)
     rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
     for e0, e1 in rev:
         e0.record(stream)
@@ -289,91 +359,62 @@ def run_w12(args):
     torch.cuda.synchronize()
     per_step = sorted(1e3 * e0.elapsed_time(e1) / G for e0, e1 in rev)
     step_stats = {"median_us": round(per_step[len(per_step) // 2], 2), "min_us": round(per_step[0], 2),
-                  "max_us": round(per_step[-1], 2), "replays": n_rep, "steps_per_replay": G}
-    args.steps = reps * G
-    step_bytes = _step_bytes(layers[0], M)
-    ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * args.steps, dist, "cuda")
-    for layer in layers:
-        for _, d, _ in layer:
-            assert w12.w12_dev_status(d) == 0, "device status after timing"
+                  "max_us": round(per_step[-1], 2), "replays": n_rep, "steps_per_replay": G,
+                  "note": "graph replays of the headline's step, after the timed region"}
+    del graph
+    # The timed region launches nothing but the M = 1 CUDA-core GEMM, back to
+    # back: its average launch duration is the timed region over the launches.
+    n_launch = steps_timed * n_launch_step
+    achieved = step_bytes * steps_timed / (ms * 1e-3) / 1e9
+    roofline = _roofline("gemm_fma_kernel<1,false> (M=1; grouped and single launches)", achieved, peak,
+                         peak_kind, _traffic("gemm_fma_m1", "gemm_fma", step_bytes / n_launch_step),
+                         1e3 * ms / n_launch, step_bytes / n_launch_step)
 
-    # per-launch durations of the dominant kernel (the M = 1 CUDA-core GEMM),
-    # from the event pairs of the measurement replay
-    kern_ms = 0.0
-    kern_bytes = 0
-    per_proj = {}
-    for i in range(G):
-        layer = layers[i % len(layers)]
-        for j, (name, d, st) in enumerate(layer):
-            bts = st["bytes_total"] - 40 + 2 * M * d.K + 4 * M * d.N
-            dt = evs[i][j][0].elapsed_time(evs[i][j][1]) if evs else None
-            if dt is None:
-                continue
-            kern_ms += dt
-            kern_bytes += bts
-            p = per_proj.setdefault(name, [0.0, 0, bts])
-            p[0] += dt
-            p[1] += 1
-    if not evs:  # no timing events in graphs: bound the kernel time by the step time
-        kern_ms, kern_bytes = ms, step_bytes * args.steps
-    peak, peak_kind = _peaks()
-    # The timed region launches nothing but the dominant kernel, back to back:
-    # its average launch duration is the timed region over the launch count.
-    n_launch = args.steps * n_proj
-    achieved = step_bytes * args.steps / (ms * 1e-3) / 1e9
-    achieved_isolated = kern_bytes / (kern_ms * 1e-3) / 1e9 if kern_ms else None
-    traffic = _traffic("gemm_fma_m1", step_bytes / n_proj)
+    # ---- the same layer in other launch forms (context) ----
+    modes_us = {
+        "grouped_dependent": round(us_layer, 2),
+        "separate_launches": round(R.us_per_step(lambda i: R.layer_separate(layers[i % nl], xs, ys)), 2),
+        "grouped_independent_inputs": round(R.us_per_step(lambda i: R.layer(layers[i % nl], xs, ys, ready=True)), 2),
+    }
+    check_status(layers)
 
-    def time_graph(Mx, xs_, ys_, mode, greps):
-        """Replay a G-step graph of the layer at Mx rows in launch mode `mode`;
-        returns ms per step."""
-        def stepm(i):
-            for name, d, st in layers[i % len(layers)]:
-                launch(mode, name, d, xs_[PROJ_GROUP[name]], ys_[name])
-
-        for i in range(max(3, args.warmup // 4)):
-            stepm(i)
-        torch.cuda.synchronize()
-        gm = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gm, stream=stream):
-            for i in range(G):
-                stepm(i)
-        gm.replay()
-        torch.cuda.synchronize()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(greps):
-            gm.replay()
-        s1.record(stream)
-        torch.cuda.synchronize()
-        for layer in layers:
-            for _, d, _ in layer:
-                assert w12.w12_dev_status(d) == 0
-        return s0.elapsed_time(s1) / (greps * G)
-
-    # the same step with every launch waiting for the previous kernel, and with
-    # every launch input-ready (the synthetic activations are all independent)
-    short = max(2, args.steps // (4 * G))
-    modes_us = {"layer": round(1e3 * ms / args.steps, 2),
-                "no_overlap": round(1e3 * time_graph(M, xs, ys, "none", short), 2),
-                "independent_inputs": round(1e3 * time_graph(M, xs, ys, "independent", short), 2)}
-
-    # the same layer at M = 32, 64, 128 (tensor-core path, one launch per
-    # projection) and 256 (two launches of 128 rows), shorter runs; GB/s counts
-    # the W12 bytes once
-    by_m = {"1": {"weight_GBps": round(value / world, 1), "us_per_layer": round(1e3 * ms / args.steps, 2)}}
-    for Mx in (32, 64, 128, 256):
-        xm = acts(Mx, 9)
-        ym = {n: torch.empty((Mx, N), dtype=torch.float32, device="cuda") for n, N, K in WL.LAYER_PROJECTIONS}
-        msm = time_graph(Mx, xm, ym, "layer", short)
+    # ---- the layer step at other row counts (tensor cores from 3 rows) ----
+    by_m = {"1": {"us_per_layer": round(us_layer, 2), "weight_GBps": round(achieved, 1),
+                  "frac": round(achieved / peak, 4)}}
+    roof_m = {}
+    for Mx in (2, 16, 32, 64, 128, 256):
+        xm, ym = acts(Mx, 9), outs(Mx)
+        us = R.us_per_step(lambda i: R.layer(layers[i % nl], xm, ym))
         bm = _step_bytes(layers[0], Mx)
-        by_m[str(Mx)] = {"weight_GBps": round(bm / (msm * 1e-3) / 1e9, 1), "us_per_layer": round(1e3 * msm, 2)}
+        gbs = bm / (us * 1e3)
+        by_m[str(Mx)] = {"us_per_layer": round(us, 2), "weight_GBps": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        if Mx in (32, 64):
+            roof_m[str(Mx)] = _roofline(f"gemm_tc_kernel<{Mx},false,false>", gbs, peak, peak_kind,
+                                        _traffic(f"gemm_tc_m{Mx}", "gemm_tc", bm / n_launch_step),
+                                        us / n_launch_step, bm / n_launch_step)
+    check_status(layers)
 
-    # Two-level-verification pair on a 17408x5120 matrix: the Q pass over the
-    # 8-bit view at M = 64 (draft-tree nodes), then the exact pass at M = 16, for
-    # the projection draw (the gate projection of the first layer) and for a
-    # heavy-tailed draw (Student-t 1.5, ~1e-2 escapes), the latter also with
-    # count-maximising windows (~2e-3 escapes; the top outliers escape instead).
+    # ---- row-count sweep on single matrices (17408x5120, 5120x17408) ----
+    sweep = {}
+    for pname in ("gate", "down"):
+        mats = [lay[pname] for lay in layers]
+        N, K = mats[0][0].N, mats[0][0].K
+        res = {}
+        for Mx in (1, 2, 4, 8, 16, 32, 64):
+            x = torch.from_numpy(WL.activations(Mx, K, seed=21).view(np.int16)).cuda().view(torch.bfloat16)
+            y = torch.empty((Mx, N), dtype=torch.float32, device="cuda")
+            us = R.us_per_step(lambda i: w12.w12_gemm_ex(x, mats[i % nl][0], y, stream))
+            b = _alg_bytes(mats[0][1], Mx, N, K)
+            res[str(Mx)] = {"us": round(us, 2), "weight_GBps": round(b / (us * 1e3), 1),
+                            "frac": round(b / (us * 1e3) / peak, 4)}
+        sweep[f"{N}x{K}"] = res
+    check_status(layers)
+
+    # ---- two-level-verification pair on 17408x5120 ----
+    # The Q pass over the 8-bit view at M = 64 (draft-tree nodes), then the
+    # exact pass at M = 16, for the projection draw (the gate projection of the
+    # first layer) and for a heavy-tailed draw (Student-t 1.5, ~1e-2 escapes),
+    # the latter also with count-maximising windows.
     tlv = {}
     heavy_w = WL.heavy_weights(17408, 5120, seed=31)
     hheavy = w12.w12_encode(heavy_w)
@@ -385,7 +426,7 @@ def run_w12(args):
     x16 = torch.from_numpy(WL.activations(16, 5120, seed=42).view(np.int16)).cuda().view(torch.bfloat16)
     y64 = torch.empty((64, 17408), dtype=torch.float32, device="cuda")
     y16 = torch.empty((16, 17408), dtype=torch.float32, device="cuda")
-    for dist_name, dm in (("projection", layers[0][4][1]), ("heavy_tail", wheavy),
+    for dist_name, dm in (("projection", layers[0]["gate"][0]), ("heavy_tail", wheavy),
                           ("heavy_tail_count_max_windows", wheavy_cm)):
         def run(kind, dm=dm):
             if kind in ("q8", "pair"):
@@ -395,44 +436,13 @@ def run_w12(args):
 
         res = {}
         for kind in ("q8", "exact", "pair"):
-            for _ in range(3):
-                run(kind)
-            torch.cuda.synchronize()
-            gt = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gt, stream=stream):
-                for _ in range(G):
-                    run(kind)
-            gt.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(short):
-                gt.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            res[kind + "_us"] = round(1e3 * e0.elapsed_time(e1) / (short * G), 2)
+            res[kind + "_us"] = round(R.us_per_step(lambda i, kind=kind: run(kind)), 2)
         assert w12.w12_dev_status(dm) == 0
         res["q8_view_GBps"] = round((17408 * 5120 + 2 * 64 * 5120 + 4 * 64 * 17408) / (res["q8_us"] * 1e3), 1)
         tlv[dist_name] = res
-    # the Q pass over a separate INT8 copy of the projection draw, at M = 64
-    q8c = w12.w12_i8_from_dev(layers[0][4][1], stream)
-    for _ in range(3):
-        w12.w12_gemm_i8(x64, q8c, y64, stream)
-    torch.cuda.synchronize()
-    gq = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gq, stream=stream):
-        for _ in range(G):
-            w12.w12_gemm_i8(x64, q8c, y64, stream)
-    gq.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(short):
-        gq.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    q8c = w12.w12_i8_from_dev(layers[0]["gate"][0], stream)
+    q_us = R.us_per_step(lambda i: w12.w12_gemm_i8(x64, q8c, y64, stream))
     assert w12.w12_i8_status(q8c) == 0
-    q_us = 1e3 * e0.elapsed_time(e1) / (short * G)
     tlv["projection"]["q_int8_copy_us"] = round(q_us, 2)
     tlv["projection"]["q_int8_copy_GBps"] = round((17408 * 5120 + 4 * 17408 + 2 * 64 * 5120 + 4 * 64 * 17408)
                                                   / (q_us * 1e3), 1)
@@ -443,52 +453,35 @@ def run_w12(args):
     wheavy.free()
     wheavy_cm.free()
 
-    # Fused projections (the same bytes, merged at encode time): q/k/v stacked
-    # into one 7168x5120 matrix and gate/up interleaved by rows into one
-    # 34816x5120 matrix (every W12 row carries its own window, and the escape
-    # tiles are 128 rows high, so merging rows is just a bigger matrix).  One
-    # step = qkv (BF16 out), o (BF16 out), gate_up with the SiLU*mul epilogue
-    # writing BF16 h[M][17408], and down reading h: each launch waits for the
-    # kernel before it, and down consumes gate_up's output, as in a decode step.
+    # ---- fused projections: the same bytes merged at encode time ----
+    # q/k/v stacked into one 7168x5120 matrix and gate/up interleaved by rows
+    # into one 34816x5120 matrix.  One step = qkv (BF16 out), o (BF16 out),
+    # gate_up with the SiLU*mul epilogue writing BF16 h[M][17408], and down
+    # reading h; each launch waits for the kernel before it.
     def fused_layer(li):
         out = []
-        for gname, parts in (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))):
-            ws = [WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi)
-                  for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS) if name in parts]
+        for gname, parts, _ in GROUPS:
+            wsl = [WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi)
+                   for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS) if name in parts]
             if gname == "gate_up":  # row 2i = gate row i, row 2i+1 = up row i
-                wcat = torch.stack(ws, 1).reshape(-1, ws[0].shape[1])
+                wcat = torch.stack(wsl, 1).reshape(-1, wsl[0].shape[1])
             else:
-                wcat = torch.cat(ws, 0) if len(ws) > 1 else ws[0]
+                wcat = torch.cat(wsl, 0) if len(wsl) > 1 else wsl[0]
             out.append((gname, w12.w12_encode_device(wcat, stream)))
-            del ws, wcat
+            del wsl, wcat
         return out
 
-    flayers = [fused_layer(li) for li in range(len(layers))]
+    flayers = [fused_layer(li) for li in range(nl)]
     f_out = {"qkv": (7168, torch.bfloat16), "o": (5120, torch.bfloat16), "gate_up": (17408, torch.bfloat16),
              "down": (5120, torch.float32)}
     fy = {g: torch.empty((M, n), dtype=dt, device="cuda") for g, (n, dt) in f_out.items()}
     fx = {"qkv": xs["qkv"], "o": xs["o"], "gate_up": xs["gate_up"], "down": fy["gate_up"]}
 
     def stepf(i):
-        for g, d in flayers[i % len(flayers)]:
+        for g, d in flayers[i % nl]:
             w12.w12_gemm_ex(fx[g], d, fy[g], stream, out_bf16=(g != "down"), silu_mul=(g == "gate_up"))
 
-    for i in range(3):
-        stepf(i)
-    torch.cuda.synchronize()
-    gf = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gf, stream=stream):
-        for i in range(G):
-            stepf(i)
-    gf.replay()
-    torch.cuda.synchronize()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(short):
-        gf.replay()
-    f1.record(stream)
-    torch.cuda.synchronize()
-    f_us = 1e3 * f0.elapsed_time(f1) / (short * G)
+    f_us = R.us_per_step(stepf)
     fused = {"us_per_layer": round(f_us, 2), "weight_GBps": round(step_bytes / (f_us * 1e3), 1),
              "step": "4 GEMMs: qkv 7168x5120 (BF16 out), o 5120x5120 (BF16 out), gate_up 34816x5120 "
                      "(gate/up rows interleaved; SiLU*mul epilogue, BF16 h[1][17408] out), down "
@@ -500,47 +493,69 @@ def run_w12(args):
             d.free()
     del flayers
 
-    # Context, not the target: the same layers as dense BF16 weights through
-    # torch.matmul (cuBLAS), graph-timed the same way (the pages compare the
-    # W12 GEMM with cuBLAS at 1 and 32 rows).
+    # ---- dense BF16 through cuBLAS (context: the pages compare with it) ----
     dense = None
     if not args.no_dense:
         dlayers = [[(name, WL.projection_weights_torch(N, K, seed=1000 + 16 * li + pi).view(torch.bfloat16))
-                    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS)] for li in range(len(layers))]
+                    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS)] for li in range(nl)]
         dense = {"us_per_layer": {}, "w12_speedup": {}}
-        for Mx, w12_us in ((1, modes_us["layer"]), (32, by_m["32"]["us_per_layer"]),
-                           (128, by_m["128"]["us_per_layer"])):
-            xdn = {g: v for g, v in acts(Mx, 9 if Mx > 1 else 7).items()}
+        for Mx in (1, 16, 32, 64, 128):
+            xdn = acts(Mx, 9 if Mx > 1 else 7)
 
-            def stepd(i):
-                for name, Wd in dlayers[i % len(dlayers)]:
+            def stepd(i, xdn=xdn):
+                for name, Wd in dlayers[i % nl]:
                     torch.matmul(xdn[PROJ_GROUP[name]], Wd.t())
 
-            for i in range(3):
-                stepd(i)
-            torch.cuda.synchronize()
-            gd = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gd, stream=stream):
-                for i in range(G):
-                    stepd(i)
-            gd.replay()
-            torch.cuda.synchronize()
-            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            d0.record(stream)
-            for _ in range(short):
-                gd.replay()
-            d1.record(stream)
-            torch.cuda.synchronize()
-            us = 1e3 * d0.elapsed_time(d1) / (short * G)
+            us = R.us_per_step(stepd)
             dense["us_per_layer"][str(Mx)] = round(us, 2)
-            dense["w12_speedup"][str(Mx)] = round(us / w12_us, 3)
+            dense["w12_speedup"][str(Mx)] = round(us / by_m[str(Mx)]["us_per_layer"], 3)
         dense["weight_bytes_per_layer"] = sum(2 * N * K for _, N, K in WL.LAYER_PROJECTIONS)
-        dense["note"] = "torch.matmul(x, W.t()) with BF16 W of the same seeds, BF16 out, one CUDA graph of G steps"
+        dense["note"] = ("torch.matmul(x, W.t()) per projection with BF16 W of the same seeds, BF16 out, "
+                         f"CUDA graphs of {SIDE_G} steps x {SIDE_REPLAYS} replays; speedup = dense time / "
+                         "W12 grouped-layer time")
         del dlayers
         torch.cuda.empty_cache()
 
-    # Conversion speed: one 17408x5120 BF16 matrix (178 MB) to W12, on the
-    # device (weights already there) and with the host encoder (all cores).
+    # ---- full decode step: 64 layers, 448 GEMMs back to back ----
+    deep = None
+    if args.deep_layers > 0:
+        def dev_bytes(d, Mx):
+            n_, k_, b_ = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+            w12.lib().w12_dev_info(d.ptr, ctypes.byref(n_), ctypes.byref(k_), ctypes.byref(b_))
+            return b_.value - 256 + 2 * Mx * d.K + 4 * Mx * d.N  # less the status word
+
+        dl = []
+        for li in range(args.deep_layers):
+            lay = {}
+            for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
+                wb = WL.projection_weights_torch(N, K, seed=5000 + 16 * li + pi)
+                lay[name] = (w12.w12_encode_device(wb, stream), None)
+                del wb
+            dl.append(lay)
+        torch.cuda.synchronize()
+        deep = {"layers": args.deep_layers, "gemms_per_step": 7 * args.deep_layers,
+                "launches_per_step": len(GROUPS) * args.deep_layers}
+        for Mx in (1, 32):
+            xm, ym = acts(Mx, 11), outs(Mx)
+            g = R.capture(lambda i: [R.layer(lay, xm, ym) for lay in dl], 1, warm=1)
+            reps_d = 5
+            ms_d = R.time_graph(g, reps_d) / reps_d
+            b = sum(dev_bytes(d, Mx) for lay in dl for d, _ in lay.values())
+            deep[f"M{Mx}"] = {"ms_per_step": round(ms_d, 3), "us_per_layer": round(1e3 * ms_d / args.deep_layers, 2),
+                              "weight_GBps": round(b / (ms_d * 1e6), 1), "frac": round(b / (ms_d * 1e6) / peak, 4),
+                              "replays": reps_d, "bytes_per_step": b}
+            del g
+        for lay in dl:
+            for d, _ in lay.values():
+                assert w12.w12_dev_status(d) == 0
+                d.free()
+        deep["note"] = ("weights drawn like the headline's (other seeds) and encoded on the device, ~31 GB of "
+                        "W12; one CUDA graph per step (4 launches a layer as in the headline), replayed; bytes "
+                        "are the W12 arrays as allocated (256-B padded) + x + y")
+        del dl
+        torch.cuda.empty_cache()
+
+    # ---- conversion speed: 17408x5120 BF16 (178 MB) to W12 ----
     wconv = WL.projection_weights_torch(17408, 5120, seed=77)
     t_dev = []
     for _ in range(3):
@@ -558,80 +573,73 @@ def run_w12(args):
                "device_GBps_bf16_in": round(2 * 17408 * 5120 / min(t_dev) / 1e9, 1),
                "host_cores": len(os.sched_getaffinity(0))}
 
-    # End to end: every step copies its activations from pinned host memory
-    # (one transfer: the four activation vectors of the layer, packed), runs
-    # the seven GEMMs through the public entry point, and copies the seven
-    # results back (one transfer), inside the timed loop.  The calls of G
-    # steps are captured once in a CUDA graph, as a serving loop would issue
-    # them, and replayed; wall-clock time on the host.
-    groups = list(ACT_GROUPS.items())
-    x_off, off = {}, 0
-    for g, K in groups:
-        x_off[g] = off
-        off += M * K
-    hx = torch.from_numpy(np.concatenate([WL.activations(M, K, seed=7 + gi).view(np.int16).ravel()
-                                          for gi, (g, K) in enumerate(groups)])).pin_memory()
-    dx = torch.empty(off, dtype=torch.int16, device="cuda")
-    dxv = {g: dx[x_off[g]:x_off[g] + M * K].view(torch.bfloat16).view(M, K) for g, K in groups}
-    y_off, off = {}, 0
-    for name, N, K in WL.LAYER_PROJECTIONS:
-        y_off[name] = off
-        off += M * N
-    hy = torch.empty(off, dtype=torch.float32).pin_memory()
-    dy = torch.empty(off, dtype=torch.float32, device="cuda")
-    dyv = {name: dy[y_off[name]:y_off[name] + M * N].view(M, N) for name, N, K in WL.LAYER_PROJECTIONS}
+    # ---- end to end through the library's host-buffer entry point ----
+    # Every step, for each of the layer's 4 launches, one w12_gemm_grouped_host
+    # call: H2D copy of the activations from pinned memory, the grouped GEMM,
+    # D2H copies of its outputs into pinned memory -- all on one stream, issued
+    # from this host thread in a plain loop (no graph); host wall clock from the
+    # first call to the stream's completion.
+    lib = w12.lib()
+    P = ctypes.c_void_p
+    hx = {g: torch.from_numpy(WL.activations(M, K, seed=7 + gi).view(np.int16)).pin_memory()
+          for gi, (g, _, K) in enumerate(GROUPS)}
+    dx = {g: torch.empty((M, K), dtype=torch.int16, device="cuda") for g, _, K in GROUPS}
+    dy = outs(M)
+    hy = {name: torch.empty((M, N), dtype=torch.float32).pin_memory() for name, N, K in WL.LAYER_PROJECTIONS}
+    e_args = []
+    for lay in layers:
+        calls = []
+        for g, ps, K in GROUPS:
+            n = len(ps)
+            calls.append((P(hx[g].data_ptr()), P(dx[g].data_ptr()), (P * n)(*[lay[p][0].ptr for p in ps]),
+                          (P * n)(*[dy[p].data_ptr() for p in ps]), (P * n)(*[hy[p].data_ptr() for p in ps]),
+                          n, M, K, 0, P(stream.cuda_stream)))
+        e_args.append(calls)
+    fn_host = lib.w12_gemm_grouped_host
 
     def step_e2e(i):
-        dx.copy_(hx, non_blocking=True)
-        for name, d, st in layers[i % len(layers)]:
-            launch("layer", name, d, dxv[PROJ_GROUP[name]], dyv[name])
-        hy.copy_(dy, non_blocking=True)
+        for a in e_args[i % nl]:
+            st_ = fn_host(*a)
+            if st_:
+                raise RuntimeError(f"w12_gemm_grouped_host: status {st_}")
 
     for i in range(args.warmup):
         step_e2e(i)
-    torch.cuda.synchronize()
-    graph_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_e2e, stream=stream):
-        for i in range(G):
-            step_e2e(i)
-    graph_e2e.replay()
-    torch.cuda.synchronize()
-    e_reps = max(2, args.steps // (2 * G))
-    e_steps = e_reps * G
+    stream.synchronize()
     if dist:
         dist.barrier()
-    torch.cuda.synchronize()
+    e_steps = args.steps
     tw = time.perf_counter()
-    for _ in range(e_reps):
-        graph_e2e.replay()
-    torch.cuda.synchronize()
+    for i in range(e_steps):
+        step_e2e(i)
+    stream.synchronize()
     e_s = time.perf_counter() - tw
-    # the job's time is the slowest rank's, its bytes the sum over ranks
+    check_status(layers)
     e_ms, e_gbs = replica_aggregate(1e3 * e_s, step_bytes * e_steps, dist, "cuda")
-    h2d = int(hx.numel() * 2)
-    d2h = int(hy.numel() * 4)
     e2e = {"value": round(e_gbs, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "us_per_layer": round(1e3 * e_ms / e_steps, 2),
-           "method": "per step: one H2D copy of the layer's activations from pinned memory, the 7 "
-                     "w12_gemm_ex calls, one D2H copy of the 7 results; the calls of "
-                     f"{G} steps captured in a CUDA graph and replayed; host wall clock"}
+           "h2d_bytes_per_step": int(sum(2 * M * K for _, _, K in GROUPS)),
+           "d2h_bytes_per_step": int(sum(4 * M * N for _, N, _ in WL.LAYER_PROJECTIONS)),
+           "us_per_layer": round(1e3 * e_ms / e_steps, 2), "steps": e_steps,
+           "method": "per step: 4 w12_gemm_grouped_host calls (q/k/v, o, gate/up, down), each an H2D copy "
+                     "of its activations from pinned memory, the GEMM and D2H copies of its outputs into "
+                     "pinned memory, on one stream; plain host loop, host wall clock"}
 
-    cpu = None
+    cpu = cpu_cfg = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
+        cpu_cfg = cpu_oracle_configs(args.cpu_seconds / 3)
 
     if rank == 0:
-        st_all = [st for _, _, st in layers[0]]
+        st_all = [st for _, st in layers[0].values()]
         line = {
             "metric": METRIC,
             "value": round(value, 1),
             "unit": "GB/s",
             "n_gpus": world,
-            "steps": args.steps,
+            "steps": steps_timed,
             "warmup": args.warmup,
-            "ms_per_step": round(ms / args.steps, 5),
-            "us_per_layer": round(1e3 * ms / args.steps, 2),
+            "ms_per_step": round(ms / steps_timed, 5),
+            "us_per_layer": round(us_layer, 2),
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -640,46 +648,36 @@ def run_w12(args):
             "config": {
                 "workload": WORKLOAD,
                 "M": M,
-                "layers_rotated": args.layers,
-                "step": "7 GEMMs (q,k,v,o,gate,up,down) of one layer; q/k/v share one activation "
-                        "vector and gate/up another; k, v and up launch input-ready (their input "
-                        "exists before the preceding GEMM starts), the others wait for the kernel "
-                        "before them",
+                "layers_rotated": nl,
+                "step": "the 7 GEMMs of one layer in 4 launches: q/k/v grouped (one launch), o, gate/up "
+                        "grouped, down; each launch waits for the kernel before it",
+                "launch": "plain host loop over the C entry points (w12_gemm_grouped, w12_gemm_ex), "
+                          "no graph; CUDA events around exactly the requested steps",
                 "bytes_per_step": step_bytes,
-                "l2": "inputs larger than L2: each step streams ~0.5 GB of W12 weights",
+                "l2": "inputs larger than L2: each step streams ~0.5 GB of W12 weights, rotating over "
+                      f"{nl} layers",
                 "escape_fraction": round(sum(s["n_escapes"] for s in st_all)
                                          / sum(s["N"] * s["K"] for s in st_all), 7),
                 "bits_per_weight": round(8 * sum(s["bytes_total"] for s in st_all)
                                          / sum(s["N"] * s["K"] for s in st_all), 4),
                 "parallelism": f"replicas x{world}",
             },
+            "roofline": roofline,
+            "roofline_by_M": roof_m,
             "by_M": by_m,
-            "us_per_layer_by_launch_mode": modes_us,
+            "us_per_layer_by_launch_form": modes_us,
+            "row_sweep": sweep,
             "two_level_verification_17408x5120": tlv,
+            "decode_step_64_layers": deep,
             "dense_bf16_cublas": dense,
-            "encode_17408x5120": convert,
             "fused_projections_m1": fused,
-            "per_projection_us_event_bracketed": {k: round(1e3 * v[0] / v[1], 2) for k, v in per_proj.items()},
-            "roofline": {
-                "bound": "hbm",
-                "kernel": "gemm_fma_kernel<1,false> (M=1)",
-                "achieved": round(achieved, 1),
-                "peak": peak,
-                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": traffic,
-                "frac_of_8TBps": round(achieved / 8000.0, 4),
-                "launch_us": round(1e3 * ms / n_launch, 3),
-                "bytes_per_launch": step_bytes // n_proj,
-                "achieved_event_bracketed": round(achieved_isolated, 1) if achieved_isolated else None,
-            },
+            "encode_17408x5120": convert,
             "e2e": e2e,
             "gpu_launches": n_launch,
             "clocks": clocks,
             "us_per_layer_spread": step_stats,
             "cpu_baseline": cpu,
+            "cpu_oracle_by_config": cpu_cfg,
         }
         print(json.dumps(line), flush=True)
     if dist:
@@ -687,36 +685,65 @@ def run_w12(args):
 
 
 # ---------------------------------------------------------------------------------------
-# the scalar CPU oracle (reference arm and CPU baseline)
+# the scalar CPU oracle (reference arm and CPU baselines)
 # ---------------------------------------------------------------------------------------
 
-def _oracle_sample(rows_frac: int, seed0=1000):
-    """Per projection: the first N/rows_frac rows, encoded by the oracle."""
+def _cores():
+    return len(os.sched_getaffinity(0))
+
+
+def _blocks(W, rows=128):
+    """A sampled matrix encoded by the oracle 128 rows at a time (a 128-row
+    block encodes exactly as inside the whole matrix: rows are independent and
+    escape tiles are 128 rows high)."""
     import oracle as O
 
-    out = []
-    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
-        R = max(1, N // rows_frac)
-        W = WL.projection_weights(R, K, seed=seed0 + pi)
-        blob = O.encode(W)
-        x = WL.activations(1, K, seed=7)
-        out.append((name, R, K, blob, x, len(blob) - 40 + 2 * K + 4 * R))
-    return out
+    return [O.encode(W[r:r + rows]) for r in range(0, W.shape[0], rows)]
 
 
-def _oracle_pass(sample, threads):
-    """Decode + float64 GEMM of every sampled projection, rows split over threads."""
-    import concurrent.futures as cf
-
+def _job_bytes(blob, M, q8):
     import oracle as O
 
-    def job(item):
-        name, R, K, blob, x, _ = item
-        W = O.decode(blob)
+    N, K, _, _ = O.blob_header(blob)
+    w = (len(blob) - 40) if not q8 else N * K + N  # the Q pass reads the A+E plane and the bases
+    return w + 2 * M * K + 4 * M * N
+
+
+def _run_jobs(jobs, threads):
+    """jobs: (blob, x_bits, q8).  Oracle decode (or 8-bit-view decode) + float64
+    GEMM of every job, spread over `threads` threads (the oracle's C calls
+    release the GIL)."""
+    import oracle as O
+
+    def one(job):
+        blob, x, q8 = job
+        W = O.decode_q8(blob) if q8 else O.decode(blob)
         return O.gemm(x, W)
 
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(job, sample))
+        list(ex.map(one, jobs))
+
+
+def _time_jobs(jobs, threads, budget_s, max_reps=20):
+    """(seconds per pass, passes): one probe pass, then as many as fit the budget."""
+    t = time.perf_counter()
+    _run_jobs(jobs, threads)
+    dt = time.perf_counter() - t
+    reps = max(1, min(max_reps, int(budget_s / max(dt, 1e-3))))
+    t = time.perf_counter()
+    for _ in range(reps):
+        _run_jobs(jobs, threads)
+    return (time.perf_counter() - t) / reps, reps
+
+
+def _layer_sample(frac, seed0=1000):
+    """The first N/frac rows of every projection of one layer, as 128-row blocks, M = 1."""
+    jobs = []
+    for pi, (name, N, K) in enumerate(WL.LAYER_PROJECTIONS):
+        W = WL.projection_weights(max(1, N // frac), K, seed=seed0 + pi)
+        x = WL.activations(1, K, seed=7)
+        jobs += [(b, x, False) for b in _blocks(W)]
+    return jobs
 
 
 def _cpu_model() -> str:
@@ -739,33 +766,75 @@ def _cpu_model() -> str:
 
 
 def cpu_baseline(seconds_budget: float):
-    """The oracle as it stands, timed on this host's cores on a bounded sample."""
+    """The oracle as it stands, on every host core, on a bounded sample of the
+    headline workload (row blocks spread over the cores)."""
     import oracle as O
 
     O.build()
-    cores = len(os.sched_getaffinity(0))
-    threads = min(cores, len(WL.LAYER_PROJECTIONS))
+    cores = _cores()
     frac = 16
-    sample = _oracle_sample(frac)
+    jobs = _layer_sample(frac)
+    dt, reps = _time_jobs(jobs, cores, seconds_budget)
+    nbytes = sum(_job_bytes(b, 1, q) for b, _, q in jobs)
     t = time.perf_counter()
-    _oracle_pass(sample, threads)
-    dt = time.perf_counter() - t
-    reps = max(1, int(seconds_budget / max(dt, 1e-3)))
-    reps = min(reps, 20)
-    t = time.perf_counter()
-    for _ in range(reps):
-        _oracle_pass(sample, threads)
-    dt = (time.perf_counter() - t) / reps
-    nbytes = sum(s[5] for s in sample)
-    t = time.perf_counter()
-    _oracle_pass(sample, 1)
+    _run_jobs(jobs, 1)
     dt1 = time.perf_counter() - t
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "value_1_thread": round(nbytes / dt1 / 1e9, 4), "cpu_model": _cpu_model(),
-            "kind": "oracle",
-            "sample": f"first 1/{frac} of the rows of each of the 7 projections of one layer, "
-                      f"M=1: oracle decode + float64 GEMM, projections in parallel threads, "
-                      f"{reps} reps; host has {cores} cores"}
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "value_1_thread": round(nbytes / dt1 / 1e9, 4), "cpu_model": _cpu_model(), "kind": "oracle",
+            "sample": f"first 1/{frac} of the rows of each of the 7 projections of one layer, M=1, as "
+                      f"{len(jobs)} blocks of 128 rows spread over {cores} threads: oracle decode + float64 "
+                      f"GEMM, {reps} passes"}
+
+
+def cpu_oracle_configs(budget_s: float):
+    """The oracle timed on the host cores for the tiny matrix, the row-count
+    sweep and the two-level-verification pair (bounded row samples)."""
+    import oracle as O
+
+    O.build()
+    cores = _cores()
+    out = {"cores": cores, "cpu_model": _cpu_model()}
+    # tiny 512x256: the whole matrix -- encode, decode, GEMM
+    W, x, _, _ = WL.tiny_weights(1)
+    t = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t < min(1.0, budget_s):
+        blob = O.encode(W)
+        O.gemm(x, O.decode(blob))
+        n += 1
+    dt = (time.perf_counter() - t) / n
+    out["tiny_512x256"] = {"us": round(1e6 * dt, 1), "GBps": round(_job_bytes(blob, 1, False) / dt / 1e9, 4),
+                           "sample": "whole matrix, M=1, one thread: oracle encode + decode + float64 GEMM"}
+    # row-count sweep: the first 128 rows a core of 17408x5120 and of 5120x17408
+    rows = 128 * max(4, min(cores, 16))
+    sweep = {}
+    for (N, K, seed) in ((17408, 5120, 1004), (5120, 17408, 1006)):
+        blobs = _blocks(WL.projection_weights(rows, K, seed=seed))
+        res = {}
+        for M in (1, 2, 4, 8, 16, 32, 64):
+            x = WL.activations(M, K, seed=21)
+            jobs = [(b, x, False) for b in blobs]
+            dt, reps = _time_jobs(jobs, cores, budget_s / 14, max_reps=5)
+            res[str(M)] = {"GBps": round(sum(_job_bytes(b, M, False) for b in blobs) / dt / 1e9, 4)}
+        sweep[f"{N}x{K}"] = {"by_M": res, "sample": f"first {rows} rows as {len(blobs)} blocks over {cores} threads"}
+    out["row_sweep"] = sweep
+    # two-level-verification pair: Q pass M=64 over the 8-bit view, exact M=16
+    tlv = {}
+    for dname, W in (("projection", WL.projection_weights(rows, 5120, seed=1004)),
+                     ("heavy_tail", WL.heavy_weights(rows, 5120, seed=31))):
+        blobs = _blocks(W)
+        x64, x16 = WL.activations(64, 5120, seed=41), WL.activations(16, 5120, seed=42)
+        dq, _ = _time_jobs([(b, x64, True) for b in blobs], cores, budget_s / 4, max_reps=5)
+        de, _ = _time_jobs([(b, x16, False) for b in blobs], cores, budget_s / 4, max_reps=5)
+        scale = 17408 / rows
+        tlv[dname] = {"q8_us_full_matrix_est": round(1e6 * dq * scale, 1),
+                      "exact_us_full_matrix_est": round(1e6 * de * scale, 1),
+                      "q8_GBps": round(sum(_job_bytes(b, 64, True) for b in blobs) / dq / 1e9, 4),
+                      "exact_GBps": round(sum(_job_bytes(b, 16, False) for b in blobs) / de / 1e9, 4)}
+    out["two_level_verification_17408x5120"] = {
+        **tlv, "sample": f"first {rows} of 17408 rows as {rows // 128} blocks over {cores} threads; "
+                         f"full-matrix times scaled by 17408/{rows}"}
+    return out
 
 
 def run_reference(args):
@@ -775,28 +844,31 @@ def run_reference(args):
     import oracle as O
 
     O.build()
-    cores = len(os.sched_getaffinity(0))
-    threads = min(cores, len(WL.LAYER_PROJECTIONS))
+    cores = _cores()
     # each step is a bounded sample (the first 1/frac of every projection's
     # rows), sized so that warm-up + steps take about 150 s in all
     frac = 64
-    sample = _oracle_sample(frac)
+    jobs = _layer_sample(frac)
     t = time.perf_counter()
-    _oracle_pass(sample, threads)
+    _run_jobs(jobs, cores)
     probe = time.perf_counter() - t
     per_step = min(0.25, 150.0 / max(1, args.steps + args.warmup))
-    while frac < 8192 and probe * 64 / frac > per_step:
-        frac *= 2
-    if frac != 64:
-        sample = _oracle_sample(frac)
+    f2 = frac
+    while f2 < 8192 and probe * frac / f2 > per_step:
+        f2 *= 2
+    if f2 != frac:
+        frac = f2
+        jobs = _layer_sample(frac)
     for _ in range(args.warmup):
-        _oracle_pass(sample, threads)
+        _run_jobs(jobs, cores)
     t = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_pass(sample, threads)
+        _run_jobs(jobs, cores)
     dt = time.perf_counter() - t
-    nbytes = sum(s[5] for s in sample) * args.steps
+    nbytes = sum(_job_bytes(b, 1, q) for b, _, q in jobs) * args.steps
     value = nbytes / dt / 1e9
+    sample = (f"first 1/{frac} of the rows of each of the 7 projections per step, as {len(jobs)} blocks of "
+              f"128 rows over {cores} threads: oracle decode + float64 GEMM")
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -811,11 +883,9 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "bf16 weights (W12) x bf16 activations, fp64 accumulate",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1,
-                   "sample": f"first 1/{frac} of the rows of each projection per step"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"first 1/{frac} of the rows of each of the 7 projections, "
-                                   "oracle decode + float64 GEMM per step"},
+        "config": {"workload": WORKLOAD, "M": 1, "sample": f"first 1/{frac} of the rows of each projection per step"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -854,7 +924,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--layers", type=int, default=3)
-    ap.add_argument("--graph-steps", type=int, default=12)
+    ap.add_argument("--deep-layers", type=int, default=64,
+                    help="layers of the full decode-step leg (0 skips it)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense BF16 (cuBLAS) comparison")

@@ -103,6 +103,7 @@ _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_q8view", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_ex", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_gemm_grouped", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
+_sig("w12_gemm_grouped_host", [_P, _P, _P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_gemm_host", [_P, _P, _P, _P, _P, _I, _I, _I, _P])
 _sig("w12_gemm_noalloc", [_P, _P, _P, _I, _I, _I, _P])
 _sig("w12_last_cuda_error", [], ctypes.c_char_p)
@@ -120,7 +121,7 @@ EXPORTED = (
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
     "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
     "w12_i8_encode_device", "w12_i8_from_dev", "w12_i8_free", "w12_i8_download", "w12_i8_status", "w12_gemm_i8",
-    "w12_gemm_plan", "w12_gemm_grouped",
+    "w12_gemm_plan", "w12_gemm_grouped", "w12_gemm_grouped_host",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -467,6 +468,21 @@ def w12_gemm_grouped(x, devs, ys=None, stream=None, q8view=False, input_ready=Fa
     _check(_lib.w12_gemm_grouped(ctypes.c_void_p(x.data_ptr()), hs, ps, n, M, K, flags, _stream_ptr(stream)),
            "w12_gemm_grouped")
     return ys
+
+
+def w12_gemm_grouped_host(x_host, x_dev, devs, ys_dev, ys_host, stream=None, out_bf16=False):
+    """H2D copy of x, one grouped GEMM over devs, a D2H copy of every output,
+    all on one stream (pinned host buffers; synchronise before reading)."""
+    devs = list(devs)
+    n = len(devs)
+    M, K = x_host.shape
+    hs = (_P * n)(*[d.ptr for d in devs])
+    pd = (_P * n)(*[y.data_ptr() for y in ys_dev])
+    ph = (_P * n)(*[y.data_ptr() for y in ys_host])
+    flags = W12_GEMM_OUT_BF16 if out_bf16 else 0
+    _check(_lib.w12_gemm_grouped_host(ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(x_dev.data_ptr()), hs, pd,
+                                      ph, n, M, K, flags, _stream_ptr(stream)), "w12_gemm_grouped_host")
+    return ys_host
 
 
 def w12_gemm_noalloc(x, d: Dev, y, stream=None):

@@ -565,15 +565,44 @@ w12_status w12_gemm_host(const uint16_t *x_host, void *x_dev, const w12_dev *w, 
     if (!x_host || !x_dev || !y_dev || !y_host)
         return W12_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(x_dev, x_host, sizeof(uint16_t) * static_cast<size_t>(M) * K,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return W12_ERR_CUDA;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, sizeof(uint16_t) * static_cast<size_t>(M) * K,
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
     const w12_status s = gemm_impl(x_dev, w, y_dev, M, N, K, st, false);
     if (s != W12_OK)
         return s;
-    if (cudaMemcpyAsync(y_host, y_dev, sizeof(float) * static_cast<size_t>(M) * N,
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return W12_ERR_CUDA;
+    e = cudaMemcpyAsync(y_host, y_dev, sizeof(float) * static_cast<size_t>(M) * N, cudaMemcpyDeviceToHost, st);
+    return e == cudaSuccess ? W12_OK : cuda_fail(e);
+}
+
+w12_status w12_gemm_grouped_host(const uint16_t *x_host, void *x_dev, const w12_dev *const *ws,
+                                 void *const *ys_dev, void *const *ys_host, int n, int M, int K, unsigned flags,
+                                 w12_stream_t stream)
+{
+    if (n < 1 || n > kMaxGroup || !ws || !ys_dev || !ys_host || M < 0 || K < 0)
+        return W12_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!ws[i] || (M > 0 && ws[i]->N > 0 && !ys_host[i]))
+            return W12_ERR_INVALID_ARG;
+    if (M == 0)
+        return W12_OK;
+    if (!x_host || !x_dev)
+        return W12_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, sizeof(uint16_t) * static_cast<size_t>(M) * K,
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    const w12_status s = w12_gemm_grouped(x_dev, ws, ys_dev, n, M, K, flags, stream);
+    if (s != W12_OK)
+        return s;
+    const size_t elem = (flags & W12_GEMM_OUT_BF16) ? 2 : 4;
+    for (int i = 0; i < n; ++i) {
+        const size_t bytes = elem * static_cast<size_t>(M) * ws[i]->N;
+        if (bytes && (e = cudaMemcpyAsync(ys_host[i], ys_dev[i], bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+            return cuda_fail(e);
+    }
     return W12_OK;
 }
 

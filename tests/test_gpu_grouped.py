@@ -181,3 +181,24 @@ def test_grouped_timeout_then_correct(w12, M):
         if W.shape[0]:
             got = y.cpu().numpy().astype(np.float64)
             assert np.all(np.abs(got - O.gemm(x, Wd)) <= BOUND * O.abs_gemm(x, W)), f"M={M}"
+
+
+@pytest.mark.parametrize("M", (1, 16))
+def test_grouped_host_buffers(w12, M):
+    """w12_gemm_grouped_host: x from pinned host memory, every output back in
+    pinned host memory, one stream; results against the oracle."""
+    import torch
+
+    Ws, Wdec, _, devs = _prepared(w12, "qkv_ragged_800")
+    K = Ws[0].shape[1]
+    x = WL.activations(M, K, seed=990 + M)
+    xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+    xd = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    yd = [torch.empty((M, W.shape[0]), dtype=torch.float32, device="cuda") for W in Ws]
+    yh = [torch.full((M, W.shape[0]), float("nan"), dtype=torch.float32).pin_memory() for W in Ws]
+    st = torch.cuda.current_stream()
+    w12.w12_gemm_grouped_host(xh, xd, devs, yd, yh, stream=st)
+    st.synchronize()
+    for W, Wd, y in zip(Ws, Wdec, yh):
+        got = y.numpy().astype(np.float64)
+        assert np.all(np.abs(got - O.gemm(x, Wd)) <= BOUND * O.abs_gemm(x, W)), f"M={M}"
