@@ -85,9 +85,44 @@ constexpr int kRegDecode = ((kRegLaunch * kThreads - 128 * kRegHelper) / (kDecod
 static_assert(kRegDecode * kDecodeWarps * 32 + kRegHelper * 128 <= kRegLaunch * kThreads,
               "register shares exceed the launch allocation");
 static_assert(kDecodeWarps % 4 == 0 && kGroupWarps % 4 == 0, "warpgroups of one role");
-constexpr int kEscCap = 256;                     // entries of a unit staged in shared memory
+#ifndef W12_TC_ESC_CAP
+#define W12_TC_ESC_CAP 512
+#endif
+constexpr int kEscCap = W12_TC_ESC_CAP;          // entries of a unit staged in shared memory
 constexpr int kPlSt = 2 * kGroups;               // escape-list stages (each serves one group)
-constexpr int kPark = 4;                         // rows patched at once per warp
+// Rows a decode warp patches at once (per activation-tile height).  Up to 32
+// activation rows every row of a warp has a parking slot, and a chunk takes
+// one round (measured on GB300, 17408 x 5120 at 16 / 32 rows: 33.8 / 35.2 us
+// with 4 rows a round, 30.9 / 31.7 with all 32); at 64 rows the 74 KB this
+// takes would leave one weight stage, so 8 rows a round.
+#ifndef W12_TC_PARK16
+#define W12_TC_PARK16 32
+#endif
+#ifndef W12_TC_PARK32
+#define W12_TC_PARK32 32
+#endif
+#ifndef W12_TC_PARK64
+#define W12_TC_PARK64 8
+#endif
+// Batches of 32 escape entries per patch round when a quadrant's list is
+// longer than a warp (32-row parking): measured on GB300 on 17408 x 5120 at
+// 16 rows with a dense escape tail (9e-3): 63.8 us with one batch a round,
+// 54.9 with 2, 51.2 with 4; on the projection draw at 32 rows, 31.3 us with
+// 2 and 32.3 with 4.
+#ifndef W12_TC_PATCH_BATCHES16
+#define W12_TC_PATCH_BATCHES16 4
+#endif
+#ifndef W12_TC_PATCH_BATCHES
+#define W12_TC_PATCH_BATCHES 2
+#endif
+#ifndef W12_TC_WST_MAX
+#define W12_TC_WST_MAX 6 // most weight stages
+#endif
+template <int MT>
+__host__ __device__ constexpr int park_rows()
+{
+    return MT == 16 ? W12_TC_PARK16 : MT == 32 ? W12_TC_PARK32 : MT == 64 ? W12_TC_PARK64 : 4;
+}
 constexpr int kParkPitch = 144;                  // bytes per parked row (128 + 16: banks spread)
 static_assert(kTcKStep == 256 && kTcRows == 128, "one unit = one escape tile");
 
@@ -115,7 +150,7 @@ struct TcSmem {
     // bounds[5], matrix}, then up to kEscCap entries
     static constexpr int PL_HDR = 32;
     static constexpr int PL = Q8 ? 0 : PL_HDR + 4 * kEscCap;
-    static constexpr int SCR = Q8 ? 0 : kDecodeWarps * kPark * kParkPitch;
+    static constexpr int SCR = Q8 ? 0 : kDecodeWarps * park_rows<MT>() * kParkPitch;
     // tensor memory (512 columns): NA decoded A tiles of 128 columns, then ND
     // FP32 accumulator buffers of DW columns (MT <= 64: 3 x 128 + 2 x 64;
     // MT = 128: 2 x 128 + 2 x 128; MT = 256: 2 x 128 + 1 x 256)
@@ -125,7 +160,7 @@ struct TcSmem {
     static constexpr int ND = MT == 256 ? 1 : 2;
     static constexpr int BUDGET = 227 * 1024 - 1024 - 640; // alignment slack, barriers
     static constexpr int WST_RAW = (BUDGET - XST * XSLOT - SCR - kPlSt * PL) / (WSTAGE + EB);
-    static constexpr int WST = WST_RAW > 6 ? 6 : WST_RAW; // weight stages
+    static constexpr int WST = WST_RAW > W12_TC_WST_MAX ? W12_TC_WST_MAX : WST_RAW; // weight stages
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W = XST * XSLOT;
     static constexpr int OFF_EB = OFF_W + WST * WSTAGE;
@@ -235,9 +270,49 @@ __device__ __forceinline__ void esc_window(const GemmArgs &a, int it0, int n_it,
 // Overwrite the escaped slots of one chunk (64 columns) in the 32 BF16 pairs v
 // of this thread's row.  e: one escape entry per lane, inj: it lies in this
 // chunk.  The rows holding such entries park their pairs in the warp's
-// scratch area, kPark rows at a time (in row order); every lane holding an
+// scratch area, PARK rows at a time (in row order); every lane holding an
 // entry of a parked row writes the exact 16 bits into the row's slot; the
 // rows take their pairs back.
+// With a parking slot for every row (PARK = 32): R batches of 32 entries in
+// one round -- every row holding one of them parks once, all entries are
+// written, the rows take their pairs back.
+template <int R>
+__device__ __forceinline__ void patch_rows(const uint32_t (&e)[R], const bool (&inj)[R], uint32_t q32, uint8_t *scr,
+                                           int lane, uint32_t (&v)[32])
+{
+    uint32_t mine_rows = 0u;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        mine_rows |= inj[r] ? 1u << (((e[r] >> 24) - q32) & 31u) : 0u;
+    const uint32_t rowmask = __reduce_or_sync(0xffffffffu, mine_rows);
+    const bool mine = (rowmask >> lane) & 1u;
+    uint8_t *const row_s = scr + lane * kParkPitch;
+    if (mine) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4 *>(row_s + 16 * i) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (inj[r])
+            *reinterpret_cast<uint16_t *>(scr + (((e[r] >> 24) - q32) & 31u) * kParkPitch + 2 * ((e[r] >> 16) & 63u)) =
+                static_cast<uint16_t>(e[r] & 0xFFFFu);
+    __syncwarp();
+    if (mine) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(row_s + 16 * i);
+            v[4 * i] = w.x;
+            v[4 * i + 1] = w.y;
+            v[4 * i + 2] = w.z;
+            v[4 * i + 3] = w.w;
+        }
+    }
+    __syncwarp();
+}
+
+template <int PARK>
 __device__ __forceinline__ void patch_chunk(uint32_t e, bool inj, uint32_t q32, uint8_t *scr, int lane,
                                             uint32_t (&v)[32])
 {
@@ -248,8 +323,8 @@ __device__ __forceinline__ void patch_chunk(uint32_t e, bool inj, uint32_t q32, 
     const uint32_t myrank = __popc(rowmask & ((1u << lane) - 1u));
     const uint32_t erank = __popc(rowmask & ((1u << rl) - 1u));
     uint8_t *const my_slot0 = scr + 2 * ((e >> 16) & 63u);
-    for (uint32_t r0 = 0; r0 < nrows; r0 += kPark) {
-        const bool park = mine && myrank - r0 < static_cast<uint32_t>(kPark);
+    for (uint32_t r0 = 0; r0 < nrows; r0 += PARK) {
+        const bool park = mine && myrank - r0 < static_cast<uint32_t>(PARK);
         uint8_t *row_s = scr + (myrank - r0) * kParkPitch;
         if (park) {
 #pragma unroll
@@ -258,7 +333,7 @@ __device__ __forceinline__ void patch_chunk(uint32_t e, bool inj, uint32_t q32, 
                     make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         __syncwarp();
-        if (inj && erank - r0 < static_cast<uint32_t>(kPark))
+        if (inj && erank - r0 < static_cast<uint32_t>(PARK))
             *reinterpret_cast<uint16_t *>(my_slot0 + (erank - r0) * kParkPitch) = static_cast<uint16_t>(e & 0xFFFFu);
         __syncwarp();
         if (park) {
@@ -324,18 +399,44 @@ __device__ __forceinline__ void decode_chunk(const uint4 (&aq)[NA], const uint4 
 
 // Patch the escapes of 64-column chunk jc of the unit into v: the quadrant's
 // entries qlo .. qlo + qn of list `esrc` (the first 32 already in e_first,
-// one per lane).
+// one per lane).  (Gathering a chunk's entries across batches of 32 before a
+// round was measured slower on GB300: 33.1 against 31.7 us at 16 rows, and no
+// faster on a dense escape tail.)
+template <int PARK, int R>
 __device__ __forceinline__ void patch_entries(uint32_t qlo, uint32_t qn, uint32_t e_first, const uint32_t *esrc,
                                               int jc, uint32_t q32, uint8_t *scr, int lane, uint32_t (&v)[32])
 {
-    for (uint32_t i0 = 0; i0 < qn; i0 += 32) {
-        const uint32_t idx = i0 + static_cast<uint32_t>(lane);
-        uint32_t e = e_first;
-        if (i0 != 0)
-            e = idx < qn ? esrc[qlo + idx] : 0u;
-        const bool inj = idx < qn && ((e >> 22) & 3u) == static_cast<uint32_t>(jc);
-        if (__any_sync(0xffffffffu, inj))
-            patch_chunk(e, inj, q32, scr, lane, v);
+    if constexpr (PARK >= 32) {
+        if (qn <= 32u) { // one batch: the common case
+            const uint32_t e[1] = {e_first};
+            const bool inj[1] = {static_cast<uint32_t>(lane) < qn && ((e_first >> 22) & 3u) == static_cast<uint32_t>(jc)};
+            if (__any_sync(0xffffffffu, inj[0]))
+                patch_rows<1>(e, inj, q32, scr, lane, v);
+            return;
+        }
+        for (uint32_t i0 = 0; i0 < qn; i0 += 32 * R) {
+            uint32_t e[R];
+            bool inj[R], any = false;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t idx = i0 + 32 * r + static_cast<uint32_t>(lane);
+                e[r] = (r == 0 && i0 == 0) ? e_first : (idx < qn ? esrc[qlo + idx] : 0u);
+                inj[r] = idx < qn && ((e[r] >> 22) & 3u) == static_cast<uint32_t>(jc);
+                any = any || inj[r];
+            }
+            if (__any_sync(0xffffffffu, any))
+                patch_rows<R>(e, inj, q32, scr, lane, v);
+        }
+    } else {
+        for (uint32_t i0 = 0; i0 < qn; i0 += 32) {
+            const uint32_t idx = i0 + static_cast<uint32_t>(lane);
+            uint32_t e = e_first;
+            if (i0 != 0)
+                e = idx < qn ? esrc[qlo + idx] : 0u;
+            const bool inj = idx < qn && ((e >> 22) & 3u) == static_cast<uint32_t>(jc);
+            if (__any_sync(0xffffffffu, inj))
+                patch_chunk<PARK>(e, inj, q32, scr, lane, v);
+        }
     }
 }
 
@@ -623,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * q + lane; // this thread's row in the unit = TMEM lane
         const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t q32 = static_cast<uint32_t>(32 * q);
-        uint8_t *const scr = smem + L::OFF_SCR + warp * kPark * kParkPitch;
+        uint8_t *const scr = smem + L::OFF_SCR + warp * park_rows<MT>() * kParkPitch;
         const uint32_t bm1 = a.bshift_mul[0], bm2 = a.bshift_mul[1], bm3 = a.bshift_mul[2];
         uint32_t acc_use0 = 0u, acc_use1 = 0u; // this group's epilogues per accumulator buffer
         constexpr int NA16 = kCols / 16, NB16 = kCols / 32; // 16-byte chunks of this thread's AE / B bytes
@@ -704,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[32];
                 decode_chunk<Q8, I8>(aq, bq, j, eb2, bm1, bm2, bm3, v);
                 if (!Q8)
-                    patch_entries(qlo, qn, e_first, esrc, hh * kChunks + j, q32, scr, lane, v);
+                    patch_entries<park_rows<MT>(), MT == 16 ? W12_TC_PATCH_BATCHES16 : W12_TC_PATCH_BATCHES>(qlo, qn, e_first, esrc, hh * kChunks + j, q32, scr, lane, v);
                 if (j == 0) {
                     // before the first store the MMA must be done with this A
                     // buffer (unit it - NA: the completions on this group's
