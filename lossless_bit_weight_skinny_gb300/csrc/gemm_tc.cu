@@ -90,11 +90,12 @@ static_assert(kDecodeWarps % 4 == 0 && kGroupWarps % 4 == 0, "warpgroups of one 
 #endif
 constexpr int kEscCap = W12_TC_ESC_CAP;          // entries of a unit staged in shared memory
 constexpr int kPlSt = 2 * kGroups;               // escape-list stages (each serves one group)
-// Rows a decode warp patches at once (per activation-tile height).  Up to 32
+// Rows a decode warp patches at once (per activation-tile height).  Up to 64
 // activation rows every row of a warp has a parking slot, and a chunk takes
 // one round (measured on GB300, 17408 x 5120 at 16 / 32 rows: 33.8 / 35.2 us
-// with 4 rows a round, 30.9 / 31.7 with all 32); at 64 rows the 74 KB this
-// takes would leave one weight stage, so 8 rows a round.
+// with 4 rows a round, 30.9 / 31.7 with all 32; 64 rows: see the activation
+// slots below); from 128 rows the 74 KB this takes would leave too little
+// room for the weights, so 4 rows a round.
 #ifndef W12_TC_PARK16
 #define W12_TC_PARK16 32
 #endif
@@ -102,7 +103,7 @@ constexpr int kPlSt = 2 * kGroups;               // escape-list stages (each ser
 #define W12_TC_PARK32 32
 #endif
 #ifndef W12_TC_PARK64
-#define W12_TC_PARK64 8
+#define W12_TC_PARK64 32
 #endif
 // Batches of 32 escape entries per patch round when a quadrant's list is
 // longer than a warp (32-row parking): measured on GB300 on 17408 x 5120 at
@@ -114,6 +115,15 @@ constexpr int kPlSt = 2 * kGroups;               // escape-list stages (each ser
 #endif
 #ifndef W12_TC_PATCH_BATCHES
 #define W12_TC_PATCH_BATCHES 2
+#endif
+// At 64 rows the exact pass holds half a unit's activations per ring slot
+// (three slots of 16 KB instead of two of 32 KB), which leaves room for a
+// parking slot per row: measured on GB300, 17408 x 5120: 36.4 us with whole-unit
+// slots and 8 rows a round, 37.8 with half-unit slots alone, 33.3 with both
+// (5120 x 17408: 40.1 -> 37.5); the Q pass keeps whole-unit slots (20.3 against
+// 20.6 us).
+#ifndef W12_TC_SPS64
+#define W12_TC_SPS64 2 // 64-column activation sub-tiles per ring slot at 64 rows (exact pass)
 #endif
 #ifndef W12_TC_WST_MAX
 #define W12_TC_WST_MAX 6 // most weight stages
@@ -135,10 +145,10 @@ struct TcSmem {
     // slots, fewer than a unit's four: a slot is reloaded within the unit as
     // soon as the MMAs that read it complete)
     static constexpr int XSUB = MT * 128;
-    static constexpr int SPS = MT >= 128 ? 1 : 4;
+    static constexpr int SPS = MT >= 128 ? 1 : (MT == 64 && !Q8) ? W12_TC_SPS64 : 4;
     static constexpr int SPU = 4 / SPS; // slots per unit
     static constexpr int XSLOT = SPS * XSUB;
-    static constexpr int XST = MT <= 32 ? 3 : MT == 64 ? 2 : MT == 128 ? W12_TC_XST128 : 3;
+    static constexpr int XST = MT <= 32 ? 3 : MT == 64 ? (SPS == 4 ? 2 : 3) : MT == 128 ? W12_TC_XST128 : 3;
     // weight stage: AE as two 128-column halves and B, each 128 rows of 128
     // bytes with the 128-byte swizzle; the rows' window bases beside it
     static constexpr int AE_HALF = 128 * 128;
