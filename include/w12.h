@@ -236,6 +236,16 @@ typedef struct {
 
 w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count, w12_gemm_plan_t *out);
 
+/*
+ * The launch w12_gemm_grouped makes for n matrices of Ns[i] rows (all with K
+ * columns), M activation rows and `sm_count` SMs: the row blocks of all of
+ * them end to end (row_blocks is their total), the rest as w12_gemm_plan.
+ * 1 <= n <= W12_MAX_GROUP; a group of one plans as w12_gemm_plan.  Errors:
+ * INVALID_ARG (no Ns, n out of range, a negative size), UNSUPPORTED and CUDA
+ * as w12_gemm_plan.
+ */
+w12_status w12_gemm_plan_grouped(int M, const int64_t *Ns, int n, int64_t K, int sm_count, w12_gemm_plan_t *out);
+
 /* Flags of w12_gemm_ex. */
 enum {
     W12_GEMM_Q8VIEW = 1,      /* the Q pass (as w12_gemm_q8view) instead of the exact GEMM */

@@ -97,6 +97,7 @@ _sig("w12_i8_download", [_P, _P, _P, _P])
 _sig("w12_i8_status", [_P, _P])
 _sig("w12_gemm_i8", [_P, _P, _P, _I, _I, _I, ctypes.c_uint, _P])
 _sig("w12_gemm_plan", [_I, _I64, _I64, _I, ctypes.POINTER(GemmPlan)])
+_sig("w12_gemm_plan_grouped", [_I, ctypes.POINTER(_I64), _I, _I64, _I, ctypes.POINTER(GemmPlan)])
 _sig("w12_download", [_P, _P, ctypes.POINTER(_P)])
 _sig("w12_dev_info", [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_size_t)])
 _sig("w12_gemm", [_P, _P, _P, _I, _I, _I, _P])
@@ -121,7 +122,7 @@ EXPORTED = (
     "w12_debug_inject_stall", "w12_gemm_noalloc", "w12_last_cuda_error", "w12_gemm_ex",
     "w12_encode_device", "w12_download", "w12_encode_ex", "w12_encode_device_ex",
     "w12_i8_encode_device", "w12_i8_from_dev", "w12_i8_free", "w12_i8_download", "w12_i8_status", "w12_gemm_i8",
-    "w12_gemm_plan", "w12_gemm_grouped", "w12_gemm_grouped_host",
+    "w12_gemm_plan", "w12_gemm_grouped", "w12_gemm_grouped_host", "w12_gemm_plan_grouped",
 )
 
 W12_GEMM_Q8VIEW = 1
@@ -529,6 +530,15 @@ def w12_debug_inject_stall(on: bool):
 def lib():
     """The loaded ctypes library (for tests that call the C ABI directly)."""
     return _lib
+
+
+def w12_gemm_plan_grouped(M: int, Ns, K: int, sm_count: int = 0) -> dict:
+    """The launch w12_gemm_grouped makes for matrices of Ns rows (same K)."""
+    Ns = list(Ns)
+    arr = (_I64 * max(1, len(Ns)))(*Ns)
+    p = GemmPlan()
+    _check(_lib.w12_gemm_plan_grouped(M, arr, len(Ns), K, sm_count, ctypes.byref(p)), "w12_gemm_plan_grouped")
+    return p.as_dict()
 
 
 def w12_gemm_plan(M: int, N: int, K: int, sm_count: int = 0) -> dict:

@@ -492,14 +492,23 @@ w12_status w12_gemm_q8view(const void *x_bf16, const w12_dev *w, float *y, int M
     return gemm_impl(x_bf16, w, y, M, N, K, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
-w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count_arg, w12_gemm_plan_t *out)
+w12_status w12_gemm_plan_grouped(int M, const int64_t *Ns, int n, int64_t K, int sm_count_arg,
+                                 w12_gemm_plan_t *out)
 {
-    if (!out || M < 0 || N < 0 || K < 0)
+    if (!out || !Ns || n < 1 || n > kMaxGroup || M < 0 || K < 0)
         return W12_ERR_INVALID_ARG;
     *out = w12_gemm_plan_t{};
-    if (M > kMaxM || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    int64_t rows = 0;
+    for (int i = 0; i < n; ++i) {
+        if (Ns[i] < 0)
+            return W12_ERR_INVALID_ARG;
+        if (Ns[i] > (int64_t(1) << 31))
+            return W12_ERR_UNSUPPORTED;
+        rows += Ns[i];
+    }
+    if (M > kMaxM || K > (int64_t(1) << 31))
         return W12_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0 || K == 0)
+    if (M == 0 || rows == 0 || K == 0)
         return W12_OK; // nothing is launched
     if (K % 32 != 0)
         return W12_ERR_UNSUPPORTED;
@@ -513,7 +522,7 @@ w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count_arg, w12_gemm
             return W12_ERR_CUDA;
     }
     Plan pl;
-    const w12_status ps = make_plan(M, N, K, sms, &pl);
+    const w12_status ps = make_plan_group(M, Ns, n, K, sms, &pl);
     if (ps != W12_OK)
         return ps;
     out->kernel = pl.tc ? 2 : 1;
@@ -532,6 +541,13 @@ w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count_arg, w12_gemm
     out->separate_fixup = pl.defer && split > 0 ? 1 : 0;
     out->partial_bytes = split > 0 ? pl.part_bytes : 0;
     return W12_OK;
+}
+
+w12_status w12_gemm_plan(int M, int64_t N, int64_t K, int sm_count_arg, w12_gemm_plan_t *out)
+{
+    if (!out || M < 0 || N < 0 || K < 0)
+        return W12_ERR_INVALID_ARG;
+    return w12_gemm_plan_grouped(M, &N, 1, K, sm_count_arg, out);
 }
 
 w12_status w12_gemm_ex(const void *x_bf16, const w12_dev *w, void *y, int M, int N, int K,

@@ -286,3 +286,36 @@ def test_gemm_plan_invariants(w12):
         w12.w12_gemm_plan(1, 64, 200, 152)   # K % 32 != 0
     with pytest.raises(w12.W12Error):
         w12.w12_gemm_plan(257, 64, 256, 152)
+
+
+def test_gemm_plan_grouped(w12):
+    """The grouped launch's planning: the row blocks of all matrices end to
+    end.  When every matrix's rows fill whole row blocks, the group plans
+    exactly like one matrix of all their rows; ragged matrices each start a
+    row block of their own; a group of one is w12_gemm_plan."""
+    rng = np.random.Generator(np.random.PCG64(78))
+    for M in (1, 2, 3, 16, 32, 64, 65, 128, 256):
+        # q/k/v and gate/up of a 5120-wide layer
+        for Ns in ([5120, 1024, 1024], [17408, 17408]):
+            g = w12.w12_gemm_plan_grouped(M, Ns, 5120, 152)
+            assert g == w12.w12_gemm_plan(M, sum(Ns), 5120, 152), (M, Ns)
+        for _ in range(20):
+            Ns = [int(v) for v in rng.integers(0, 9000, size=int(rng.integers(1, 5)))]
+            K = 32 * int(rng.integers(1, 400))
+            sms = int(rng.choice([8, 132, 152]))
+            g = w12.w12_gemm_plan_grouped(M, Ns, K, sms)
+            if sum(Ns) == 0:
+                assert g["kernel"] == 0
+                continue
+            assert g["row_blocks"] == sum(-(-n // g["block_rows"]) for n in Ns)
+            assert g["k_steps"] == -(-K // 256)
+            assert 1 <= g["grid"] <= min(g["row_blocks"] * g["k_steps"], sms - (4 if M <= 2 else 0))
+            assert g["kernel"] == (1 if M <= 2 else 2)
+            if len(Ns) == 1:
+                assert g == w12.w12_gemm_plan(M, Ns[0], K, sms)
+    with pytest.raises(w12.W12Error):
+        w12.w12_gemm_plan_grouped(1, [64] * 5, 256, 152)   # more than four matrices
+    with pytest.raises(w12.W12Error):
+        w12.w12_gemm_plan_grouped(1, [], 256, 152)
+    with pytest.raises(w12.W12Error):
+        w12.w12_gemm_plan_grouped(1, [64, -1], 256, 152)
