@@ -469,15 +469,15 @@ inline int64_t tc_min_iters(int M)
     return std::max<int64_t>(1, (static_cast<int64_t>(M) + ratio - 1) / ratio);
 }
 
-// SMs the CUDA-core kernel leaves out of its grid.  A launch's CTAs start in
-// block order as the previous kernel's CTAs free their SMs, and the last few
-// start after its activations are ready and end a few microseconds after the
-// rest, which delays the next launch that reads their output; with four SMs
-// left out, no CTA waits for the last SMs to free.  Measured on GB300 on the
-// single-row layer step: 109.5 -> 108.6 us (0, 8 and 16 reserved: 109.5,
-// 109.1, 109.0).
+// SMs the CUDA-core kernel leaves out of its grid (at most one in eight).  A
+// launch's CTAs start as the previous kernel's CTAs free their SMs; with some
+// SMs left out, the first CTAs start at once, and at 16 of 152 the grid is
+// 136 CTAs, which holds two whole 128-row blocks of a 34816-row (gate/up)
+// group per CTA with no split.  Measured on GB300 on the grouped single-row
+// layer step: 4 / 8 / 12 / 16 / 24 SMs left out: 100.9 / 101.1 / 100.3 /
+// 99.8 / 107.1 us.
 #ifndef W12_FMA_SM_RESERVE
-#define W12_FMA_SM_RESERVE 4
+#define W12_FMA_SM_RESERVE 16
 #endif
 inline int choose_grid(int64_t n_rowblk, int64_t n_kstep, int sms, int64_t min_iters)
 {
