@@ -476,6 +476,15 @@ inline int64_t tc_min_iters(int M)
 // group per CTA with no split.  Measured on GB300 on the grouped single-row
 // layer step: 4 / 8 / 12 / 16 / 24 SMs left out: 100.9 / 101.1 / 100.3 /
 // 99.8 / 107.1 us.
+// SMs the tensor-core kernel leaves out of its grid (at most one in eight):
+// at 136 CTAs the gate/up group and 17408-row matrices split into whole row
+// blocks, and the split-K tail goes.  Measured on GB300, grouped layer step
+// at 16 / 32 / 64 / 128 rows: none left out 125.6 / 129.0 / 146.9 / - us;
+// 8: 125.3 / 128.7 / 146.7 / 201.7; 16: 124.4 / 126.6 / 138.8 / 184.6;
+// 24: 130.4 / 132.8 / 148.7 / 209.2.
+#ifndef W12_TC_SM_RESERVE
+#define W12_TC_SM_RESERVE 16
+#endif
 #ifndef W12_FMA_SM_RESERVE
 #define W12_FMA_SM_RESERVE 16
 #endif

@@ -198,7 +198,8 @@ w12_status make_plan_group(int M, const int64_t *Ns, int n, int64_t K, int sms, 
     // 48 KB of W12, its partial is M x 512 B)
     const int64_t min_iters = q.tc ? tc_min_iters(M) : W12_FMA_MIN_ITERS;
     const int fma_sms = std::max(1, sms * fma_ctas_per_sm(q.mt) - std::min(W12_FMA_SM_RESERVE, sms / 8));
-    q.grid = choose_grid(q.n_rowblk, q.n_kstep, q.tc ? sms : fma_sms, min_iters);
+    const int tc_sms = std::max(1, sms - std::min(W12_TC_SM_RESERVE, sms / 8));
+    q.grid = choose_grid(q.n_rowblk, q.n_kstep, q.tc ? tc_sms : fma_sms, min_iters);
     q.part_bytes = sizeof(float) * 2 * static_cast<size_t>(q.grid) * M * q.rows_blk;
     *p = q;
     return W12_OK;

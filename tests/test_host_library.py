@@ -246,10 +246,10 @@ def test_package_fails_loudly_without_the_library(tmp_path):
 @pytest.mark.parametrize("M,N,K,kernel,tile,grid,split", [
     (1, 17408, 5120, 1, 1, 136, 0),    # aligned: one whole row block per CTA
     (1, 1024, 5120, 1, 1, 80, 8),      # aligned: 10 CTAs share each of 8 row blocks
-    (1, 5120, 5120, 1, 1, 136, 40),    # stream-K over 152 - 16 SMs
+    (1, 5120, 5120, 1, 1, 136, 40),    # stream-K over 152 - 16 SMs (both kernels)
     (1, 5120, 17408, 1, 1, 136, 40),
     (2, 5120, 5120, 1, 2, 136, 40),
-    (3, 5120, 5120, 2, 16, 152, 40),   # tensor cores from 3 rows
+    (3, 5120, 5120, 2, 16, 136, 40),   # tensor cores from 3 rows
     (16, 17408, 5120, 2, 16, 136, 0),
     (64, 17408, 5120, 2, 64, 136, 0),
     (65, 1024, 5120, 2, 128, 80, 8),
@@ -275,7 +275,7 @@ def test_gemm_plan_invariants(w12):
         assert p["kernel"] == (1 if M <= 2 else 2)
         assert p["tile_rows"] >= M and (p["tile_rows"] == M or p["tile_rows"] // 2 < M or p["tile_rows"] == 16)
         assert p["row_blocks"] == -(-N // p["block_rows"]) and p["k_steps"] == -(-K // 256)
-        assert 1 <= p["grid"] <= min(units, sms - (min(16, sms // 8) if M <= 2 else 0))
+        assert 1 <= p["grid"] <= min(units, sms - min(16, sms // 8))
         assert 0 <= p["split_row_blocks"] <= p["row_blocks"]
         if p["split_row_blocks"]:
             assert p["partial_bytes"] == 4 * 2 * p["grid"] * M * p["block_rows"]
@@ -309,7 +309,7 @@ def test_gemm_plan_grouped(w12):
                 continue
             assert g["row_blocks"] == sum(-(-n // g["block_rows"]) for n in Ns)
             assert g["k_steps"] == -(-K // 256)
-            assert 1 <= g["grid"] <= min(g["row_blocks"] * g["k_steps"], sms - (min(16, sms // 8) if M <= 2 else 0))
+            assert 1 <= g["grid"] <= min(g["row_blocks"] * g["k_steps"], sms - min(16, sms // 8))
             assert g["kernel"] == (1 if M <= 2 else 2)
             if len(Ns) == 1:
                 assert g == w12.w12_gemm_plan(M, Ns[0], K, sms)
