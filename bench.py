@@ -905,15 +905,22 @@ def run_case(cases):
     N, K = 17408, 5120
     wb = WL.projection_weights_torch(N, K, seed=5)
     d = w12.w12_upload(w12.w12_encode(wb.cpu().numpy().view(np.uint16)))
-    rows = {"fma": 1, "fma2": 2, "fma4": 4, "tc16": 16, "tc32": 32, "tc": 64, "tc128": 128, "q8": 64, "q8m1": 1}
+    dh = None
+    rows = {"fma": 1, "fma2": 2, "fma4": 4, "tc16": 16, "tc32": 32, "tc": 64, "tc128": 128, "q8": 64, "q8m1": 1,
+            "heavy16": 16}
     for case in cases.split(","):
         M = rows[case]
+        dm = d
+        if case == "heavy16":  # the heavy-tailed draw (about 1e-2 escapes)
+            if dh is None:
+                dh = w12.w12_upload(w12.w12_encode(WL.heavy_weights(N, K, seed=31)))
+            dm = dh
         x = torch.from_numpy(WL.activations(M, K, seed=1).view(np.int16)).cuda().view(torch.bfloat16)
         fn = w12.w12_gemm_q8view if case.startswith("q8") else w12.w12_gemm
         for _ in range(3):
-            y = fn(x, d)
+            y = fn(x, dm)
         torch.cuda.synchronize()
-        assert w12.w12_dev_status(d) == 0
+        assert w12.w12_dev_status(dm) == 0
         print(case, "ok", float(y.abs().sum()))
 
 
@@ -930,7 +937,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense BF16 (cuBLAS) comparison")
     ap.add_argument("--case", default=None,
-                    help="profiling cases, comma-separated: fma, fma2, fma4, tc16, tc32, tc (M=64), tc128, q8, q8m1")
+                    help="profiling cases, comma-separated: fma, fma2, fma4, tc16, tc32, tc (M=64), tc128, q8, q8m1, "
+                         "heavy16 (the heavy-tailed draw at M=16)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
