@@ -202,3 +202,25 @@ def test_grouped_host_buffers(w12, M):
     for W, Wd, y in zip(Ws, Wdec, yh):
         got = y.numpy().astype(np.float64)
         assert np.all(np.abs(got - O.gemm(x, Wd)) <= BOUND * O.abs_gemm(x, W)), f"M={M}"
+
+
+@pytest.mark.parametrize("M", (1, 2, 16, 32, 64))
+def test_grouped_gate_up_full_size(w12, M):
+    """The gate/up group of the benchmark layer at full size (two 17408x5120
+    matrices, one x, the launch the benchmark times), on sampled rows of each
+    matrix against the oracle (rows decode independently, so a sample's own
+    encoding decodes to the same rows)."""
+    K = 5120
+    Ws = [WL.projection_weights(17408, K, seed=s) for s in (61, 62)]
+    devs = [w12.w12_upload(w12.w12_encode(W)) for W in Ws]
+    x = WL.activations(M, K, seed=960 + M)
+    ys = w12.w12_gemm_grouped(_xdev(x), devs)
+    rng = np.random.Generator(np.random.PCG64(M))
+    for i, (W, y) in enumerate(zip(Ws, ys)):
+        rows = np.unique(np.concatenate([rng.choice(17408, size=96, replace=False), [0, 127, 128, 17407]]))
+        Wr = O.decode(O.encode(W[rows]))
+        assert np.array_equal(Wr, W[rows])
+        got = y.cpu().numpy().astype(np.float64)[:, rows]
+        assert np.all(np.abs(got - O.gemm(x, Wr)) <= BOUND * O.abs_gemm(x, Wr)), f"gate/up matrix {i} M={M}"
+    for d in devs:
+        assert w12.w12_dev_status(d) == 0
