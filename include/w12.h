@@ -352,9 +352,11 @@ w12_status w12_gemm_grouped(const void *x_bf16, const w12_dev *const *ws, void *
  * x_host [M][K] (BF16 bits) -> x_dev, runs w12_gemm_grouped into ys_dev, and
  * copies each ys_dev[i] -> ys_host[i] ([M][N_i], FP32 or, with
  * W12_GEMM_OUT_BF16, BF16), all on `stream` (pinned host memory makes the
- * copies asynchronous: synchronise the stream before reading ys_host).  Every
- * buffer is caller-owned; arguments, flags and errors as w12_gemm_grouped,
- * plus W12_ERR_INVALID_ARG for a missing host buffer.
+ * copies asynchronous: synchronise the stream before reading ys_host).
+ * Outputs that follow one another in memory both on the device and on the
+ * host go back in one transfer.  Every buffer is caller-owned; arguments,
+ * flags and errors as w12_gemm_grouped, plus W12_ERR_INVALID_ARG for a
+ * missing host buffer.
  */
 w12_status w12_gemm_grouped_host(const uint16_t *x_host, void *x_dev, const w12_dev *const *ws,
                                  void *const *ys_dev, void *const *ys_host, int n, int M, int K, unsigned flags,

@@ -614,11 +614,21 @@ w12_status w12_gemm_grouped_host(const uint16_t *x_host, void *x_dev, const w12_
     const w12_status s = w12_gemm_grouped(x_dev, ws, ys_dev, n, M, K, flags, stream);
     if (s != W12_OK)
         return s;
+    // outputs that lie end to end both on the device and on the host go
+    // back in one copy (a run of small copies costs a round trip each)
     const size_t elem = (flags & W12_GEMM_OUT_BF16) ? 2 : 4;
-    for (int i = 0; i < n; ++i) {
-        const size_t bytes = elem * static_cast<size_t>(M) * ws[i]->N;
-        if (bytes && (e = cudaMemcpyAsync(ys_host[i], ys_dev[i], bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    for (int i = 0; i < n;) {
+        char *dst = static_cast<char *>(ys_host[i]);
+        const char *src = static_cast<const char *>(ys_dev[i]);
+        size_t bytes = elem * static_cast<size_t>(M) * ws[i]->N;
+        int j = i + 1;
+        while (j < n && ys_host[j] == dst + bytes && ys_dev[j] == src + bytes) {
+            bytes += elem * static_cast<size_t>(M) * ws[j]->N;
+            ++j;
+        }
+        if (bytes && (e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
             return cuda_fail(e);
+        i = j;
     }
     return W12_OK;
 }

@@ -224,3 +224,31 @@ def test_grouped_gate_up_full_size(w12, M):
         assert np.all(np.abs(got - O.gemm(x, Wr)) <= BOUND * O.abs_gemm(x, Wr)), f"gate/up matrix {i} M={M}"
     for d in devs:
         assert w12.w12_dev_status(d) == 0
+
+
+def test_grouped_host_packed_outputs(w12):
+    """Outputs laid end to end on the device and on the host go back in one
+    transfer; the results are the same as with separate buffers.  (Every
+    output must start on a 16-byte boundary: M = 4 keeps the ragged row
+    counts' offsets aligned.)"""
+    import torch
+
+    Ws, Wdec, _, devs = _prepared(w12, "qkv_ragged_800")
+    M, K = 4, Ws[0].shape[1]
+    x = WL.activations(M, K, seed=997)
+    xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+    xd = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    n = sum(M * W.shape[0] for W in Ws)
+    yd_all = torch.empty(n, dtype=torch.float32, device="cuda")
+    yh_all = torch.full((n,), float("nan"), dtype=torch.float32).pin_memory()
+    yd, yh, off = [], [], 0
+    for W in Ws:
+        yd.append(yd_all[off:off + M * W.shape[0]].view(M, -1))
+        yh.append(yh_all[off:off + M * W.shape[0]].view(M, -1))
+        off += M * W.shape[0]
+    st = torch.cuda.current_stream()
+    w12.w12_gemm_grouped_host(xh, xd, devs, yd, yh, stream=st)
+    st.synchronize()
+    for W, Wd, y in zip(Ws, Wdec, yh):
+        got = y.numpy().astype(np.float64)
+        assert np.all(np.abs(got - O.gemm(x, Wd)) <= BOUND * O.abs_gemm(x, W))
