@@ -329,20 +329,35 @@ def run_w12(args):
     run_steps(args.warmup)
     torch.cuda.synchronize()
     check_status(layers)
+    # the step's duration, for sizing the load around the timed region
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    run_steps(50)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    per_step_s = max(1e-3 * p0.elapsed_time(p1) / 50, 1e-5)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # nvidia-smi samples every 100 ms: the same steps run untimed for ~0.4 s
+    # before the timed region and ~0.2 s after it, so that the clock samples
+    # are taken under this load
+    n_load = int(min(20000, max(1, 0.4 / per_step_s)))
     sampler = ClockSampler(local)
     with sampler:
-        time.sleep(0.25)
+        time.sleep(0.2)
+        run_steps(n_load)
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         t0.record(stream)
         run_steps(args.steps)
         t1.record(stream)
+        run_steps(n_load // 2)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
     clocks = sampler.stop()
+    clocks["note"] = ("sampled every 100 ms while the step ran untimed for ~0.4 s before and ~0.2 s after "
+                      "the timed region")
     steps_timed = args.steps
     ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * steps_timed, dist, "cuda")
     check_status(layers)
