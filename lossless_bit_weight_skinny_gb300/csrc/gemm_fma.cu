@@ -273,6 +273,12 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     constexpr int LOGV = (V >= 64) ? 6 : (V >= 32) ? 5 : (V >= 16) ? 4 : 3;
     constexpr int NE = S::NE;
     constexpr int WARP_P = CW, WARP_E = CW + 1; // producer, escape warps WARP_E .. WARP_E + NE - 1
+    // Weight units streamed ahead of the activation wait: one short of the
+    // ring, so that a CTA that starts while the previous kernel ends adds
+    // less traffic to that kernel's last loads (measured on GB300, the M = 1
+    // grouped layer: 99.4 us with the whole ring of 4, 98.5 with 3 or 2,
+    // 100.1 with 1)
+    constexpr int kPreUnits = STAGES > 1 ? STAGES - 1 : 1;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -339,12 +345,12 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
             const int row0 = (rb - mm.rb0) * RBLK, k0 = ks * 256; // rows of matrix g
             uint8_t *st = smem + s * L::STAGE;
             const uint32_t fb = full0 + 8 * s;
-            // The first ring's worth of weights streams before the previous
-            // kernel in the stream has finished; activations, which it may have
-            // written, only after it has -- unless the caller declared them
-            // complete before that kernel started.  (Writes wait for the
+            // The first kPreUnits units' weights stream before the previous
+            // kernel in the stream has finished; activations, which it may
+            // have written, only after it has -- unless the caller declared
+            // them complete before that kernel started.  (Writes wait for the
             // previous kernel in any case: see the row-block end.)
-            const int pre = a.x_ready ? 0 : (n_it < STAGES ? n_it : STAGES);
+            const int pre = a.x_ready ? 0 : (n_it < kPreUnits ? n_it : kPreUnits);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, L::TX_BYTES);
                 tma_load_2d(smem_u32(st + L::OFF_AE), &tm.ae[g], k0, row0, fb);
