@@ -311,11 +311,14 @@ def run_w12(args):
     step_bytes = _step_bytes(layers[0], M)
     n_launch_step = len(GROUPS)
 
-    # ---- headline: exactly --steps steps, launched one after another ----
-    # A plain host loop over the library's C entry points (argument lists
-    # built once), so that no graph boundary falls between two steps; the
-    # launches queue up ahead of the GPU (each takes a few microseconds to
-    # issue, each kernel runs 13-50).
+    # ---- headline: exactly --steps steps in one CUDA graph ----
+    # The steps' launches are captured once into a single graph (a decode
+    # loop's usual form: no host launch cost between kernels, and no graph
+    # boundary between two steps) and replayed once between CUDA events.  The
+    # untimed steps around it (warm-up, the clock-sample load) and a second
+    # timing for comparison run as a plain host loop over the library's C
+    # entry points (argument lists built once), whose launches queue up ahead
+    # of the GPU.
     lib = w12.lib()
     calls = [_layer_calls(lib, lay, xs, ys, M, stream) for lay in layers]
 
@@ -328,6 +331,9 @@ def run_w12(args):
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
+    check_status(layers)
+    # the timed graph: exactly --steps steps (one untimed replay on capture)
+    timed_graph = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), args.steps, warm=0)
     check_status(layers)
     # the step's duration, for sizing the load around the timed region
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -349,7 +355,7 @@ def run_w12(args):
             dist.barrier()
         torch.cuda.synchronize()
         t0.record(stream)
-        run_steps(args.steps)
+        timed_graph.replay()
         t1.record(stream)
         run_steps(n_load // 2)
         torch.cuda.synchronize()
@@ -362,6 +368,16 @@ def run_w12(args):
     ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * steps_timed, dist, "cuda")
     check_status(layers)
     us_layer = 1e3 * ms / steps_timed
+    del timed_graph
+    # the same steps as a host loop of stream launches (context)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run_steps(n_load // 4)
+    h0.record(stream)
+    run_steps(args.steps)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    check_status(layers)
+    us_layer_loop = 1e3 * h0.elapsed_time(h1) / args.steps
     # spread: the same steps as CUDA graphs of G steps, each replay between
     # its own events (after the timed region)
     G, n_rep = SIDE_G, 20
@@ -676,8 +692,8 @@ def run_w12(args):
                 "layers_rotated": nl,
                 "step": "the 7 GEMMs of one layer in 4 launches: q/k/v grouped (one launch), o, gate/up "
                         "grouped, down; each launch waits for the kernel before it",
-                "launch": "plain host loop over the C entry points (w12_gemm_grouped, w12_gemm_ex), "
-                          "no graph; CUDA events around exactly the requested steps",
+                "launch": "one CUDA graph holding exactly the requested steps (the library's grouped and "
+                          "single launches, captured once), replayed once between CUDA events on its stream",
                 "bytes_per_step": step_bytes,
                 "l2": "inputs larger than L2: each step streams ~0.5 GB of W12 weights, rotating over "
                       f"{nl} layers",
@@ -691,6 +707,9 @@ def run_w12(args):
             "roofline_by_M": roof_m,
             "by_M": by_m,
             "us_per_layer_by_launch_form": modes_us,
+            "us_per_layer_host_loop": {"us_per_layer": round(us_layer_loop, 2), "steps": args.steps,
+                                       "note": "the same steps as a plain host loop of stream launches over "
+                                               "the C entry points, after the timed region"},
             "row_sweep": sweep,
             "two_level_verification_17408x5120": tlv,
             "decode_step_64_layers": deep,
