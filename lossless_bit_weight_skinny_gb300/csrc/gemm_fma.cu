@@ -300,6 +300,16 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
     const int n_it = sk_begin(cta + 1, grid, a.total_iters) - it0;
     const int nk = a.n_kstep;
 
+    // the tensor maps' descriptors are fetched while the CTA sets up
+    if (warp == WARP_P) {
+        if (lane < a.n_mat) {
+            prefetch_tmap(&tm.ae[lane]);
+            if (!Q8)
+                prefetch_tmap(&tm.b[lane]);
+        }
+        if (lane == 0)
+            prefetch_tmap(&tm.x);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, Q8 ? 1 : 33);
@@ -326,13 +336,6 @@ __global__ void __maxnreg__(FmaShape<MT>::MAXREG)
 
     if (warp == WARP_P) {
         // ------------------------------ producer ------------------------------
-        if (lane < a.n_mat) {
-            prefetch_tmap(&tm.ae[lane]);
-            if (!Q8)
-                prefetch_tmap(&tm.b[lane]);
-        }
-        if (lane == 0)
-            prefetch_tmap(&tm.x);
         int issued = 0;
         int rb = it0 / nk, ks = it0 % nk, s = 0;
         uint32_t ph = 0;
