@@ -11,6 +11,9 @@ grouped launch, down alone; every launch waits for the kernel before it
 (its input is, in a decode step, that kernel's output or produced after it).
 Steps rotate over several independently drawn layers, each ~0.5 GB of W12
 data, so every step streams its weights from HBM (inputs larger than L2).
+The timed region is exactly --steps steps captured into one CUDA graph and
+replayed once between CUDA events; the same steps are also timed as a plain
+host loop of stream launches, for comparison.
 
 Prints one JSON line (rank 0).  `--impl reference` times the scalar CPU oracle
 on a bounded sample of the same workload instead.
