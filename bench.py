@@ -51,6 +51,7 @@ GROUPS = (("qkv", ("q", "k", "v"), 5120), ("o", ("o",), 5120), ("gate_up", ("gat
           ("down", ("down",), 17408))
 PROJ_GROUP = {p: g for g, ps, _ in GROUPS for p in ps}
 SIDE_G, SIDE_REPLAYS = 12, 10  # graph steps and replays of every leg besides the headline
+GRAPH_MAX_STEPS = 2400  # most steps captured into one graph for the headline
 
 
 def _peaks():
@@ -335,8 +336,13 @@ def run_w12(args):
     run_steps(args.warmup)
     torch.cuda.synchronize()
     check_status(layers)
-    # the timed graph: exactly --steps steps (one untimed replay on capture)
-    timed_graph = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), args.steps, warm=0)
+    # the timed graphs: exactly --steps steps (one untimed replay on capture);
+    # above GRAPH_MAX_STEPS a graph of that many steps is replayed as often as
+    # it fits and a second graph holds the rest (each graph starts the layer
+    # rotation afresh; GRAPH_MAX_STEPS is a multiple of the default 3 layers)
+    n_full, n_rest = divmod(args.steps, GRAPH_MAX_STEPS)
+    g_full = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), GRAPH_MAX_STEPS, warm=0) if n_full else None
+    g_rest = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), n_rest, warm=0) if n_rest else None
     check_status(layers)
     # the step's duration, for sizing the load around the timed region
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -358,7 +364,10 @@ def run_w12(args):
             dist.barrier()
         torch.cuda.synchronize()
         t0.record(stream)
-        timed_graph.replay()
+        for _ in range(n_full):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
         t1.record(stream)
         run_steps(n_load // 2)
         torch.cuda.synchronize()
@@ -371,7 +380,7 @@ def run_w12(args):
     ms, value = replica_aggregate(t0.elapsed_time(t1), step_bytes * steps_timed, dist, "cuda")
     check_status(layers)
     us_layer = 1e3 * ms / steps_timed
-    del timed_graph
+    del g_full, g_rest
     # the same steps as a host loop of stream launches (context)
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     run_steps(n_load // 4)
