@@ -363,6 +363,11 @@ def run_w12(args):
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
+        # a ~1 ms device-side wait keeps the stream busy while the host submits
+        # the graphs, so that the timed region opens with their first kernel
+        # rather than with the submission latency
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(2_000_000)
         t0.record(stream)
         for _ in range(n_full):
             g_full.replay()
