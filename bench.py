@@ -229,9 +229,12 @@ class Runner:
         return g
 
     def time_graph(self, g, reps):
-        """ms of `reps` back-to-back replays, CUDA events on the stream."""
+        """ms of `reps` back-to-back replays, CUDA events on the stream (a
+        device-side sleep ahead of the first event covers the submission)."""
         torch = self.torch
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(2_000_000)
         e0.record(self.stream)
         for _ in range(reps):
             g.replay()
@@ -400,6 +403,8 @@ def run_w12(args):
     G, n_rep = SIDE_G, 20
     graph = R.capture(lambda i: R.layer(layers[i % nl], xs, ys), G, warm=0)
     rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)  # covers the first replay's submission
     for e0, e1 in rev:
         e0.record(stream)
         graph.replay()
