@@ -107,11 +107,12 @@ constexpr int kPlSt = 2 * kGroups;               // escape-list stages (each ser
 #endif
 // Batches of 32 escape entries per patch round when a quadrant's list is
 // longer than a warp (32-row parking): measured on GB300 on 17408 x 5120 at
-// 16 rows with a dense escape tail (9e-3): 63.8 us with one batch a round,
-// 54.9 with 2, 51.2 with 4; on the projection draw at 32 rows, 31.3 us with
+// 16 rows with a dense escape tail (9e-3, ~74 entries a quadrant): 63.8 us
+// with one batch a round, 54.9 with 2, 51.1 with 4, 48.9 with 3 (the
+// projection draw 31.5 -> 30.9 us with 3 against 4); at 32 rows, 31.3 us with
 // 2 and 32.3 with 4.
 #ifndef W12_TC_PATCH_BATCHES16
-#define W12_TC_PATCH_BATCHES16 4
+#define W12_TC_PATCH_BATCHES16 3
 #endif
 #ifndef W12_TC_PATCH_BATCHES
 #define W12_TC_PATCH_BATCHES 2
