@@ -1006,6 +1006,10 @@ def main():
                     help="profiling cases, comma-separated: fma, fma2, fma4, tc16, tc32, tc (M=64), tc128, q8, q8m1, "
                          "heavy16 (the heavy-tailed draw at M=16)")
     args = ap.parse_args()
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    if args.layers < 1:
+        ap.error("--layers must be at least 1")
     if args.warmup < 3:
         args.warmup = 3
     if args.case:
